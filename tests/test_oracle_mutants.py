@@ -1,0 +1,183 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant patches one decision of the float64 oracle (on the CPU, inside this test
+only) with a plausible error -- a dropped term, an off-by-one bound, a wrong index map,
+a transposed operand -- and at least one pin of tests/test_oracle_pins.py or
+tests/test_oracle_equivalence.py has to fail under it.  This is what makes the pins
+worth trusting.
+"""
+
+import contextlib
+
+import numpy as np
+import pytest
+
+from oracle import ring_oracle as orc
+from tests import test_oracle_equivalence as eqv
+from tests import test_oracle_pins as pins
+
+
+def _rope_drop_term(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    half = x.shape[-1] // 2
+    ang = np.asarray(pos, np.float64)[..., None] * orc.rope_inv_freq(x.shape[-1], theta)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c, x1 * s + x2 * c], axis=-1)
+
+
+def _rope_gptj_pairs(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(pos, np.float64)[..., None] * orc.rope_inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * c - x2 * s
+    out[..., 1::2] = x1 * s + x2 * c
+    return out
+
+
+def _inv_freq_wrong_exponent(head_dim, theta):
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(np.float64(theta), -i / head_dim)
+
+
+def _to_f16_truncate(x):
+    x = np.asarray(x, np.float64).astype(np.float32)
+    bits = x.view(np.uint32) & np.uint32(0xFFFFE000)       # chop the low mantissa bits
+    return bits.view(np.float32).astype(np.float16)
+
+
+def _step_window_lo_off_by_one(committed, next_pos, cap):
+    win = min(committed, cap)
+    lo = committed - win + 1
+    start = max(next_pos, lo)
+    return win, lo, start, committed - start
+
+
+def _mask_full_shows_empty_slots(self):
+    # On a ring the window test can only reject never-written slots (every written slot
+    # already holds a position in [lo, c)), so the plausible slip is to skip it.
+    m = np.full((self.q_len, self.kv_total), orc.NEG_INF, np.float32)
+    m[:, :self.cap + self.q_len] = 0.0
+    return m
+
+
+def _mask_swa_uses_full_window(self):
+    c = self.committed
+    lo = c - min(c, self.cap)
+    m = np.full((self.q_len, self.kv_total), orc.NEG_INF, np.float32)
+    for s in range(self.cap):
+        if lo <= self.slot_pos[s] < c:
+            m[:, s] = 0.0
+    for i in range(self.q_len):
+        m[i, self.cap:self.cap + i + 1] = 0.0
+    return m
+
+
+def _mask_swa_not_causal(self):
+    c = self.committed
+    slo = orc.swa_low(c, self.cap, self.swa_window)
+    m = np.full((self.q_len, self.kv_total), orc.NEG_INF, np.float32)
+    for s in range(self.cap):
+        if slo <= self.slot_pos[s] < c:
+            m[:, s] = 0.0
+    m[:, self.cap:self.cap + self.q_len] = 0.0
+    return m
+
+
+def _write_noise_shifted(self, layer, k_noise, v_noise):
+    c = self.committed
+    for j in range(self.q_len):
+        kr = orc.rope_rows(k_noise[j], c + j + 1, self.n_head_kv, self.head_dim, self.theta)
+        self.k[layer, self.cap + j] = orc.to_f16(kr)
+        self.v[layer, self.cap + j] = v_noise[j]
+
+
+def _masked_attention_kv_swapped(q, k, v, mask, scale):
+    return _ORIG_MA(q, v, k, mask, scale)
+
+
+_ORIG_MA = orc.masked_attention
+_ORIG_BEGIN = orc.RingOracle.begin_step
+
+
+def _begin_step_no_pad_zero(self, committed, k_rows, v_rows, first_pos):
+    keep_k = self.k[:, self.trash_slot].copy()
+    keep_v = self.v[:, self.trash_slot].copy()
+    path = _ORIG_BEGIN(self, committed, k_rows, v_rows, first_pos)
+    self.k[:, self.trash_slot] = keep_k
+    self.v[:, self.trash_slot] = keep_v
+    return path
+
+
+MUTANTS = {
+    "slot map off by one": ("slot_of", lambda p, cap: (p + 1) % cap),
+    "lo off by one": ("step_window", _step_window_lo_off_by_one),
+    "mask_full shows empty slots": ("RingOracle.mask_full", _mask_full_shows_empty_slots),
+    "mask_swa ignores swa_window": ("RingOracle.mask_swa", _mask_swa_uses_full_window),
+    "mask_swa noise bidirectional": ("RingOracle.mask_swa", _mask_swa_not_causal),
+    "rope drops the x2*sin term": ("rope_neox", _rope_drop_term),
+    "rope pairs adjacent elements": ("rope_neox", _rope_gptj_pairs),
+    "rope exponent -i/d": ("rope_inv_freq", _inv_freq_wrong_exponent),
+    "softmax scale 1/d": ("softmax_scale", lambda d: 1.0 / d),
+    "kv head h % n_head_kv": ("kv_head_of", lambda h, group: h % 2),
+    "f16 by truncation": ("to_f16", _to_f16_truncate),
+    "noise keys one position late": ("RingOracle.write_noise", _write_noise_shifted),
+    "keys and values swapped": ("masked_attention", _masked_attention_kv_swapped),
+    "pad rows not zeroed": ("RingOracle.begin_step", _begin_step_no_pad_zero),
+}
+
+PINS = [
+    pins.test_geometry_matches_printed_values,
+    lambda: [pins.test_tiny_ring_hand_cases(c) for c in pins._golden("tiny_ring.json")["cases"]],
+    pins.test_slot_pos_brute_force_and_window_invariant,
+    pins.test_mask_counts_closed_form,
+    pins.test_empty_context_only_noise_visible,
+    pins.test_pad_rows_leave_trash_zero_and_untouched_slots,
+    pins.test_f16_round_to_nearest_even,
+    pins.test_rope_golden_values,
+    pins.test_rope_invariants,
+    lambda: pins.test_zero_query_gives_mean_of_visible_positions("full"),
+    lambda: pins.test_zero_query_gives_mean_of_visible_positions("swa"),
+    pins.test_single_visible_key_returns_its_value,
+    pins.test_softmax_scale_is_one_over_sqrt_head_dim,
+    pins.test_gqa_head_map,
+    pins.test_masked_attention_core_closed_form,
+    eqv.test_ring_equals_dense_window_tiny_workload,
+]
+
+
+@contextlib.contextmanager
+def _patched(target, repl):
+    if "." in target:
+        cls_name, attr = target.split(".")
+        owner = getattr(orc, cls_name)
+    else:
+        owner, attr = orc, target
+    orig = getattr(owner, attr)
+    setattr(owner, attr, repl)
+    try:
+        yield
+    finally:
+        setattr(owner, attr, orig)
+
+
+def test_unmutated_oracle_passes_every_pin():
+    for pin in PINS:
+        pin()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    target, repl = MUTANTS[name]
+    caught = []
+    with _patched(target, repl):
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                caught.append(pin)
+                break
+    assert caught, f"no pin caught the mutant '{name}'"
