@@ -1,0 +1,216 @@
+/*
+ * dflash_ring.h -- C ABI of the DFlash draft-KV ring step for one GB300 GPU (sm_103a).
+ *
+ * The draft model of DFlash block-diffusion speculative decoding keeps the K/V rows of
+ * its context in a fixed ring of `cap` slots instead of a cache that grows with the
+ * prompt.  Source: the page "DFLASH2_RING_PORT.md" (DFlash2 draft KV-ring port to
+ * llama.cpp), sections 1.1-1.7.  One step is
+ *
+ *   ring_begin_step   append the newly committed rows (slot = p % cap, RoPE at p),
+ *                     route fold-in pad rows to trash_slot, update slot_pos and
+ *                     build mask_full / mask_swa on the device          (sections 1.2-1.4)
+ *   ring_attend       per layer: write the noise block to slots cap..cap+q_len-1 and
+ *                     run masked GQA attention of the q_len noise queries over the
+ *                     kv_total slots                                       (sections 1.3-1.4)
+ *
+ * Conventions shared by every call
+ *   - Every function returns a status (RING_OK or a negative RING_E* code) and never
+ *     aborts.  ring_last_error() gives a one-line message for the last failure.
+ *   - Argument checks happen on the host before anything is launched; a call that
+ *     fails a check changes no state.
+ *   - "device pointer" means memory the GPU can read or write directly (cudaMalloc or a
+ *     PyTorch CUDA tensor); the caller owns it and keeps it alive until the work queued
+ *     on `stream` has finished.  The ring owns only what ring_init allocated.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls that take a stream only enqueue work and return without synchronising.
+ *     Issue all calls on one stream (or order the streams yourself): begin_step
+ *     rewrites per-step state that the previous step's attend kernels read.
+ *   - Read-back calls (ring_get_*) synchronise the device and copy to host memory.
+ *   - Layouts are row-major, innermost index last.  A K/V "row" is kv_row = head_dim *
+ *     n_head_kv F16 values, head-major (the page's [kv_row, kv_total] ggml tensor,
+ *     section 1.1).  F16 values travel as uint16_t bit patterns.
+ *   - Fast-path limits of this build: head_dim == 128 and (n_head / n_head_kv) * q_len
+ *     <= 32; other shapes are rejected with RING_EINVAL.
+ */
+#ifndef DFLASH_RING_H
+#define DFLASH_RING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dflash_ring ring_t;
+
+enum ring_status {
+    RING_OK = 0,
+    RING_EINVAL = -1,   /* a bad argument: dimension, kind, layer, sequence, NULL pointer   */
+    RING_ERANGE = -2,   /* committed went backwards, exceeds the position range, or the rows
+                           passed do not cover [start, committed)                        */
+    RING_ENOMEM = -3,   /* a device or pinned-host allocation failed                       */
+    RING_ECUDA = -4,    /* a CUDA runtime call failed (message in ring_last_error)         */
+    RING_ESTATE = -5,   /* call out of order, e.g. ring_attend before any ring_begin_step  */
+    RING_EDEVICE = -6   /* a kernel raised its device-side error flag (a bounded wait ran
+                           out); see ring_device_error                                    */
+};
+
+enum ring_mask_kind {
+    RING_MASK_FULL = 0, /* section 1.4 mask_full: window [lo, committed), noise bidirectional */
+    RING_MASK_SWA = 1   /* section 1.4 mask_swa: window [committed - min(swa_window, win),
+                           committed), noise causal within the block                      */
+};
+
+/* Extended construction parameters.  Zero in an optional field selects its default. */
+typedef struct ring_params {
+    int32_t cap;             /* ring capacity in context slots (section 1.1)                 */
+    int32_t q_len;           /* noise-block length = draft block size (section 1.1)          */
+    int32_t head_dim;        /* 128 in this build                                            */
+    int32_t n_head_kv;       /* K/V heads                                                    */
+    int32_t n_head;          /* query heads, a multiple of n_head_kv (GQA)                   */
+    int32_t n_layer;         /* draft layers sharing the slot map                            */
+    float rope_theta;        /* RoPE base; NeoX pairing (i, i + head_dim/2)                  */
+    int32_t n_seq;           /* independent rings (sequences); default 1                     */
+    int32_t swa_window;      /* SWA window for RING_MASK_SWA; 0 = no SWA mask                */
+    int32_t bulk_chunk;      /* rows per bulk-append chunk; default 1024 (section 1.3)       */
+    int32_t tiles_per_split; /* attention split length in 64-slot tiles; 0 = chosen from the
+                                SM count                                                     */
+} ring_params;
+
+/* Geometry and sizes of an initialised ring (all counts, no pointers). */
+typedef struct ring_geometry {
+    int32_t cap, q_len, a_step, trash_slot, kv_total, kv_row;
+    int32_t head_dim, n_head_kv, n_head, n_layer, n_seq, swa_window, bulk_chunk;
+    int32_t tile_slots;      /* slots per attention tile (64)                                */
+    int32_t n_tiles;         /* ceil(kv_total / tile_slots)                                  */
+    int32_t tiles_per_split; /* tiles streamed by one attention CTA                          */
+    int32_t n_splits;        /* CTAs per (sequence, kv head)                                 */
+    int64_t cache_bytes;     /* F16 K+V of one sequence: 2 * n_layer * kv_row * kv_total * 2
+                                (section 1.7)                                                */
+    int64_t device_bytes;    /* everything ring_init allocated on the device                 */
+} ring_geometry;
+
+/* Per-kernel timing collected while profiling is on (CUDA events on the launch stream). */
+typedef struct ring_profile {
+    int64_t launches[5];     /* 0 append (fold-in + bulk), 1 mask build, 2 attend prologue,
+                                3 split-KV attention, 4 split combine                       */
+    double total_ms[5];      /* summed event time per kernel class                          */
+} ring_profile;
+
+/*
+ * ring_init -- allocate one ring (n_seq = 1, no SWA) on the current CUDA device.
+ * Section 1.1: a_step = 2*q_len + 2, trash_slot = cap + q_len,
+ * kv_total = align_up(cap + q_len + 1, 32), kv_row = head_dim * n_head_kv; separate F16
+ * K and V tensors per layer, zeroed once; slot_pos[] = -1; next position 0.
+ * *out receives the handle (NULL on failure).  Errors: EINVAL, ENOMEM, ECUDA.
+ */
+int ring_init(ring_t **out, int32_t cap, int32_t q_len, int32_t head_dim, int32_t n_head_kv,
+              int32_t n_head, int32_t n_layer, float rope_theta);
+
+/* ring_init_ex -- as ring_init with n_seq rings, an SWA window, bulk chunk and split size. */
+int ring_init_ex(ring_t **out, const ring_params *params);
+
+/* ring_destroy -- synchronise the device, free everything the ring owns.  NULL is a no-op. */
+int ring_destroy(ring_t *r);
+
+/* ring_get_geometry -- fill *g.  Errors: EINVAL (NULL). */
+int ring_get_geometry(const ring_t *r, ring_geometry *g);
+
+/*
+ * ring_rows_needed -- section 1.3 window arithmetic for sequence `seq` if `committed`
+ * were passed to the next begin_step: win = min(c, cap), lo = c - win,
+ * start = max(next_pos, lo), n_new = c - start.  Tells a caller which rows to produce.
+ * Errors: EINVAL, ERANGE (committed below the ring's next position).
+ */
+int ring_rows_needed(const ring_t *r, int32_t seq, int64_t committed, int64_t *start,
+                     int32_t *n_new);
+
+/*
+ * ring_begin_step -- sections 1.2-1.4 for every sequence, enqueued on `stream`.
+ *
+ *   committed  host int64[n_seq]: tokens committed so far per sequence; never decreases.
+ *   k_rows     device F16 [n_layer][n_rows][kv_row]: pre-RoPE context K rows.
+ *   v_rows     device F16 [n_layer][n_rows][kv_row]: context V rows.
+ *   row_off    host int64[n_seq]: row (within n_rows) holding position first_pos[s].
+ *   first_pos  host int64[n_seq]: position of that row; rows of sequence s cover
+ *              [first_pos[s], committed[s]) contiguously.
+ *   n_rows     rows per layer in k_rows / v_rows (the layer stride).
+ *
+ * For each sequence with n_new rows to append (see ring_rows_needed): when
+ * n_new <= a_step the fold-in path writes a_step rows -- the n_new real rows to slot
+ * p % cap with RoPE at p, and the rest as pad rows of zeros to trash_slot; otherwise
+ * the bulk path appends all n_new rows in chunks of bulk_chunk rows.  slot_pos[p % cap]
+ * = p.  Then mask_full (and mask_swa when swa_window > 0) and their per-tile flags are
+ * rebuilt from slot_pos on the device.  Rows below `start` are ignored; k_rows/v_rows
+ * may be NULL when no sequence appends.  Positions must stay below 2^31 - q_len.
+ * Errors: EINVAL, ERANGE (state unchanged), ECUDA.
+ */
+int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows,
+                    const void *v_rows, const int64_t *row_off, const int64_t *first_pos,
+                    int64_t n_rows, void *stream);
+
+/*
+ * ring_attend -- one draft layer's masked attention, enqueued on `stream`.
+ *
+ *   q        device F32 [n_seq][q_len][n_head][head_dim]: pre-RoPE noise-block queries.
+ *   k_noise  device F16 [n_seq][q_len][kv_row]: pre-RoPE noise-block K rows.
+ *   v_noise  device F16 [n_seq][q_len][kv_row]: noise-block V rows.
+ *   o        device F32 [n_seq][q_len][n_head][head_dim]: output (overwritten).
+ *
+ * Noise row j is stored in slot cap + j of this layer with RoPE at committed + j; query
+ * i is rotated to committed + i (section 1.3).  Then, per query head h (kv head
+ * h / (n_head / n_head_kv)) and row i:
+ *   o[i,h] = sum_s softmax_s(q_i . k_s / sqrt(head_dim) + mask[i,s]) v_s,
+ * over the kv_total slots with the mask of `mask_kind` built by the last begin_step
+ * (section 1.4).  Computed by a split-KV flash-decode kernel (F16 tensor-core products,
+ * F32 softmax and accumulation) that skips slot tiles with no visible slot.
+ * Errors: EINVAL (layer, kind, NULL, SWA without a window), ESTATE (no begin_step yet),
+ * ECUDA.
+ */
+int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q,
+                const void *k_noise, const void *v_noise, float *o, void *stream);
+
+/* ring_get_slot_pos -- host int32[cap] of sequence `seq` (-1 = never written).  Syncs. */
+int ring_get_slot_pos(ring_t *r, int32_t seq, int32_t *out);
+
+/* ring_get_mask -- host F32 [q_len][kv_total] (0 or -inf) of the last begin_step.  Syncs. */
+int ring_get_mask(ring_t *r, int32_t seq, int32_t mask_kind, float *out);
+
+/* ring_get_tile_flags -- host uint8[n_tiles]: 0 = no visible slot, 1 = every slot visible
+ * to every row, 2 = mixed.  Syncs. */
+int ring_get_tile_flags(ring_t *r, int32_t seq, int32_t mask_kind, uint8_t *out);
+
+/* ring_get_kv -- host F16 bits [kv_total][kv_row] of K and V of (seq, layer), in the
+ * page's row layout (either pointer may be NULL).  Syncs. */
+int ring_get_kv(ring_t *r, int32_t seq, int32_t layer, uint16_t *k, uint16_t *v);
+
+/* ring_device_error -- synchronise, read and clear the device-side error word.  Returns
+ * RING_OK, or RING_EDEVICE with the word's bits stored in *bits (may be NULL). */
+int ring_device_error(ring_t *r, uint32_t *bits);
+
+/* ring_describe -- the geometry line the Luce server logs (section 11, Test 4), e.g.
+ * "[draft-kv] ctx-KV ring active: cap=4096 kv_total=4128 a_step=18 layers=5 f16 cache
+ * 80.6 MiB", written NUL-terminated into buf[len]. */
+int ring_describe(const ring_t *r, char *buf, size_t len);
+
+/* ring_profile_enable -- on != 0 starts recording CUDA events around every kernel the ring
+ * launches (not allowed while a stream capture is in progress); 0 stops. */
+int ring_profile_enable(ring_t *r, int32_t on);
+
+/* ring_profile_read -- synchronise on the recorded events, add them into *out (which the
+ * caller zeroes first) and forget them. */
+int ring_profile_read(ring_t *r, ring_profile *out);
+
+/* ring_launch_count -- kernels this ring has launched since ring_init. */
+int64_t ring_launch_count(const ring_t *r);
+
+/* ring_last_error -- message of the last failing call on r (or of the last failed
+ * ring_init when r is NULL).  Never NULL. */
+const char *ring_last_error(const ring_t *r);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_RING_H */

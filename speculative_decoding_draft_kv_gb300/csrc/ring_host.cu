@@ -1,0 +1,589 @@
+// Host side of the C ABI declared in include/dflash_ring.h.
+//
+// Owns the ring's device buffers (allocated and zeroed once, like the persistent buffer
+// of the page "DFLASH2_RING_PORT.md", section 1.1), validates every argument before
+// launching anything, performs the per-sequence window arithmetic of section 1.3 on the
+// host (it needs only integers the caller already holds), stages those few bytes to the
+// device through pinned memory and enqueues the kernels.  Nothing here blocks on the GPU
+// except the read-back calls, destroy, and the rare reuse of a still-busy staging slot.
+#include "dflash_ring.h"
+#include "ring_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace dflash;
+
+namespace {
+
+constexpr int kStagingSlots = 8;
+constexpr int kKinds = 5;
+
+struct EventRec {
+    int cls;
+    cudaEvent_t a, b;
+};
+
+thread_local std::string g_init_error = "no error";
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+struct dflash_ring {
+    RingDims d{};
+    RingDev m{};
+    float rope_theta = 0.f;
+    float scale_log2 = 0.f;
+    int device = 0;
+    std::vector<int64_t> next_pos, committed;
+    bool have_step = false;
+    CUtensorMap tm_k{}, tm_v{};
+    SeqStep *h_steps = nullptr;            // pinned [kStagingSlots][n_seq]
+    cudaEvent_t slot_ev[kStagingSlots] = {};
+    bool slot_used[kStagingSlots] = {};
+    int slot_next = 0;
+    int64_t launches = 0;
+    int64_t device_bytes = 0;
+    bool profiling = false;
+    std::vector<EventRec> recs;
+    std::vector<cudaEvent_t> ev_pool;
+    std::string err = "no error";
+    std::vector<void *> allocs;
+};
+
+namespace {
+
+int fail(ring_t *r, int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (r)
+        r->err = buf;
+    else
+        g_init_error = buf;
+    return code;
+}
+
+int cuda_fail(ring_t *r, cudaError_t e, const char *what) {
+    return fail(r, e == cudaErrorMemoryAllocation ? RING_ENOMEM : RING_ECUDA, "%s: %s", what,
+                cudaGetErrorString(e));
+}
+
+cudaEvent_t pool_event(ring_t *r) {
+    if (!r->ev_pool.empty()) {
+        cudaEvent_t e = r->ev_pool.back();
+        r->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Launch wrapper: counts the launch and, while profiling, brackets it with events.
+template <typename F>
+cudaError_t timed(ring_t *r, int cls, cudaStream_t st, F &&launch) {
+    EventRec rec{cls, nullptr, nullptr};
+    if (r->profiling) {
+        rec.a = pool_event(r);
+        rec.b = pool_event(r);
+        cudaEventRecord(rec.a, st);
+    }
+    cudaError_t e = launch();
+    if (r->profiling) {
+        cudaEventRecord(rec.b, st);
+        r->recs.push_back(rec);
+    }
+    if (e == cudaSuccess) ++r->launches;
+    return e;
+}
+
+void *dalloc(ring_t *r, size_t bytes, cudaError_t *err) {
+    void *p = nullptr;
+    *err = cudaMalloc(&p, bytes);
+    if (*err != cudaSuccess) return nullptr;
+    r->allocs.push_back(p);
+    r->device_bytes += (int64_t)bytes;
+    return p;
+}
+
+void release(ring_t *r) {
+    if (!r) return;
+    cudaDeviceSynchronize();
+    for (void *p : r->allocs) cudaFree(p);
+    r->allocs.clear();
+    if (r->h_steps) cudaFreeHost(r->h_steps);
+    for (auto &e : r->slot_ev)
+        if (e) cudaEventDestroy(e);
+    for (auto &rec : r->recs) {
+        cudaEventDestroy(rec.a);
+        cudaEventDestroy(rec.b);
+    }
+    for (auto e : r->ev_pool) cudaEventDestroy(e);
+    delete r;
+}
+
+bool encode_kv_map(CUtensorMap *tm, void *base, const RingDims &d) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    // dims (innermost first): head_dim, kv_total slots, (seq, layer, kv head) planes
+    cuuint64_t dims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.kv_total,
+                          (cuuint64_t)d.n_seq * d.n_layer * d.n_head_kv};
+    cuuint64_t strides[2] = {(cuuint64_t)d.head_dim * 2, (cuuint64_t)d.kv_total * d.head_dim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+int auto_tiles_per_split(const RingDims &d, int sms) {
+    // Aim for about four waves of two resident CTAs per SM, but never fewer than 2 or
+    // more than 64 tiles per CTA (the partial write is 16 KiB per CTA).
+    const int64_t work = (int64_t)d.n_seq * d.n_head_kv * d.n_tiles;
+    const int64_t target = (int64_t)sms * 2 * 4;
+    int64_t tps = (work + target - 1) / target;
+    tps = std::max<int64_t>(2, std::min<int64_t>(64, tps));
+    return (int)std::min<int64_t>(tps, d.n_tiles);
+}
+
+bool check_seq(ring_t *r, int32_t seq) { return r && seq >= 0 && seq < r->d.n_seq; }
+
+}  // namespace
+
+extern "C" {
+
+int ring_init(ring_t **out, int32_t cap, int32_t q_len, int32_t head_dim, int32_t n_head_kv,
+              int32_t n_head, int32_t n_layer, float rope_theta) {
+    ring_params p{};
+    p.cap = cap;
+    p.q_len = q_len;
+    p.head_dim = head_dim;
+    p.n_head_kv = n_head_kv;
+    p.n_head = n_head;
+    p.n_layer = n_layer;
+    p.rope_theta = rope_theta;
+    p.n_seq = 1;
+    return ring_init_ex(out, &p);
+}
+
+int ring_init_ex(ring_t **out, const ring_params *p) {
+    if (!out) return fail(nullptr, RING_EINVAL, "ring_init: out is NULL");
+    *out = nullptr;
+    if (!p) return fail(nullptr, RING_EINVAL, "ring_init: params is NULL");
+    const int n_seq = p->n_seq > 0 ? p->n_seq : 1;
+    if (p->cap <= 0 || p->q_len <= 0 || p->head_dim <= 0 || p->n_head_kv <= 0 ||
+        p->n_head <= 0 || p->n_layer <= 0 || p->swa_window < 0 || p->bulk_chunk < 0 ||
+        p->tiles_per_split < 0 || !(p->rope_theta > 0.f))
+        return fail(nullptr, RING_EINVAL, "ring_init: every dimension must be positive");
+    if (p->n_head % p->n_head_kv)
+        return fail(nullptr, RING_EINVAL, "ring_init: n_head %d not a multiple of n_head_kv %d",
+                    p->n_head, p->n_head_kv);
+    if (p->head_dim != kHeadDim)
+        return fail(nullptr, RING_EINVAL, "ring_init: head_dim %d unsupported (needs %d)",
+                    p->head_dim, kHeadDim);
+    const int group = p->n_head / p->n_head_kv;
+    if ((int64_t)group * p->q_len > kRows)
+        return fail(nullptr, RING_EINVAL,
+                    "ring_init: (n_head/n_head_kv)*q_len = %d exceeds %d query rows per kv head",
+                    group * p->q_len, kRows);
+    if ((int64_t)p->cap + p->q_len + 32 > (int64_t)INT32_MAX / 2)
+        return fail(nullptr, RING_EINVAL, "ring_init: cap too large");
+
+    ring_t *r = new dflash_ring();
+    RingDims &d = r->d;
+    d.cap = p->cap;
+    d.q_len = p->q_len;
+    d.head_dim = p->head_dim;
+    d.n_head_kv = p->n_head_kv;
+    d.n_head = p->n_head;
+    d.n_layer = p->n_layer;
+    d.n_seq = n_seq;
+    d.swa_window = p->swa_window;
+    d.a_step = 2 * p->q_len + 2;                       // section 1.1
+    d.trash_slot = p->cap + p->q_len;
+    d.kv_total = (p->cap + p->q_len + 1 + 31) / 32 * 32;
+    d.kv_row = p->head_dim * p->n_head_kv;
+    d.group = group;
+    d.rows = group * p->q_len;
+    d.n_tiles = (d.kv_total + kTile - 1) / kTile;
+    d.n_kinds = p->swa_window > 0 ? 2 : 1;
+    d.bulk_chunk = p->bulk_chunk > 0 ? p->bulk_chunk : 1024;
+    r->rope_theta = p->rope_theta;
+    r->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+
+    cudaError_t e = cudaGetDevice(&r->device);
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(nullptr, e, "ring_init: cudaGetDevice");
+        delete r;
+        return rc;
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, r->device);
+    d.tiles_per_split = p->tiles_per_split > 0 ? std::min(p->tiles_per_split, d.n_tiles)
+                                               : auto_tiles_per_split(d, std::max(sms, 1));
+    d.n_splits = (d.n_tiles + d.tiles_per_split - 1) / d.tiles_per_split;
+
+    const size_t kv_elems = (size_t)d.n_seq * d.n_layer * d.n_head_kv * d.kv_total * d.head_dim;
+    RingDev &m = r->m;
+#define ALLOC(ptr, type, count)                                                  \
+    do {                                                                         \
+        ptr = static_cast<type *>(dalloc(r, sizeof(type) * (size_t)(count), &e)); \
+        if (!ptr) {                                                              \
+            int rc = cuda_fail(nullptr, e, "ring_init: cudaMalloc " #ptr);       \
+            release(r);                                                          \
+            return rc;                                                           \
+        }                                                                        \
+    } while (0)
+    ALLOC(m.k, uint16_t, kv_elems);
+    ALLOC(m.v, uint16_t, kv_elems);
+    ALLOC(m.slot_pos, int32_t, (size_t)d.n_seq * d.cap);
+    ALLOC(m.mask, float, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total);
+    ALLOC(m.flags, uint8_t, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
+    ALLOC(m.steps, SeqStep, d.n_seq);
+    ALLOC(m.q16, uint16_t, (size_t)d.n_seq * d.n_head_kv * kRows * kHeadDim);
+    ALLOC(m.part_acc, float, (size_t)d.n_seq * d.n_head_kv * d.n_splits * kRows * kHeadDim);
+    ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.n_splits * kRows);
+    ALLOC(m.err, uint32_t, 1);
+    ALLOC(m.inv_freq, double, d.head_dim / 2);
+#undef ALLOC
+
+    // zeroed once (section 1.1); slot_pos = -1; masks start fully masked
+    cudaError_t z = cudaSuccess;
+    auto zero = [&](void *ptr, int val, size_t bytes) {
+        if (z == cudaSuccess) z = cudaMemset(ptr, val, bytes);
+    };
+    zero(m.k, 0, kv_elems * 2);
+    zero(m.v, 0, kv_elems * 2);
+    zero(m.slot_pos, 0xff, (size_t)d.n_seq * d.cap * 4);
+    zero(m.mask, 0, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total * 4);
+    zero(m.flags, 0, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
+    zero(m.steps, 0, sizeof(SeqStep) * d.n_seq);
+    zero(m.q16, 0, (size_t)d.n_seq * d.n_head_kv * kRows * kHeadDim * 2);
+    zero(m.err, 0, 4);
+    std::vector<double> inv(d.head_dim / 2);
+    for (int i = 0; i < d.head_dim / 2; ++i)
+        inv[i] = std::pow((double)p->rope_theta, -2.0 * i / d.head_dim);
+    if (z == cudaSuccess)
+        z = cudaMemcpy(m.inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+    if (z == cudaSuccess) z = cudaDeviceSynchronize();
+    if (z != cudaSuccess) {
+        int rc = cuda_fail(nullptr, z, "ring_init: initialising buffers");
+        release(r);
+        return rc;
+    }
+    e = cudaMallocHost(reinterpret_cast<void **>(&r->h_steps), sizeof(SeqStep) * kStagingSlots * d.n_seq);
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(nullptr, e, "ring_init: cudaMallocHost");
+        r->h_steps = nullptr;
+        release(r);
+        return rc;
+    }
+    for (auto &ev : r->slot_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (!encode_kv_map(&r->tm_k, m.k, d) || !encode_kv_map(&r->tm_v, m.v, d)) {
+        int rc = fail(nullptr, RING_ECUDA, "ring_init: cuTensorMapEncodeTiled failed");
+        release(r);
+        return rc;
+    }
+    e = attend_kernels_init();
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(nullptr, e, "ring_init: kernel attributes");
+        release(r);
+        return rc;
+    }
+    r->next_pos.assign(d.n_seq, 0);
+    r->committed.assign(d.n_seq, 0);
+    *out = r;
+    return RING_OK;
+}
+
+int ring_destroy(ring_t *r) {
+    release(r);
+    return RING_OK;
+}
+
+int ring_get_geometry(const ring_t *r, ring_geometry *g) {
+    if (!r || !g) return RING_EINVAL;
+    const RingDims &d = r->d;
+    g->cap = d.cap;
+    g->q_len = d.q_len;
+    g->a_step = d.a_step;
+    g->trash_slot = d.trash_slot;
+    g->kv_total = d.kv_total;
+    g->kv_row = d.kv_row;
+    g->head_dim = d.head_dim;
+    g->n_head_kv = d.n_head_kv;
+    g->n_head = d.n_head;
+    g->n_layer = d.n_layer;
+    g->n_seq = d.n_seq;
+    g->swa_window = d.swa_window;
+    g->bulk_chunk = d.bulk_chunk;
+    g->tile_slots = kTile;
+    g->n_tiles = d.n_tiles;
+    g->tiles_per_split = d.tiles_per_split;
+    g->n_splits = d.n_splits;
+    g->cache_bytes = 2LL * d.n_layer * d.kv_row * d.kv_total * 2;
+    g->device_bytes = r->device_bytes;
+    return RING_OK;
+}
+
+int ring_rows_needed(const ring_t *r, int32_t seq, int64_t committed, int64_t *start,
+                     int32_t *n_new) {
+    if (!r || seq < 0 || seq >= r->d.n_seq) return RING_EINVAL;
+    const int64_t c = committed, np = r->next_pos[seq];
+    if (c < np || c < 0) return RING_ERANGE;
+    const int64_t win = std::min<int64_t>(c, r->d.cap);    // section 1.3
+    const int64_t lo = c - win;
+    const int64_t st = std::max(np, lo);
+    if (start) *start = st;
+    if (n_new) *n_new = (int32_t)(c - st);
+    return RING_OK;
+}
+
+int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
+                    const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                    void *stream) {
+    if (!r) return RING_EINVAL;
+    if (!committed) return fail(r, RING_EINVAL, "ring_begin_step: committed is NULL");
+    const RingDims &d = r->d;
+    const int64_t pos_limit = (int64_t)INT32_MAX - d.q_len - 1;
+    std::vector<SeqStep> st(d.n_seq);
+    int64_t max_bulk = 0;
+    bool any_rows = false;
+    for (int s = 0; s < d.n_seq; ++s) {
+        const int64_t c = committed[s];
+        if (c < 0 || c > pos_limit)
+            return fail(r, RING_ERANGE, "ring_begin_step: committed[%d] = %lld out of range", s,
+                        (long long)c);
+        if (c < r->next_pos[s])
+            return fail(r, RING_ERANGE,
+                        "ring_begin_step: committed[%d] = %lld went below %lld", s,
+                        (long long)c, (long long)r->next_pos[s]);
+        const int64_t win = std::min<int64_t>(c, d.cap);
+        const int64_t lo = c - win;
+        const int64_t start = std::max(r->next_pos[s], lo);
+        const int64_t n_new = c - start;
+        SeqStep &x = st[s];
+        x.committed = c;
+        x.lo = lo;
+        x.swa_lo = d.swa_window > 0 ? c - std::min<int64_t>(d.swa_window, win) : lo;
+        x.start = start;
+        x.n_new = (int32_t)n_new;
+        x.fold_rows = n_new <= d.a_step ? (int32_t)n_new : 0;
+        x.src_row = 0;
+        if (n_new > 0) {
+            any_rows = true;
+            if (!row_off || !first_pos)
+                return fail(r, RING_EINVAL, "ring_begin_step: row_off/first_pos are NULL");
+            if (first_pos[s] > start || first_pos[s] < 0)
+                return fail(r, RING_ERANGE,
+                            "ring_begin_step: rows of seq %d start at %lld, after start %lld", s,
+                            (long long)first_pos[s], (long long)start);
+            if (row_off[s] < 0 || row_off[s] + (c - first_pos[s]) > n_rows)
+                return fail(r, RING_ERANGE,
+                            "ring_begin_step: rows of seq %d run past n_rows %lld", s,
+                            (long long)n_rows);
+            x.src_row = row_off[s] + (start - first_pos[s]);
+            if (n_new > d.a_step) max_bulk = std::max(max_bulk, n_new);
+        }
+    }
+    if (any_rows) {
+        if (!k_rows || !v_rows) return fail(r, RING_EINVAL, "ring_begin_step: rows are NULL");
+        if ((reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows)) & 15)
+            return fail(r, RING_EINVAL, "ring_begin_step: rows must be 16-byte aligned");
+    }
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int slot = r->slot_next;
+    r->slot_next = (slot + 1) % kStagingSlots;
+    if (r->slot_used[slot]) {
+        cudaError_t e = cudaEventSynchronize(r->slot_ev[slot]);
+        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: staging event");
+    }
+    SeqStep *h = r->h_steps + (size_t)slot * d.n_seq;
+    std::memcpy(h, st.data(), sizeof(SeqStep) * d.n_seq);
+    cudaError_t e = cudaMemcpyAsync(r->m.steps, h, sizeof(SeqStep) * d.n_seq,
+                                    cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: staging copy");
+    cudaEventRecord(r->slot_ev[slot], cs);
+    r->slot_used[slot] = true;
+
+    const auto *kr = static_cast<const uint16_t *>(k_rows);
+    const auto *vr = static_cast<const uint16_t *>(v_rows);
+    e = timed(r, 0, cs, [&] { return launch_fold_append(d, r->m, kr, vr, n_rows, cs); });
+    const int n_chunks = (int)((max_bulk + d.bulk_chunk - 1) / d.bulk_chunk);
+    for (int c = 0; c < n_chunks && e == cudaSuccess; ++c)
+        e = timed(r, 0, cs, [&] { return launch_bulk_append(d, r->m, kr, vr, n_rows, c, cs); });
+    if (e == cudaSuccess) e = timed(r, 1, cs, [&] { return launch_build_mask(d, r->m, cs); });
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
+    for (int s = 0; s < d.n_seq; ++s) {
+        r->next_pos[s] = committed[s];
+        r->committed[s] = committed[s];
+    }
+    r->have_step = true;
+    return RING_OK;
+}
+
+int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q, const void *k_noise,
+                const void *v_noise, float *o, void *stream) {
+    if (!r) return RING_EINVAL;
+    const RingDims &d = r->d;
+    if (layer < 0 || layer >= d.n_layer)
+        return fail(r, RING_EINVAL, "ring_attend: layer %d out of range", layer);
+    if (mask_kind != RING_MASK_FULL && mask_kind != RING_MASK_SWA)
+        return fail(r, RING_EINVAL, "ring_attend: unknown mask kind %d", mask_kind);
+    if (mask_kind == RING_MASK_SWA && d.n_kinds < 2)
+        return fail(r, RING_EINVAL, "ring_attend: SWA mask needs swa_window > 0 at init");
+    if (!q || !k_noise || !v_noise || !o)
+        return fail(r, RING_EINVAL, "ring_attend: NULL input or output");
+    if ((reinterpret_cast<uintptr_t>(k_noise) | reinterpret_cast<uintptr_t>(v_noise) |
+         reinterpret_cast<uintptr_t>(o)) & 15)
+        return fail(r, RING_EINVAL, "ring_attend: noise rows and output must be 16-byte aligned");
+    if (!r->have_step) return fail(r, RING_ESTATE, "ring_attend: no ring_begin_step yet");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const auto *kn = static_cast<const uint16_t *>(k_noise);
+    const auto *vn = static_cast<const uint16_t *>(v_noise);
+    cudaError_t e = timed(r, 2, cs, [&] {
+        return launch_attend_prologue(d, r->m, layer, q, kn, vn, cs);
+    });
+    if (e == cudaSuccess)
+        e = timed(r, 3, cs, [&] {
+            return launch_attend_split(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind,
+                                       r->scale_log2, o, cs);
+        });
+    if (e == cudaSuccess && d.n_splits > 1)
+        e = timed(r, 4, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_attend: launch");
+    return RING_OK;
+}
+
+int ring_get_slot_pos(ring_t *r, int32_t seq, int32_t *out) {
+    if (!check_seq(r, seq) || !out) return RING_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(out, r->m.slot_pos + (size_t)seq * r->d.cap, sizeof(int32_t) * r->d.cap,
+                       cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? RING_OK : cuda_fail(r, e, "ring_get_slot_pos");
+}
+
+int ring_get_mask(ring_t *r, int32_t seq, int32_t mask_kind, float *out) {
+    if (!check_seq(r, seq) || !out || mask_kind < 0 || mask_kind >= r->d.n_kinds)
+        return RING_EINVAL;
+    const RingDims &d = r->d;
+    const size_t n = (size_t)d.q_len * d.kv_total;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(out, r->m.mask + ((size_t)seq * d.n_kinds + mask_kind) * n, n * sizeof(float),
+                       cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? RING_OK : cuda_fail(r, e, "ring_get_mask");
+}
+
+int ring_get_tile_flags(ring_t *r, int32_t seq, int32_t mask_kind, uint8_t *out) {
+    if (!check_seq(r, seq) || !out || mask_kind < 0 || mask_kind >= r->d.n_kinds)
+        return RING_EINVAL;
+    const RingDims &d = r->d;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(out, r->m.flags + ((size_t)seq * d.n_kinds + mask_kind) * d.n_tiles,
+                       d.n_tiles, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? RING_OK : cuda_fail(r, e, "ring_get_tile_flags");
+}
+
+int ring_get_kv(ring_t *r, int32_t seq, int32_t layer, uint16_t *k, uint16_t *v) {
+    if (!check_seq(r, seq) || layer < 0 || layer >= r->d.n_layer) return RING_EINVAL;
+    const RingDims &d = r->d;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_get_kv");
+    // device [kv head][slot][head_dim] -> host [slot][kv head * head_dim]
+    const size_t head_elems = (size_t)d.kv_total * d.head_dim;
+    for (int t = 0; t < 2; ++t) {
+        uint16_t *dst = t == 0 ? k : v;
+        if (!dst) continue;
+        const uint16_t *src = (t == 0 ? r->m.k : r->m.v) +
+                              ((size_t)seq * d.n_layer + layer) * d.n_head_kv * head_elems;
+        e = cudaMemcpy2D(dst, (size_t)d.kv_row * 2, src, (size_t)d.head_dim * 2,
+                         (size_t)d.head_dim * 2, d.kv_total, cudaMemcpyDeviceToHost);
+        for (int g = 1; g < d.n_head_kv && e == cudaSuccess; ++g)
+            e = cudaMemcpy2D(dst + (size_t)g * d.head_dim, (size_t)d.kv_row * 2,
+                             src + g * head_elems, (size_t)d.head_dim * 2, (size_t)d.head_dim * 2,
+                             d.kv_total, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(r, e, "ring_get_kv");
+    }
+    return RING_OK;
+}
+
+int ring_device_error(ring_t *r, uint32_t *bits) {
+    if (!r) return RING_EINVAL;
+    uint32_t w = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&w, r->m.err, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && w) e = cudaMemset(r->m.err, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_device_error");
+    if (bits) *bits = w;
+    if (w) return fail(r, RING_EDEVICE, "device error word 0x%x", w);
+    return RING_OK;
+}
+
+int ring_describe(const ring_t *r, char *buf, size_t len) {
+    if (!r || !buf || !len) return RING_EINVAL;
+    const RingDims &d = r->d;
+    const double mib = 2.0 * d.n_layer * d.kv_row * d.kv_total * 2 / 1048576.0;
+    snprintf(buf, len,
+             "[draft-kv] ctx-KV ring active: cap=%d kv_total=%d a_step=%d layers=%d f16 cache %.1f MiB",
+             d.cap, d.kv_total, d.a_step, d.n_layer, mib);
+    return RING_OK;
+}
+
+int ring_profile_enable(ring_t *r, int32_t on) {
+    if (!r) return RING_EINVAL;
+    r->profiling = on != 0;
+    return RING_OK;
+}
+
+int ring_profile_read(ring_t *r, ring_profile *out) {
+    if (!r || !out) return RING_EINVAL;
+    for (auto &rec : r->recs) {
+        cudaError_t e = cudaEventSynchronize(rec.b);
+        if (e != cudaSuccess) return cuda_fail(r, e, "ring_profile_read");
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, rec.a, rec.b);
+        if (rec.cls >= 0 && rec.cls < kKinds) {
+            out->launches[rec.cls] += 1;
+            out->total_ms[rec.cls] += ms;
+        }
+        r->ev_pool.push_back(rec.a);
+        r->ev_pool.push_back(rec.b);
+    }
+    r->recs.clear();
+    return RING_OK;
+}
+
+int64_t ring_launch_count(const ring_t *r) { return r ? r->launches : 0; }
+
+const char *ring_last_error(const ring_t *r) {
+    return r ? r->err.c_str() : g_init_error.c_str();
+}
+
+}  // extern "C"

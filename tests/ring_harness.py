@@ -1,0 +1,214 @@
+"""Test helper: drives the CUDA ring (through the C ABI binding) and the float64 oracle on
+the same seeded workload.  Inputs for the GPU are drawn on the GPU by the seeded
+generator; inputs for the oracle are drawn on the CPU by the same generator (the two are
+bit-identical, which test_gpu_ring checks).  Nothing here computes ring arithmetic."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+from oracle import ring_oracle as orc
+from speculative_decoding_draft_kv_gb300 import ring as R
+
+# Attention tolerance of the method's parity bar.
+ATOL = 2e-3
+REL_L2 = 1e-3
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def f16_ulp_diff(a, b) -> np.ndarray:
+    """Distance in binary16 units in the last place (+0 and -0 coincide)."""
+    def ordered(x):
+        u = np.asarray(x, np.float16).view(np.uint16).astype(np.int32)
+        mag = u & 0x7FFF
+        return np.where(u & 0x8000, -mag, mag)
+    return np.abs(ordered(a) - ordered(b))
+
+
+class RowSource:
+    """Pre-RoPE context rows by absolute position, drawn on the CPU and cached per
+    (seq, layer) as one contiguous window that slides with the requests."""
+
+    def __init__(self, w):
+        self.w = w
+        self.cache = {}
+
+    def _gen(self, seq, layer, a, b):
+        k, v = synth.context_rows(self.w.seed, seq, layer, torch.arange(a, b), self.w.kv_row,
+                                  self.w.sigma)
+        return k.numpy(), v.numpy()
+
+    def rows(self, seq, layer, pos):
+        pos = np.asarray(pos, np.int64)
+        if pos.size == 0:
+            z = np.zeros((0, self.w.kv_row), np.float16)
+            return z, z
+        lo, hi = int(pos.min()), int(pos.max()) + 1
+        key = (seq, layer)
+        if key in self.cache:
+            b, k, v = self.cache[key]
+            e = b + len(k)
+            if lo < b or hi > e:
+                ks, vs = [], []
+                if lo < b:
+                    kk, vv = self._gen(seq, layer, lo, min(b, hi))
+                    ks.append(kk), vs.append(vv)
+                ov_a, ov_b = max(b, lo), min(e, hi)
+                if ov_a < ov_b:
+                    ks.append(k[ov_a - b:ov_b - b]), vs.append(v[ov_a - b:ov_b - b])
+                if hi > e:
+                    kk, vv = self._gen(seq, layer, max(e, lo), hi)
+                    ks.append(kk), vs.append(vv)
+                k, v, b = np.concatenate(ks), np.concatenate(vs), lo
+                self.cache[key] = (b, k, v)
+        else:
+            k, v = self._gen(seq, layer, lo, hi)
+            b = lo
+            self.cache[key] = (b, k, v)
+        return k[pos - b], v[pos - b]
+
+    def fn(self, seq, layer):
+        return lambda pos: self.rows(seq, layer, pos)
+
+
+class GpuRun:
+    """One CUDA ring plus bookkeeping oracles (slot_pos and masks only) per sequence."""
+
+    def __init__(self, w, swa_window=None, tiles_per_split=0, bulk_chunk=0, device="cuda"):
+        self.w = w
+        self.swa = w.swa_window if swa_window is None else swa_window
+        self.dev = torch.device(device)
+        self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
+                           w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
+                           bulk_chunk=bulk_chunk, tiles_per_split=tiles_per_split)
+        self.g = self.ring.geometry
+        # head_dim 2, one head, one layer: only slot_pos and masks are read from these
+        self.book = [orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta,
+                                    swa_window=self.swa) for _ in range(w.n_seq)]
+        self.committed = np.zeros(w.n_seq, np.int64)
+        self.rows = RowSource(w)
+        self._keep = None
+
+    def close(self):
+        self.ring.close()
+
+    def begin_step(self, committed):
+        w = self.w
+        committed = np.asarray(committed, np.int64)
+        starts, counts = [], []
+        for s in range(w.n_seq):
+            st, nn = self.book[s].rows_needed(int(committed[s]))
+            assert self.ring.rows_needed(s, int(committed[s])) == (st, nn)
+            starts.append(st)
+            counts.append(nn)
+        n_rows = int(sum(counts))
+        row_off = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
+        k_rows = v_rows = None
+        if n_rows:
+            k_rows = torch.empty((w.n_layer, n_rows, w.kv_row), dtype=torch.float16, device=self.dev)
+            v_rows = torch.empty_like(k_rows)
+            for s in range(w.n_seq):
+                if counts[s] == 0:
+                    continue
+                pos = torch.arange(starts[s], committed[s], device=self.dev)
+                a, b = int(row_off[s]), int(row_off[s]) + counts[s]
+                for layer in range(w.n_layer):
+                    k, v = synth.context_rows(w.seed, s, layer, pos, w.kv_row, w.sigma, device=self.dev)
+                    k_rows[layer, a:b] = k
+                    v_rows[layer, a:b] = v
+        self.ring.begin_step(committed, k_rows, v_rows, row_off, np.asarray(starts, np.int64))
+        self._keep = (k_rows, v_rows)
+        paths = []
+        for s in range(w.n_seq):
+            z = np.zeros((1, counts[s], 2), np.float16)
+            paths.append(self.book[s].begin_step(int(committed[s]), z, z, starts[s]))
+        self.committed = committed.copy()
+        return paths
+
+    def inputs(self, step, layer, device):
+        w = self.w
+        qs, ks, vs = [], [], []
+        for s in range(w.n_seq):
+            qs.append(synth.query_block(w.seed, step, s, layer, w.q_len, w.n_head, w.head_dim,
+                                        w.sigma, device=device))
+            k, v = synth.noise_rows(w.seed, step, s, layer, w.q_len, w.kv_row, w.sigma, device=device)
+            ks.append(k)
+            vs.append(v)
+        return torch.stack(qs), torch.stack(ks), torch.stack(vs)
+
+    def attend(self, step, layer, kind):
+        q, kn, vn = self.inputs(step, layer, self.dev)
+        o = torch.empty_like(q)
+        self.ring.attend(layer, kind, q, kn, vn, o)
+        torch.cuda.synchronize()
+        return o.cpu().numpy()
+
+    def expected(self, step, layer, kind, seq, heads=None):
+        w = self.w
+        q = synth.query_block(w.seed, step, seq, layer, w.q_len, w.n_head, w.head_dim, w.sigma)
+        kn, vn = synth.noise_rows(w.seed, step, seq, layer, w.q_len, w.kv_row, w.sigma)
+        return orc.attend_dense(int(self.committed[seq]), w.cap, self.rows.fn(seq, layer),
+                                q.numpy(), kn.numpy(), vn.numpy(), w.head_dim, w.n_head_kv,
+                                w.n_head, w.rope_theta, kind=kind, swa_window=self.swa,
+                                heads=heads)
+
+    def check_slots_and_masks(self, seqs=None):
+        for s in (range(self.w.n_seq) if seqs is None else seqs):
+            b = self.book[s]
+            np.testing.assert_array_equal(self.ring.slot_pos(s), b.slot_pos.astype(np.int32))
+            kinds = ["full"] + (["swa"] if self.swa else [])
+            for kind in kinds:
+                want = b.mask(kind)
+                got = self.ring.mask(s, kind)
+                assert got.view(np.uint32).tobytes() == want.view(np.uint32).tobytes(), (s, kind)
+                np.testing.assert_array_equal(self.ring.tile_flags(s, kind),
+                                              expected_tile_flags(want, self.g["tile_slots"]))
+
+    def check_kv_slots(self, seq, layer, slots):
+        """Sampled slots of K/V against RoPE'd rows regenerated by position."""
+        w = self.w
+        k, v = self.ring.kv(seq, layer)
+        sp = self.book[seq].slot_pos
+        slots = [s for s in slots if sp[s] >= 0]
+        pos = np.array([sp[s] for s in slots], np.int64)
+        if not len(pos):
+            return 0
+        kr, vr = self.rows.rows(seq, layer, pos)
+        want_k = orc.to_f16(orc.rope_rows(kr.astype(np.float64), pos, w.n_head_kv, w.head_dim,
+                                          w.rope_theta))
+        np.testing.assert_array_equal(v[slots], vr)
+        d = f16_ulp_diff(k[slots], want_k)
+        assert d.max() <= 1, d.max()
+        assert np.all(k[self.g["trash_slot"]] == 0) and np.all(v[self.g["trash_slot"]] == 0)
+        return int((d > 0).sum())
+
+
+def expected_tile_flags(mask, tile):
+    """0: no slot of the tile visible to any row; 1: every slot of a full-size tile
+    visible to every row; 2: anything else."""
+    q_len, kv_total = mask.shape
+    n_tiles = (kv_total + tile - 1) // tile
+    out = np.zeros(n_tiles, np.uint8)
+    for t in range(n_tiles):
+        seg = mask[:, t * tile:(t + 1) * tile] == 0
+        if not seg.any():
+            out[t] = 0
+        elif seg.shape[1] == tile and seg.all():
+            out[t] = 1
+        else:
+            out[t] = 2
+    return out
+
+
+def assert_close(got, want, what=""):
+    err = float(np.abs(got - want).max())
+    rl2 = rel_l2(got, want)
+    assert err <= ATOL and rl2 <= REL_L2, f"{what}: max abs {err:.3g}, rel L2 {rl2:.3g}"
+    return err, rl2
