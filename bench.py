@@ -211,7 +211,8 @@ def run_gb300(args):
 
     def new_ring():
         r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
-                   n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split)
+                   n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
+                   max_cluster=args.max_cluster)
         c, k_rows, v_rows, row_off, start, _ = P.steps[0]      # prefill (bulk path), untimed
         r.begin_step(c, k_rows, v_rows, row_off, start, stream)
         torch.cuda.synchronize()
@@ -281,7 +282,7 @@ def run_gb300(args):
     prof = R.ring_profile_read(ring.h)
     R.ring_profile_enable(ring.h, False)
     ring.close()
-    attn = prof["attend_split"]
+    attn = prof["attend"]
     attn_ms = attn["total_ms"] / max(attn["launches"], 1)
     vis = float(np.mean([visible_rows(w, P.steps[1 + j][0], kind) for j in range(n_prof)]))
     kv_bytes = vis * w.kv_row * 2 * 2
@@ -362,6 +363,7 @@ def run_gb300(args):
                 "n_layer": w.n_layer, "head_dim": w.head_dim, "n_head_kv": w.n_head_kv,
                 "n_head": w.n_head, "mask": kind, "kv_total": g["kv_total"],
                 "tiles_per_split": g["tiles_per_split"], "n_splits": g["n_splits"],
+                "cluster": g["cluster"], "groups": g["groups"],
                 "l2": ("flushed between steps (512 MiB write, untimed)" if flush
                        else "inputs larger than L2"),
                 "query_pool": pool, "parallelism": f"independent rings x{world}",
@@ -370,7 +372,7 @@ def run_gb300(args):
             "step_kv_gbs": vis_step / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "k_attend_split", "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": "k_attend", "peak_source": f"{peak_kind} hbm_gbs",
                          "alg_bytes_per_launch": alg_bytes, "launch_ms": attn_ms,
                          "timing": "CUDA events around each launch on its stream, "
                                    "instrumented repeat of the timed steps",
@@ -495,6 +497,7 @@ def main():
     ap.add_argument("--mask", choices=["full", "swa"], default="full")
     ap.add_argument("--pool", type=int, default=64)
     ap.add_argument("--tiles-per-split", type=int, default=0)
+    ap.add_argument("--max-cluster", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

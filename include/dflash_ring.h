@@ -75,7 +75,9 @@ typedef struct ring_params {
     int32_t swa_window;      /* SWA window for RING_MASK_SWA; 0 = no SWA mask                */
     int32_t bulk_chunk;      /* rows per bulk-append chunk; default 1024 (section 1.3)       */
     int32_t tiles_per_split; /* attention split length in 64-slot tiles; 0 = chosen from the
-                                SM count                                                     */
+                                SM count and the number of (sequence, kv head) pairs          */
+    int32_t max_cluster;     /* upper bound on the attention cluster size (1 = no clusters);
+                                0 = the largest the device can co-schedule, at most 16        */
 } ring_params;
 
 /* Geometry and sizes of an initialised ring (all counts, no pointers). */
@@ -85,7 +87,10 @@ typedef struct ring_geometry {
     int32_t tile_slots;      /* slots per attention tile (64)                                */
     int32_t n_tiles;         /* ceil(kv_total / tile_slots)                                  */
     int32_t tiles_per_split; /* tiles streamed by one attention CTA                          */
-    int32_t n_splits;        /* CTAs per (sequence, kv head)                                 */
+    int32_t n_splits;        /* CTAs per (sequence, kv head) = cluster * groups              */
+    int32_t cluster;         /* CTAs per thread-block cluster; they merge their partial
+                                softmax states through distributed shared memory            */
+    int32_t groups;          /* clusters per (sequence, kv head); > 1 adds a combine kernel  */
     int64_t cache_bytes;     /* F16 K+V of one sequence: 2 * n_layer * kv_row * kv_total * 2
                                 (section 1.7)                                                */
     int64_t device_bytes;    /* everything ring_init allocated on the device                 */
@@ -93,8 +98,9 @@ typedef struct ring_geometry {
 
 /* Per-kernel timing collected while profiling is on (CUDA events on the launch stream). */
 typedef struct ring_profile {
-    int64_t launches[5];     /* 0 append (fold-in + bulk), 1 mask build, 2 attend prologue,
-                                3 split-KV attention, 4 split combine                       */
+    int64_t launches[5];     /* 0 bulk append chunk, 1 begin-step kernel (fold-in append,
+                                slot_pos, masks, flags, RoPE table), 2 attention, 3 group
+                                combine, 4 unused                                            */
     double total_ms[5];      /* summed event time per kernel class                          */
 } ring_profile;
 

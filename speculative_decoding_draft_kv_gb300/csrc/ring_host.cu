@@ -159,14 +159,53 @@ bool encode_kv_map(CUtensorMap *tm, void *base, const RingDims &d) {
     return res == CUDA_SUCCESS;
 }
 
-int auto_tiles_per_split(const RingDims &d, int sms) {
-    // Aim for about four waves of two resident CTAs per SM, but never fewer than 2 or
-    // more than 64 tiles per CTA (the partial write is 16 KiB per CTA).
-    const int64_t work = (int64_t)d.n_seq * d.n_head_kv * d.n_tiles;
-    const int64_t target = (int64_t)sms * 2 * 4;
-    int64_t tps = (work + target - 1) / target;
-    tps = std::max<int64_t>(2, std::min<int64_t>(64, tps));
-    return (int)std::min<int64_t>(tps, d.n_tiles);
+int pow2_floor(int x) {
+    int p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
+int pow2_ceil(int x) {
+    int p = 1;
+    while (p < x) p *= 2;
+    return p;
+}
+
+// Work split of the attention kernel.  A thread-block cluster holds every one of its SM
+// slots until its slowest CTA is done, so clusters (merging through distributed shared
+// memory, no second kernel) are used only when the whole grid fits in one wave of two
+// CTAs per SM -- the few-sequence case, where latency rules.  Otherwise each CTA is its
+// own group: about four waves of independent CTAs stream the tiles and a small combine
+// kernel merges the per-CTA partials.
+void choose_split(RingDims &d, int sms, int max_cluster, int tps_req) {
+    const int cmax = std::max(1, std::min(16, pow2_floor(std::max(1, max_cluster))));
+    const int slots = 2 * std::max(sms, 1);
+    const int pairs = d.n_seq * d.n_head_kv;
+    if (tps_req > 0) {
+        const int tps = std::min(tps_req, d.n_tiles);
+        const int ns = (d.n_tiles + tps - 1) / tps;
+        d.cluster = std::min(cmax, pow2_floor(ns));
+        d.groups = (ns + d.cluster - 1) / d.cluster;
+        d.tiles_per_split = tps;
+        d.n_splits = d.cluster * d.groups;
+        return;
+    }
+    int c = std::min(cmax, pow2_floor(std::max(1, slots / pairs)));
+    c = std::min(c, pow2_ceil(d.n_tiles));
+    if (c >= 2 && (d.n_tiles + c - 1) / c <= 128) {
+        d.cluster = c;
+        d.groups = 1;
+        d.tiles_per_split = (d.n_tiles + c - 1) / c;
+    } else {
+        const int64_t work = (int64_t)pairs * d.n_tiles;
+        int64_t tps = (work + 4LL * slots - 1) / (4LL * slots);
+        tps = std::max<int64_t>(2, std::min<int64_t>(64, tps));
+        tps = std::min<int64_t>(tps, d.n_tiles);
+        d.cluster = 1;
+        d.tiles_per_split = (int)tps;
+        d.groups = (d.n_tiles + d.tiles_per_split - 1) / d.tiles_per_split;
+    }
+    d.n_splits = d.cluster * d.groups;
 }
 
 bool check_seq(ring_t *r, int32_t seq) { return r && seq >= 0 && seq < r->d.n_seq; }
@@ -196,7 +235,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     const int n_seq = p->n_seq > 0 ? p->n_seq : 1;
     if (p->cap <= 0 || p->q_len <= 0 || p->head_dim <= 0 || p->n_head_kv <= 0 ||
         p->n_head <= 0 || p->n_layer <= 0 || p->swa_window < 0 || p->bulk_chunk < 0 ||
-        p->tiles_per_split < 0 || !(p->rope_theta > 0.f))
+        p->tiles_per_split < 0 || p->max_cluster < 0 || !(p->rope_theta > 0.f))
         return fail(nullptr, RING_EINVAL, "ring_init: every dimension must be positive");
     if (p->n_head % p->n_head_kv)
         return fail(nullptr, RING_EINVAL, "ring_init: n_head %d not a multiple of n_head_kv %d",
@@ -242,9 +281,16 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, r->device);
-    d.tiles_per_split = p->tiles_per_split > 0 ? std::min(p->tiles_per_split, d.n_tiles)
-                                               : auto_tiles_per_split(d, std::max(sms, 1));
-    d.n_splits = (d.n_tiles + d.tiles_per_split - 1) / d.tiles_per_split;
+    e = attend_kernels_init();
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(nullptr, e, "ring_init: kernel attributes");
+        delete r;
+        return rc;
+    }
+    int max_cluster = attend_max_cluster();
+    if (p->max_cluster > 0) max_cluster = std::min(max_cluster, p->max_cluster);
+    choose_split(d, sms, max_cluster, p->tiles_per_split);
+    d.single_wave = (int64_t)d.n_splits * d.n_head_kv * d.n_seq <= 2LL * std::max(sms, 1) ? 1 : 0;
 
     const size_t kv_elems = (size_t)d.n_seq * d.n_layer * d.n_head_kv * d.kv_total * d.head_dim;
     RingDev &m = r->m;
@@ -263,9 +309,9 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     ALLOC(m.mask, float, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total);
     ALLOC(m.flags, uint8_t, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
     ALLOC(m.steps, SeqStep, d.n_seq);
-    ALLOC(m.q16, uint16_t, (size_t)d.n_seq * d.n_head_kv * kRows * kHeadDim);
-    ALLOC(m.part_acc, float, (size_t)d.n_seq * d.n_head_kv * d.n_splits * kRows * kHeadDim);
-    ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.n_splits * kRows);
+    ALLOC(m.rope32, float2, (size_t)d.n_seq * d.q_len * d.head_dim / 2);
+    ALLOC(m.part_acc, float, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows * kHeadDim);
+    ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows);
     ALLOC(m.err, uint32_t, 1);
     ALLOC(m.inv_freq, double, d.head_dim / 2);
 #undef ALLOC
@@ -281,7 +327,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     zero(m.mask, 0, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total * 4);
     zero(m.flags, 0, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
     zero(m.steps, 0, sizeof(SeqStep) * d.n_seq);
-    zero(m.q16, 0, (size_t)d.n_seq * d.n_head_kv * kRows * kHeadDim * 2);
+    zero(m.rope32, 0, (size_t)d.n_seq * d.q_len * d.head_dim / 2 * sizeof(float2));
     zero(m.err, 0, 4);
     std::vector<double> inv(d.head_dim / 2);
     for (int i = 0; i < d.head_dim / 2; ++i)
@@ -304,12 +350,6 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     for (auto &ev : r->slot_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (!encode_kv_map(&r->tm_k, m.k, d) || !encode_kv_map(&r->tm_v, m.v, d)) {
         int rc = fail(nullptr, RING_ECUDA, "ring_init: cuTensorMapEncodeTiled failed");
-        release(r);
-        return rc;
-    }
-    e = attend_kernels_init();
-    if (e != cudaSuccess) {
-        int rc = cuda_fail(nullptr, e, "ring_init: kernel attributes");
         release(r);
         return rc;
     }
@@ -344,6 +384,8 @@ int ring_get_geometry(const ring_t *r, ring_geometry *g) {
     g->n_tiles = d.n_tiles;
     g->tiles_per_split = d.tiles_per_split;
     g->n_splits = d.n_splits;
+    g->cluster = d.cluster;
+    g->groups = d.groups;
     g->cache_bytes = 2LL * d.n_layer * d.kv_row * d.kv_total * 2;
     g->device_bytes = r->device_bytes;
     return RING_OK;
@@ -432,11 +474,14 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
 
     const auto *kr = static_cast<const uint16_t *>(k_rows);
     const auto *vr = static_cast<const uint16_t *>(v_rows);
-    e = timed(r, 0, cs, [&] { return launch_fold_append(d, r->m, kr, vr, n_rows, cs); });
+    // bulk chunks first (slot_pos of those slots is then read by the begin kernel)
     const int n_chunks = (int)((max_bulk + d.bulk_chunk - 1) / d.bulk_chunk);
     for (int c = 0; c < n_chunks && e == cudaSuccess; ++c)
         e = timed(r, 0, cs, [&] { return launch_bulk_append(d, r->m, kr, vr, n_rows, c, cs); });
-    if (e == cudaSuccess) e = timed(r, 1, cs, [&] { return launch_build_mask(d, r->m, cs); });
+    if (e == cudaSuccess)
+        e = timed(r, 1, cs, [&] {
+            return launch_begin_step(d, r->m, kr, vr, n_rows, !r->profiling, cs);
+        });
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
     for (int s = 0; s < d.n_seq; ++s) {
         r->next_pos[s] = committed[s];
@@ -459,22 +504,18 @@ int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q, con
     if (!q || !k_noise || !v_noise || !o)
         return fail(r, RING_EINVAL, "ring_attend: NULL input or output");
     if ((reinterpret_cast<uintptr_t>(k_noise) | reinterpret_cast<uintptr_t>(v_noise) |
-         reinterpret_cast<uintptr_t>(o)) & 15)
-        return fail(r, RING_EINVAL, "ring_attend: noise rows and output must be 16-byte aligned");
+         reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(q)) & 15)
+        return fail(r, RING_EINVAL, "ring_attend: inputs and output must be 16-byte aligned");
     if (!r->have_step) return fail(r, RING_ESTATE, "ring_attend: no ring_begin_step yet");
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const auto *kn = static_cast<const uint16_t *>(k_noise);
     const auto *vn = static_cast<const uint16_t *>(v_noise);
     cudaError_t e = timed(r, 2, cs, [&] {
-        return launch_attend_prologue(d, r->m, layer, q, kn, vn, cs);
+        return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q,
+                             kn, vn, o, !r->profiling, cs);
     });
-    if (e == cudaSuccess)
-        e = timed(r, 3, cs, [&] {
-            return launch_attend_split(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind,
-                                       r->scale_log2, o, cs);
-        });
-    if (e == cudaSuccess && d.n_splits > 1)
-        e = timed(r, 4, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
+    if (e == cudaSuccess && d.groups > 1)
+        e = timed(r, 3, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_attend: launch");
     return RING_OK;
 }

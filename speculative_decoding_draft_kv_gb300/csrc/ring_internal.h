@@ -8,15 +8,21 @@
 //   mask      F32  [n_seq][n_kinds][q_len][kv_total]    0 or -inf
 //   flags     U8   [n_seq][n_kinds][n_tiles]            0 none / 1 all / 2 mixed visible
 //   steps     SeqStep[n_seq]                            this step's window, per sequence
-//   q16       F16  [n_seq][n_head_kv][32][head_dim]     RoPE'd queries, GQA-grouped rows
-//   part_acc  F32  [n_seq][n_head_kv][n_splits][32][head_dim]  split partial numerators
-//   part_ml   F32x2[n_seq][n_head_kv][n_splits][32]            split (max, sum), log2 units
+//   rope32    F32x2[n_seq][q_len][head_dim/2]           cos, sin of the noise positions
+//   part_acc  F32  [n_seq][n_head_kv][groups][32][head_dim]  cluster-group partial numerators
+//   part_ml   F32x2[n_seq][n_head_kv][groups][32]            their (max, sum), log2 units
 //   err       U32  device error word (bounded waits that ran out)
+//
+// Attention work split: n_splits = cluster * groups CTAs per (sequence, kv head), each
+// streaming tiles_per_split consecutive 64-slot tiles.  The `cluster` CTAs of a group are
+// one thread-block cluster and merge their partial softmax states through distributed
+// shared memory; with groups > 1 a combine kernel merges the group partials.
 #pragma once
 
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 namespace dflash {
 
@@ -44,6 +50,8 @@ struct RingDims {
     int cap, q_len, head_dim, n_head_kv, n_head, n_layer, n_seq, swa_window;
     int a_step, trash_slot, kv_total, kv_row, group, rows;
     int n_tiles, tiles_per_split, n_splits, n_kinds, bulk_chunk;
+    int cluster, groups;
+    int single_wave;      // attention grid fits in one wave of two CTAs per SM
 };
 
 struct RingDev {
@@ -52,32 +60,60 @@ struct RingDev {
     float *mask;
     uint8_t *flags;
     SeqStep *steps;
-    uint16_t *q16;
+    float2 *rope32;
     float *part_acc;
     float2 *part_ml;
     uint32_t *err;
     double *inv_freq;     // [head_dim / 2] theta^(-2i/head_dim), computed on the host
 };
 
+// RoPE angle of position p for the pair with inverse frequency f (= theta^(-2i/d)):
+// the angle p * f is formed in float64 (one rounding, as a float64 reference does),
+// reduced to [-pi, pi] with a two-part 2*pi, and only then handed to float32 sincosf.
+// float64 work per angle is a multiply and two FMAs: this GPU's float64 rate is far
+// below its float32 rate, so float64 sin/cos would dominate the small kernels.
+__device__ __forceinline__ float2 rope_angle_cs(int64_t p, double f) {
+    const double kTwoPiHi = 6.283185307179586;            // nearest double to 2*pi
+    const double kTwoPiLo = 2.4492935982947064e-16;        // 2*pi - kTwoPiHi
+    const double kInvTwoPi = 0.15915494309189535;
+    const double a = (double)p * f;
+    const double k = rint(a * kInvTwoPi);
+    double r = fma(-k, kTwoPiHi, a);
+    r = fma(-k, kTwoPiLo, r);
+    float sn, c;
+    sincosf((float)r, &sn, &c);
+    return make_float2(c, sn);
+}
+
+// NeoX rotation of one F16 pair (x1, x2) by (cos, sin): float32 FMAs.
+__device__ __forceinline__ float2 rope_rotate(uint16_t x1b, uint16_t x2b, float2 cs) {
+    const float x1 = __half2float(__ushort_as_half(x1b));
+    const float x2 = __half2float(__ushort_as_half(x2b));
+    return make_float2(fmaf(x1, cs.x, -x2 * cs.y), fmaf(x1, cs.y, x2 * cs.x));
+}
+
 // ---- launchers (ring_kernels.cu) ----
-cudaError_t launch_fold_append(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
-                               const uint16_t *v_rows, int64_t n_rows, cudaStream_t st);
+// Bulk append of one chunk (rows chunk*bulk_chunk ...) for sequences on the bulk path.
 cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                                const uint16_t *v_rows, int64_t n_rows, int chunk,
                                cudaStream_t st);
-cudaError_t launch_build_mask(const RingDims &d, const RingDev &m, cudaStream_t st);
+// Fold-in append + slot_pos + masks + tile flags + the step's RoPE table, one kernel.
+// pdl: launch with programmatic stream serialization (the kernel waits on its
+// predecessor before touching ring state).
+cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
+                              const uint16_t *v_rows, int64_t n_rows, bool pdl,
+                              cudaStream_t st);
 
 // ---- launchers (attn_kernels.cu) ----
-cudaError_t launch_attend_prologue(const RingDims &d, const RingDev &m, int layer,
-                                   const float *q, const uint16_t *k_noise,
-                                   const uint16_t *v_noise, cudaStream_t st);
 cudaError_t attend_kernels_init();   // per device, before the first launch
+int attend_max_cluster();            // largest cluster the attention kernel can launch with
 // scale_log2 = log2(e) / sqrt(head_dim): the softmax runs in base 2.
-cudaError_t launch_attend_split(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
-                                const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
-                                float *o, cudaStream_t st);
+cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
+                          const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
+                          const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
+                          float *o, bool pdl, cudaStream_t st);
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,
                                   cudaStream_t st);
-size_t attend_split_smem_bytes();
+size_t attend_smem_bytes();
 
 }  // namespace dflash

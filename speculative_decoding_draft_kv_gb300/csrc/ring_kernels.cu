@@ -2,9 +2,10 @@
 //
 // Page "DFLASH2_RING_PORT.md": section 1.2 (slot = p % cap, slot_pos[slot] = p, RoPE at
 // absolute positions), section 1.3 (fold-in of a_step rows with pad rows routed to
-// trash_slot; bulk append in chunks when n_new > a_step) and section 1.4 (mask_full,
-// mask_swa).  These kernels move a few KiB per step; they are latency-bound, so they
-// are written for few instructions per row rather than for bandwidth.
+// trash_slot; bulk append in chunks when n_new > a_step; noise positions committed + i)
+// and section 1.4 (mask_full, mask_swa).  These kernels move a few KiB per step: they are
+// latency-bound, so one kernel does the whole fold-in step (append, slot_pos, masks, tile
+// flags and the RoPE table of the noise positions) instead of a chain of small launches.
 #include "ring_internal.h"
 
 #include <cuda_fp16.h>
@@ -12,76 +13,77 @@
 namespace dflash {
 namespace {
 
-constexpr int kAppendThreads = 128;
-constexpr int kMaskThreads = kTile;   // one thread per slot of a tile
+constexpr int kBeginThreads = 128;
 
-__device__ __forceinline__ double h2d(uint16_t bits) {
-    return (double)__half2float(__ushort_as_half(bits));
-}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ uint16_t d2h(double x) {
-    return __half_as_ushort(__double2half(x));   // round to nearest even
-}
-
-// cos/sin of position `pos` for every rotary pair, float64 (inv_freq from the host).
-__device__ __forceinline__ void rope_table(double *cs_cos, double *cs_sin, int64_t pos,
-                                           const double *inv_freq, int half) {
-    for (int j = threadIdx.x; j < half; j += blockDim.x) {
-        double s, c;
-        sincos((double)pos * inv_freq[j], &s, &c);
-        cs_cos[j] = c;
-        cs_sin[j] = s;
-    }
+// cos/sin of position `pos` for every rotary pair (see rope_angle_cs).
+__device__ __forceinline__ void rope_table(float2 *cs, int64_t pos, const double *inv_freq,
+                                           int half) {
+    for (int j = threadIdx.x; j < half; j += blockDim.x) cs[j] = rope_angle_cs(pos, inv_freq[j]);
 }
 
 // Write context row `row` (position p) into slot p % cap of every layer of sequence s:
-// K turned by RoPE at p (NeoX pairs j, j + head_dim/2; float64 products rounded once to
-// F16), V copied.  Called by a whole block after rope_table() for p.
+// K turned by RoPE at p (NeoX pairs j, j + head_dim/2, float32 products, one rounding to
+// F16), V copied.  Called by a whole block after rope_table() for p.  Work item u is
+// (layer, kv head, 8 consecutive pairs); all of a thread's loads are issued before any of
+// its stores, so a row costs one memory round trip instead of one per item.
 __device__ void append_row(const RingDims &d, const RingDev &m, int s, int64_t p,
-                           int64_t row, const uint16_t *k_rows, const uint16_t *v_rows,
-                           int64_t n_rows, const double *cs_cos, const double *cs_sin) {
+                           int64_t row, const uint16_t *__restrict__ k_rows,
+                           const uint16_t *__restrict__ v_rows, int64_t n_rows,
+                           const float2 *cs) {
+    constexpr int kBatch = 4;
     const int slot = (int)(p % d.cap);
     const int hd = d.head_dim, half = hd / 2;
-    for (int layer = 0; layer < d.n_layer; ++layer) {
-        const uint16_t *ks = k_rows + ((int64_t)layer * n_rows + row) * d.kv_row;
-        const uint4 *vs = reinterpret_cast<const uint4 *>(v_rows + ((int64_t)layer * n_rows + row) * d.kv_row);
-        const int64_t head0 = ((int64_t)s * d.n_layer + layer) * d.n_head_kv;
-        for (int idx = threadIdx.x; idx < d.n_head_kv * half; idx += blockDim.x) {
-            const int g = idx / half, j = idx - g * half;
-            const double x1 = h2d(ks[g * hd + j]);
-            const double x2 = h2d(ks[g * hd + j + half]);
-            const double c = cs_cos[j], sn = cs_sin[j];
-            const double y1 = __dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, sn));
-            const double y2 = __dadd_rn(__dmul_rn(x1, sn), __dmul_rn(x2, c));
-            uint16_t *dst = m.k + ((head0 + g) * d.kv_total + slot) * hd;
-            dst[j] = d2h(y1);
-            dst[j + half] = d2h(y2);
+    const int chunks = half / 8;                          // 8-pair chunks per head
+    const int n_items = d.n_layer * d.n_head_kv * chunks;
+    for (int base = 0; base < n_items; base += kBatch * (int)blockDim.x) {
+        uint4 xa[kBatch], xb[kBatch], xv[kBatch][2];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int u = base + b * (int)blockDim.x + (int)threadIdx.x;
+            if (u < n_items) {
+                const int layer = u / (d.n_head_kv * chunks);
+                const int g = (u / chunks) % d.n_head_kv, jc = u % chunks;
+                const int64_t src = ((int64_t)layer * n_rows + row) * d.kv_row + g * hd + jc * 8;
+                xa[b] = *reinterpret_cast<const uint4 *>(k_rows + src);
+                xb[b] = *reinterpret_cast<const uint4 *>(k_rows + src + half);
+                xv[b][0] = *reinterpret_cast<const uint4 *>(v_rows + src);
+                xv[b][1] = *reinterpret_cast<const uint4 *>(v_rows + src + half);
+            }
         }
-        const int vec_per_head = hd / 8;
-        for (int idx = threadIdx.x; idx < d.n_head_kv * vec_per_head; idx += blockDim.x) {
-            const int g = idx / vec_per_head, cidx = idx - g * vec_per_head;
-            uint4 *dst = reinterpret_cast<uint4 *>(m.v + ((head0 + g) * d.kv_total + slot) * hd);
-            dst[cidx] = vs[g * vec_per_head + cidx];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int u = base + b * (int)blockDim.x + (int)threadIdx.x;
+            if (u < n_items) {
+                const int layer = u / (d.n_head_kv * chunks);
+                const int g = (u / chunks) % d.n_head_kv, jc = u % chunks;
+                const int64_t head = ((int64_t)s * d.n_layer + layer) * d.n_head_kv + g;
+                const int64_t dst = (head * d.kv_total + slot) * hd + jc * 8;
+                const uint16_t *a16 = reinterpret_cast<const uint16_t *>(&xa[b]);
+                const uint16_t *b16 = reinterpret_cast<const uint16_t *>(&xb[b]);
+                uint4 ya, yb;
+                uint16_t *ya16 = reinterpret_cast<uint16_t *>(&ya);
+                uint16_t *yb16 = reinterpret_cast<uint16_t *>(&yb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 r = rope_rotate(a16[e], b16[e], cs[jc * 8 + e]);
+                    ya16[e] = __half_as_ushort(__float2half_rn(r.x));
+                    yb16[e] = __half_as_ushort(__float2half_rn(r.y));
+                }
+                *reinterpret_cast<uint4 *>(m.k + dst) = ya;
+                *reinterpret_cast<uint4 *>(m.k + dst + half) = yb;
+                *reinterpret_cast<uint4 *>(m.v + dst) = xv[b][0];
+                *reinterpret_cast<uint4 *>(m.v + dst + half) = xv[b][1];
+            }
         }
     }
     if (threadIdx.x == 0) m.slot_pos[(int64_t)s * d.cap + slot] = (int32_t)p;
 }
 
-// Fold-in append: grid (a_step, n_seq).  Block i appends real row i of the step when
-// i < fold_rows, otherwise it is a pad row and writes zeros to trash_slot.
-__global__ void __launch_bounds__(kAppendThreads)
-k_fold_append(RingDims d, RingDev m, const uint16_t *k_rows, const uint16_t *v_rows,
-              int64_t n_rows) {
-    __shared__ double cs_cos[kHeadDim / 2], cs_sin[kHeadDim / 2];
-    const int i = blockIdx.x, s = blockIdx.y;
-    const SeqStep st = m.steps[s];
-    if (i < st.fold_rows) {
-        const int64_t p = st.start + i;
-        rope_table(cs_cos, cs_sin, p, m.inv_freq, d.head_dim / 2);
-        __syncthreads();
-        append_row(d, m, s, p, st.src_row + i, k_rows, v_rows, n_rows, cs_cos, cs_sin);
-        return;
-    }
+// Pad row of the fold-in path: zeros to trash_slot of every layer (reading: pad rows are
+// zeros, so concurrent pad writers agree and the slot stays finite).
+__device__ void pad_row(const RingDims &d, const RingDev &m, int s) {
     const int vec_per_head = d.head_dim / 8;
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int layer = 0; layer < d.n_layer; ++layer) {
@@ -95,49 +97,32 @@ k_fold_append(RingDims d, RingDev m, const uint16_t *k_rows, const uint16_t *v_r
     }
 }
 
-// Bulk append, one chunk of bulk_chunk rows: grid (bulk_chunk, n_seq).  Only sequences
-// that took the bulk path (n_new > a_step) do anything.
-__global__ void __launch_bounds__(kAppendThreads)
-k_bulk_append(RingDims d, RingDev m, const uint16_t *k_rows, const uint16_t *v_rows,
-              int64_t n_rows, int chunk) {
-    __shared__ double cs_cos[kHeadDim / 2], cs_sin[kHeadDim / 2];
-    const int s = blockIdx.y;
-    const SeqStep st = m.steps[s];
-    if (st.n_new <= d.a_step) return;
-    const int64_t i = (int64_t)chunk * d.bulk_chunk + blockIdx.x;
-    if (i >= st.n_new) return;
-    const int64_t p = st.start + i;
-    rope_table(cs_cos, cs_sin, p, m.inv_freq, d.head_dim / 2);
-    __syncthreads();
-    append_row(d, m, s, p, st.src_row + i, k_rows, v_rows, n_rows, cs_cos, cs_sin);
-}
-
-// Masks from slot_pos: grid (n_tiles, n_seq), one thread per slot.  Writes the F32 mask
-// rows of every kind and one visibility flag per tile and kind.
-__global__ void __launch_bounds__(kMaskThreads)
-k_build_mask(RingDims d, RingDev m) {
-    const int tile = blockIdx.x, s = blockIdx.y;
-    const int slot = tile * kTile + threadIdx.x;
-    const SeqStep st = m.steps[s];
-    const bool in_range = slot < d.kv_total;
+// Masks and flags of one 64-slot tile.  The slot_pos a slot holds after this step is
+// computed here rather than read back: a slot written by this step's fold-in rows holds
+// start + k with k = (slot - start) mod cap < fold_rows; any other slot keeps its value
+// (already updated by the bulk kernels, which run before this one).
+__device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, const SeqStep &st) {
+    const int slot = tile * kTile + (int)threadIdx.x;
+    const bool active = threadIdx.x < kTile;
+    const bool in_range = active && slot < d.kv_total;
     bool ctx_full = false, ctx_swa = false;
     int noise_j = -1;
-    if (slot < d.cap) {
-        const int64_t p = m.slot_pos[(int64_t)s * d.cap + slot];
+    if (active && slot < d.cap) {
+        const int64_t k = ((int64_t)slot - st.start % d.cap + d.cap) % d.cap;
+        const int64_t p = k < st.fold_rows ? st.start + k
+                                           : (int64_t)m.slot_pos[(int64_t)s * d.cap + slot];
         ctx_full = p >= st.lo && p < st.committed;
         ctx_swa = p >= st.swa_lo && p < st.committed;
-    } else if (slot < d.cap + d.q_len) {
+    } else if (active && slot < d.cap + d.q_len) {
         noise_j = slot - d.cap;
     }
     const float ninf = __int_as_float(0xff800000);
-
-    // mask_full: the same row for every query (noise block bidirectional)
-    {
+    {   // mask_full: the same row for every query (noise block bidirectional)
         float *mk = m.mask + (int64_t)s * d.n_kinds * d.q_len * d.kv_total;
         const bool vis = ctx_full || noise_j >= 0;
         if (in_range)
             for (int i = 0; i < d.q_len; ++i) mk[(int64_t)i * d.kv_total + slot] = vis ? 0.f : ninf;
-        const int all = __syncthreads_and(in_range && vis);
+        const int all = __syncthreads_and(!active || (in_range && vis));
         const int any = __syncthreads_or(in_range && vis);
         if (threadIdx.x == 0)
             m.flags[((int64_t)s * d.n_kinds) * d.n_tiles + tile] = any ? (all ? 1 : 2) : 0;
@@ -152,32 +137,89 @@ k_build_mask(RingDims d, RingDev m) {
             all_rows = all_rows && vis;
             any_row = any_row || vis;
         }
-        const int all = __syncthreads_and(in_range && all_rows);
+        const int all = __syncthreads_and(!active || (in_range && all_rows));
         const int any = __syncthreads_or(in_range && any_row);
         if (threadIdx.x == 0)
             m.flags[((int64_t)s * d.n_kinds + 1) * d.n_tiles + tile] = any ? (all ? 1 : 2) : 0;
     }
 }
 
-}  // namespace
-
-cudaError_t launch_fold_append(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
-                               const uint16_t *v_rows, int64_t n_rows, cudaStream_t st) {
-    k_fold_append<<<dim3(d.a_step, d.n_seq), kAppendThreads, 0, st>>>(d, m, k_rows, v_rows, n_rows);
-    return cudaGetLastError();
+// One begin_step for every sequence: grid (a_step + n_tiles + 1, n_seq).
+//   blocks [0, a_step)                 fold-in row i (real row, or pad row to trash)
+//   blocks [a_step, a_step + n_tiles)  mask rows and flags of one tile
+//   block  a_step + n_tiles            cos/sin of the noise positions committed + i
+__global__ void __launch_bounds__(kBeginThreads)
+k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
+             const uint16_t *__restrict__ v_rows, int64_t n_rows) {
+    __shared__ float2 cs[kHeadDim / 2];
+    pdl_wait();   // the previous step's attention must be done with the ring state
+    // one small wave: the first attention kernel may settle its CTAs right away (it waits
+    // for this grid to finish before reading anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int b = blockIdx.x, s = blockIdx.y;
+    const SeqStep st = m.steps[s];
+    if (b < d.a_step) {
+        if (b < st.fold_rows) {
+            const int64_t p = st.start + b;
+            rope_table(cs, p, m.inv_freq, d.head_dim / 2);
+            __syncthreads();
+            append_row(d, m, s, p, st.src_row + b, k_rows, v_rows, n_rows, cs);
+        } else {
+            pad_row(d, m, s);
+        }
+        return;
+    }
+    if (b < d.a_step + d.n_tiles) {
+        mask_tile(d, m, s, b - d.a_step, st);
+        return;
+    }
+    const int half = d.head_dim / 2;
+    for (int idx = threadIdx.x; idx < d.q_len * half; idx += blockDim.x) {
+        const int i = idx / half, j = idx - i * half;
+        m.rope32[((int64_t)s * d.q_len + i) * half + j] = rope_angle_cs(st.committed + i, m.inv_freq[j]);
+    }
 }
+
+// Bulk append, one chunk of bulk_chunk rows: grid (bulk_chunk, n_seq).  Only sequences
+// that took the bulk path (n_new > a_step) do anything.
+__global__ void __launch_bounds__(kBeginThreads)
+k_bulk_append(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
+              const uint16_t *__restrict__ v_rows, int64_t n_rows, int chunk) {
+    __shared__ float2 cs[kHeadDim / 2];
+    const int s = blockIdx.y;
+    const SeqStep st = m.steps[s];
+    if (st.n_new <= d.a_step) return;
+    const int64_t i = (int64_t)chunk * d.bulk_chunk + blockIdx.x;
+    if (i >= st.n_new) return;
+    const int64_t p = st.start + i;
+    rope_table(cs, p, m.inv_freq, d.head_dim / 2);
+    __syncthreads();
+    append_row(d, m, s, p, st.src_row + i, k_rows, v_rows, n_rows, cs);
+}
+
+}  // namespace
 
 cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                                const uint16_t *v_rows, int64_t n_rows, int chunk,
                                cudaStream_t st) {
-    k_bulk_append<<<dim3(d.bulk_chunk, d.n_seq), kAppendThreads, 0, st>>>(d, m, k_rows, v_rows,
-                                                                         n_rows, chunk);
+    k_bulk_append<<<dim3(d.bulk_chunk, d.n_seq), kBeginThreads, 0, st>>>(d, m, k_rows, v_rows,
+                                                                        n_rows, chunk);
     return cudaGetLastError();
 }
 
-cudaError_t launch_build_mask(const RingDims &d, const RingDev &m, cudaStream_t st) {
-    k_build_mask<<<dim3(d.n_tiles, d.n_seq), kMaskThreads, 0, st>>>(d, m);
-    return cudaGetLastError();
+cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
+                              const uint16_t *v_rows, int64_t n_rows, bool pdl,
+                              cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d.a_step + d.n_tiles + 1, d.n_seq);
+    cfg.blockDim = dim3(kBeginThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_begin_step, d, m, k_rows, v_rows, n_rows);
 }
 
 }  // namespace dflash

@@ -48,14 +48,14 @@ class RingParams(ctypes.Structure):
                 ("n_head", ctypes.c_int32), ("n_layer", ctypes.c_int32),
                 ("rope_theta", ctypes.c_float), ("n_seq", ctypes.c_int32),
                 ("swa_window", ctypes.c_int32), ("bulk_chunk", ctypes.c_int32),
-                ("tiles_per_split", ctypes.c_int32)]
+                ("tiles_per_split", ctypes.c_int32), ("max_cluster", ctypes.c_int32)]
 
 
 class RingGeometry(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cap", "q_len", "a_step", "trash_slot", "kv_total", "kv_row", "head_dim", "n_head_kv",
         "n_head", "n_layer", "n_seq", "swa_window", "bulk_chunk", "tile_slots", "n_tiles",
-        "tiles_per_split", "n_splits")] + [("cache_bytes", ctypes.c_int64),
+        "tiles_per_split", "n_splits", "cluster", "groups")] + [("cache_bytes", ctypes.c_int64),
                                            ("device_bytes", ctypes.c_int64)]
 
 
@@ -63,9 +63,10 @@ class RingProfile(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int64 * 5), ("total_ms", ctypes.c_double * 5)]
 
 
-PROFILE_CLASSES = ("append", "mask", "prologue", "attend_split", "combine")
+PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "unused")
 
 _LIB = None
+_N_SEQ = {}      # handle -> n_seq, so per-step calls skip a geometry query
 
 
 def _load():
@@ -155,21 +156,24 @@ def ring_init(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta):
     rc = _load().ring_init(ctypes.byref(h), cap, q_len, head_dim, n_head_kv, n_head, n_layer,
                            float(rope_theta))
     _check(rc, None, "ring_init")
+    _N_SEQ[h.value] = 1
     return h
 
 
 def ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0):
     p = RingParams(cap, q_len, head_dim, n_head_kv, n_head, n_layer, float(rope_theta), n_seq,
-                   swa_window, bulk_chunk, tiles_per_split)
+                   swa_window, bulk_chunk, tiles_per_split, max_cluster)
     h = ctypes.c_void_p()
     rc = _load().ring_init_ex(ctypes.byref(h), ctypes.byref(p))
     _check(rc, None, "ring_init_ex")
+    _N_SEQ[h.value] = max(1, int(n_seq))
     return h
 
 
 def ring_destroy(h):
     if h:
+        _N_SEQ.pop(getattr(h, "value", h), None)
         _load().ring_destroy(h)
 
 
@@ -190,7 +194,7 @@ def ring_rows_needed(h, seq, committed):
 def ring_begin_step(h, committed, k_rows, v_rows, row_off, first_pos, stream=None):
     """``k_rows``/``v_rows``: CUDA float16 [n_layer, n_rows, kv_row] or None."""
     import torch
-    n_seq = ring_get_geometry(h)["n_seq"]
+    n_seq = _N_SEQ.get(getattr(h, "value", h)) or ring_get_geometry(h)["n_seq"]
     c_arr, c_ptr = _i64_array(committed, n_seq, "committed")
     o_arr, o_ptr = _i64_array(row_off, n_seq, "row_off")
     f_arr, f_ptr = _i64_array(first_pos, n_seq, "first_pos")
@@ -283,9 +287,9 @@ class Ring:
     """Owning handle around the C entry points (closes itself)."""
 
     def __init__(self, cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0):
         self.h = ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta,
-                              n_seq, swa_window, bulk_chunk, tiles_per_split)
+                              n_seq, swa_window, bulk_chunk, tiles_per_split, max_cluster)
         self.geometry = ring_get_geometry(self.h)
 
     def rows_needed(self, seq, committed):

@@ -32,6 +32,24 @@ def f16_ulp_diff(a, b) -> np.ndarray:
     return np.abs(ordered(a) - ordered(b))
 
 
+# K slots: the GPU turns K by RoPE in float32 (angle formed and reduced in float64, then
+# float32 sin/cos), the oracle in float64; both round once to F16.  The float32 path is
+# off by at most |x1| * |dcos| + |x2| * |dsin| + rounding <= 3e-7 * (|x1| + |x2|) before
+# the F16 rounding, and the seeded rows are bounded by 3.46 * 0.5, so a stored K may sit
+# one F16 step away, or up to 2e-6 away where the F16 grid is finer than that.
+K_ABS = 2e-6
+
+
+def k_within_tolerance(got, want):
+    """(ok, n_not_bit_exact) for F16 K slots against the float64 oracle's F16 K slots."""
+    got = np.asarray(got, np.float16)
+    want = np.asarray(want, np.float16)
+    d = f16_ulp_diff(got, want)
+    absdiff = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    ok = bool(np.all((d <= 1) | (absdiff <= K_ABS)))
+    return ok, int((d > 0).sum())
+
+
 class RowSource:
     """Pre-RoPE context rows by absolute position, drawn on the CPU and cached per
     (seq, layer) as one contiguous window that slides with the requests."""
@@ -81,13 +99,15 @@ class RowSource:
 class GpuRun:
     """One CUDA ring plus bookkeeping oracles (slot_pos and masks only) per sequence."""
 
-    def __init__(self, w, swa_window=None, tiles_per_split=0, bulk_chunk=0, device="cuda"):
+    def __init__(self, w, swa_window=None, tiles_per_split=0, bulk_chunk=0, device="cuda",
+                 max_cluster=0):
         self.w = w
         self.swa = w.swa_window if swa_window is None else swa_window
         self.dev = torch.device(device)
         self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                            w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
-                           bulk_chunk=bulk_chunk, tiles_per_split=tiles_per_split)
+                           bulk_chunk=bulk_chunk, tiles_per_split=tiles_per_split,
+                           max_cluster=max_cluster)
         self.g = self.ring.geometry
         # head_dim 2, one head, one layer: only slot_pos and masks are read from these
         self.book = [orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta,
@@ -184,10 +204,10 @@ class GpuRun:
         want_k = orc.to_f16(orc.rope_rows(kr.astype(np.float64), pos, w.n_head_kv, w.head_dim,
                                           w.rope_theta))
         np.testing.assert_array_equal(v[slots], vr)
-        d = f16_ulp_diff(k[slots], want_k)
-        assert d.max() <= 1, d.max()
+        ok, inexact = k_within_tolerance(k[slots], want_k)
+        assert ok and inexact <= 0.01 * want_k.size, inexact
         assert np.all(k[self.g["trash_slot"]] == 0) and np.all(v[self.g["trash_slot"]] == 0)
-        return int((d > 0).sum())
+        return inexact
 
 
 def expected_tile_flags(mask, tile):

@@ -45,7 +45,8 @@ def test_build_targets_sm_103a_only():
 
 def _init_rc(**kw):
     p = dict(cap=64, q_len=8, head_dim=128, n_head_kv=8, n_head=32, n_layer=1,
-             rope_theta=1e6, n_seq=1, swa_window=0, bulk_chunk=0, tiles_per_split=0)
+             rope_theta=1e6, n_seq=1, swa_window=0, bulk_chunk=0, tiles_per_split=0,
+             max_cluster=0)
     p.update(kw)
     h = ctypes.c_void_p()
     rc = R.library().ring_init_ex(ctypes.byref(h), ctypes.byref(R.RingParams(**p)))

@@ -13,7 +13,7 @@ import torch
 import synth
 from oracle import ring_oracle as orc
 from speculative_decoding_draft_kv_gb300 import ring as R
-from tests.ring_harness import GpuRun, assert_close, f16_ulp_diff
+from tests.ring_harness import GpuRun, assert_close, k_within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +55,7 @@ def test_tiny_ring_full_state_parity():
     run = GpuRun(w)
     full = orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                           w.rope_theta, swa_window=w.swa_window)
-    k_not_exact = 0
+    k_not_exact = k_total = 0
     try:
         for t, c in enumerate(synth.commit_schedule(w)):
             run.begin_step(c)
@@ -72,10 +72,12 @@ def test_tiny_ring_full_state_parity():
                 assert_close(o[0], o2, f"step {t} {kind}")
             gk, gv = run.ring.kv(0, 0)
             np.testing.assert_array_equal(gv, full.v[0])
-            d = f16_ulp_diff(gk, full.k[0])
-            assert d.max() <= 1
-            k_not_exact += int((d > 0).sum())
-        assert k_not_exact <= 64      # a float64 sin/cos ulp rarely moves an F16 rounding
+            ok, inexact = k_within_tolerance(gk, full.k[0])
+            assert ok
+            k_not_exact += inexact
+            k_total += gk.size
+        # the GPU rotates in float32: rarely it lands on the other side of an F16 rounding
+        assert k_not_exact <= 0.01 * k_total
         assert run.ring.device_error() == 0
     finally:
         run.close()
@@ -169,17 +171,23 @@ def test_large_ring_parity_full_size():
         run.close()
 
 
-@pytest.mark.parametrize("tps", [1, 3, 100])
-def test_split_sizes_agree(tps):
-    """The split-KV partition (including a single split, no combine pass) changes only
-    rounding."""
+@pytest.mark.parametrize("tps,max_cluster", [(0, 0), (0, 1), (0, 2), (1, 0), (3, 0), (3, 1),
+                                             (100, 0), (2, 16)])
+def test_split_sizes_agree(tps, max_cluster):
+    """Any split of the slot tiles -- one CTA, clusters merging through distributed shared
+    memory, independent CTAs with a combine kernel, or both -- changes only rounding."""
     w = synth.workload(2, cap=1024, n_layer=2)
-    run = GpuRun(w, tiles_per_split=tps)
+    run = GpuRun(w, tiles_per_split=tps, max_cluster=max_cluster)
     try:
+        g = run.g
+        assert g["n_splits"] == g["cluster"] * g["groups"]
+        assert g["n_splits"] * g["tiles_per_split"] >= g["n_tiles"]
         for t, c in enumerate(synth.commit_schedule(w, 3)):
             run.begin_step(c)
-        o = run.attend(3, 1, "full")
-        assert_close(o[0], run.expected(3, 1, "full", 0), f"tps {tps}")
+        for kind in ("full",):
+            o = run.attend(3, 1, kind)
+            assert_close(o[0], run.expected(3, 1, kind, 0), f"tps {tps} cluster {g['cluster']}")
+        assert run.ring.device_error() == 0
     finally:
         run.close()
 
@@ -252,3 +260,22 @@ def test_edge_cases_and_host_errors():
         assert e.value.code == R.RING_EINVAL
     finally:
         nos.close()
+
+
+@pytest.mark.parametrize("cap,tps", [(60, 1), (60, 0), (4, 0), (200, 1), (1000, 2)])
+def test_noise_tiles_and_small_rings(cap, tps):
+    """Noise slots cap..cap+7 straddling two tiles owned by two CTAs (cap 60, one tile per
+    CTA), a ring smaller than one tile (cap 4), and group-combine splits."""
+    w = synth.workload(1, cap=cap, n_layer=2, swa_window=max(2, cap // 3))
+    run = GpuRun(w, tiles_per_split=tps)
+    try:
+        for t, c in enumerate(synth.commit_schedule(w, 12)):
+            run.begin_step(c)
+            run.check_slots_and_masks()
+            for kind in ("full", "swa"):
+                layer = t % 2
+                o = run.attend(t, layer, kind)
+                assert_close(o[0], run.expected(t, layer, kind, 0), f"cap {cap} step {t} {kind}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
