@@ -2,13 +2,23 @@
 //
 // Page "DFLASH2_RING_PORT.md", sections 1.1 and 1.4: the q_len noise queries attend to
 // all kv_total slots of the layer's F16 K/V tensors under mask_full or mask_swa.  The
-// hot kernel streams each kv head's visible 64-slot tiles with 3-D TMA boxes into a
-// 3-stage shared-memory ring (128-byte swizzle), guarded by mbarriers; one producer warp
-// issues the copies and four consumer warps compute S = Q K^T and O += P V on the F16
-// tensor cores (m16n8k16, F32 accumulation) with an online softmax in F32 registers.
-// All 32 query rows that share a kv head (4 heads x 8 queries) ride in one CTA, so each
-// K/V byte is read from HBM once per step and layer.  Tiles whose mask flag says "no
-// visible slot" are never fetched.
+// kernel streams each kv head's visible 64-slot tiles with 3-D TMA boxes into a
+// 3-stage shared-memory ring (128-byte swizzle), guarded by mbarriers.  One producer
+// warp issues the copies (plus a 16-byte-aligned bulk copy of the tile's per-row
+// visibility bits when the tile is only partly visible); the consumer warps compute
+// S = Q K^T and O += P V on the F16 tensor cores (m16n8k16, F32 accumulation) with an
+// online softmax in F32 registers.  All 32 query rows that share a kv head (4 heads x 8
+// queries) ride in one CTA, so each K/V byte is read from HBM once per step and layer.
+// Tiles whose flag says "no visible slot" are never fetched.
+//
+// Two shapes of the same kernel:
+//   * many (sequence, kv head) pairs -- a multi-wave grid of independent CTAs, 4 consumer
+//     warps, two CTAs per SM; each CTA writes a partial softmax state and a combine
+//     kernel merges them (unless a pair has a single CTA);
+//   * few pairs -- one wave of thread-block clusters, 8 consumer warps per CTA (one CTA
+//     per SM, so per-tile latency halves); every warp pushes its partial state into the
+//     shared memory of the CTA that owns its rows (distributed shared memory stores),
+//     and after one cluster barrier each CTA finishes 32 / cluster rows locally.
 #include "ring_internal.h"
 
 #include <cuda_fp16.h>
@@ -16,22 +26,39 @@
 namespace dflash {
 namespace {
 
-constexpr int kStages = 3;              // 3 x 32 KiB + Q: two CTAs fit on one SM
 constexpr int kTileBytes = kTile * kHeadDim * 2;   // one 64-slot tile of one head, K or V
 constexpr int kHalfBox = kTileBytes / 2;           // TMA box: 64 slots x 64 columns
 constexpr int kStageBytes = 2 * kTileBytes;        // K + V
 constexpr int kQBytes = kRows * kHeadDim * 2;
-constexpr int kComputeWarps = 4;
-constexpr int kThreads = (kComputeWarps + 1) * 32;
-constexpr int kBarBytes = 2 * kStages * 8;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kQBytes + kBarBytes;
+constexpr int kBitsPerStage = kMaxQWords * 8;      // visibility words of one tile
 constexpr uint64_t kWaitNs = 2000000000ull;        // bounded waits give up after 2 s
 
-static_assert(kComputeWarps * 32 == 128, "named barrier below assumes 128 consumers");
+// Two shapes of one kernel.  CLUSTER: 8 consumer warps (4 key slices), one CTA per SM,
+// partial states pushed to the owning CTA of the cluster.  Plain: 4 consumer warps (2 key
+// halves), two CTAs per SM, key halves merged in shared memory and the CTA's partial
+// written straight from registers.
+template <bool CLUSTER>
+struct Shape {
+    static constexpr int CW = CLUSTER ? 8 : 4;      // consumer warps
+    static constexpr int kConsumers = CW * 32;
+    static constexpr int kThreads = kConsumers + 32;
+    static constexpr int kStages = 3;
+    static constexpr int kSlices = CW / 2;          // key slices per tile
+    static constexpr int kKeys = kTile / kSlices;   // keys per warp per tile (32 or 16)
+    static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
+    static constexpr int kKK = kKeys / 16;          // k-steps of P V per warp
+    static constexpr int kMinBlocks = CLUSTER ? 1 : 2;
+    static constexpr int kOffQ = kStages * kStageBytes;  // 1024-aligned (swizzled like K)
+    static constexpr int kOffBits = kOffQ + kQBytes;
+    static constexpr int kOffBars = kOffBits + kStages * kBitsPerStage;
+    static constexpr int kOffRecv = kOffBars + 2 * kStages * 8 + 16;
+    // cluster receive buffer: kSlices * 32 rows of partial numerators + (max, sum) per row
+    static constexpr int kRecvAcc = kSlices * kRows * kHeadDim * 4;
+    static constexpr int kRecvBytes = kRecvAcc + kSlices * kRows * 8;
+    static constexpr int kSmem = 1024 + kOffRecv + (CLUSTER ? kRecvBytes : 0);
+};
 static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStageBytes,
               "key-half merge scratch must fit in stage buffer 0");
-static_assert(kStages >= 2 && kRows * 132 * 4 + kRows * 8 <= kStageBytes,
-              "cluster-merge partial must fit in stage buffer 1");
 
 // ---------------------------------------------------------------------------------
 // PTX helpers
@@ -163,54 +190,69 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ float ld_cluster(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+
+
+// Named barriers: 1 = the consumer warps; 2 = the noise rows are in global memory (the
+// consumer warps arrive, the producer warp waits before fetching a tile holding noise
+// slots).  Both are always executed by whole, converged warps.
+__device__ __forceinline__ void bar_sync(int id, int n) {
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Named barrier 2: the consumer warps arrive (non-blocking) once the noise rows are in
-// global memory; the producer warp waits on it before fetching a tile that holds noise
-// slots.  Both are always executed by whole, converged warps.
-__device__ __forceinline__ void noise_bar_arrive() {
-    asm volatile("barrier.arrive 2, %0;" ::"r"(kThreads) : "memory");
-}
-__device__ __forceinline__ void noise_bar_sync() {
-    asm volatile("barrier.sync 2, %0;" ::"r"(kThreads) : "memory");
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
-constexpr int kPartStride = 132;   // floats per row of a CTA's merged partial in smem
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
 
 // ---------------------------------------------------------------------------------
 // Split-KV attention of one layer.  Grid (n_splits, n_head_kv, n_seq) in clusters of
-// `cluster` CTAs along x; 5 warps: warps 0-3 compute, warp 4 produces.
+// `cluster` CTAs along x; CW consumer warps + one producer warp.
 //
 //   prologue   consumers turn this kv head's 32 query rows by RoPE at committed + i
 //              (float32, the step's cos/sin table) into F16 shared memory; the CTA whose
 //              tiles hold the noise slots writes the noise block's K (RoPE at
 //              committed + j) and V rows of this head to slots cap + j.  Meanwhile the
 //              producer already streams the context tiles.
-//   main loop  compute warp w owns query rows 16*(w & 1) .. +16 and key half (w >> 1) of
-//              every 64-slot tile: S = Q K^T, online softmax, O += P V.
-//   merge      the two key halves merge through shared memory; then the CTAs of the
-//              cluster merge their (max, sum, numerator) rows through distributed shared
-//              memory, each CTA finishing 32 / cluster rows.
+//   main loop  consumer warp w owns query rows 16*(w & 1) .. +16 and key slice (w >> 1)
+//              of every 64-slot tile: S = Q K^T, online softmax, O += P V.
+//   merge      each warp stores its rows' (max, sum, numerators) into the receive buffer
+//              of the CTA that finishes those rows (itself without a cluster); after one
+//              barrier that CTA merges the kSlices * cluster partial states of its rows
+//              and writes O (or a group partial for the combine kernel).
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool CLUSTER>
+__global__ void __launch_bounds__(Shape<CLUSTER>::kThreads, Shape<CLUSTER>::kMinBlocks)
 k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          RingDims d, RingDev m, int layer, int kind, float scale_log2,
          const float *__restrict__ q, const uint16_t *__restrict__ k_noise,
          const uint16_t *__restrict__ v_noise, float *__restrict__ o) {
+    using SH = Shape<CLUSTER>;
+    constexpr int CW = SH::CW;
+    constexpr int kStages = SH::kStages;
+    constexpr int kOffQ = SH::kOffQ, kOffBits = SH::kOffBits, kOffBars = SH::kOffBars,
+                  kOffRecv = SH::kOffRecv;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sq = smem + kStages * kStageBytes;
-    const uint32_t bar0 = smem_u32(sq + kQBytes);   // full[0..S-1], then empty[0..S-1]
+    uint8_t *sq = smem + kOffQ;
+    const uint64_t *sbits = reinterpret_cast<const uint64_t *>(smem + kOffBits);
+    const uint32_t bar0 = smem_u32(smem + kOffBars);   // full[0..S-1], then empty[0..S-1]
     __shared__ volatile int s_abort;
-    // merged partial of this CTA (rows x head_dim numerators, then max and sum per row);
-    // lives in stage buffer 1, which is idle once the main loop is over
-    float *pacc = reinterpret_cast<float *>(smem + kStageBytes);
-    float *pml = pacc + kRows * kPartStride;
+
+    const uint32_t nct = CLUSTER ? cluster_size() : 1u, rank = CLUSTER ? cluster_rank() : 0u;
+    // receive buffer (clusters only): dedicated, since other CTAs of the cluster push into
+    // it while this CTA may still be streaming
+    float *recv_acc = reinterpret_cast<float *>(smem + kOffRecv);
+    float2 *recv_ml = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(recv_acc) + SH::kRecvAcc);
+    const int rows_per = kRows / (int)nct;
 
     const int sp = blockIdx.x, gk = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,13 +260,14 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const int t1 = min(d.n_tiles, t0 + d.tiles_per_split);
     const int tn0 = d.cap / kTile, tn1 = (d.cap + d.q_len - 1) / kTile;
     const bool owns_noise = t0 < t1 && t0 <= tn1 && t1 > tn0;
-    const uint8_t *flags = m.flags + ((int64_t)s * d.n_kinds + kind) * d.n_tiles;
-    const float *maskp = m.mask + ((int64_t)s * d.n_kinds + kind) * d.q_len * d.kv_total;
+    const int64_t fbase = ((int64_t)s * d.n_kinds + kind) * d.n_tiles;
+    const uint8_t *flags = m.flags + fbase;
+    const int qw = (d.q_len + 1) & ~1;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kStages; ++k) {
             mbar_init(bar0 + 8 * k, 1);
-            mbar_init(bar0 + 8 * (kStages + k), kComputeWarps);
+            mbar_init(bar0 + 8 * (kStages + k), CW);
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -236,12 +279,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     // a multi-wave grid must not, or they would take slots its own later CTAs need.
     if (d.single_wave) pdl_trigger();
 
-    const int mb = warp & 1, kh = warp >> 1;
-    const int g = lane >> 2, c = lane & 3;
-    const int r0 = mb * 16 + g, r1 = r0 + 8;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-    if (warp == kComputeWarps) {
+    if (warp == CW) {
         // ---------------- producer ----------------
         // The whole warp walks the tile list (so every barrier it meets is met by all 32
         // lanes together); lane 0 alone waits on the stage barriers and issues the copies.
@@ -249,10 +287,11 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         bool noise_ready = false;
         int it = 0;
         for (int t = t0; t < t1; ++t) {
-            if (flags[t] == 0) continue;
+            const int flag = flags[t];
+            if (flag == 0) continue;
             if (!noise_ready && t >= tn0 && t <= tn1) {
                 __syncwarp();
-                noise_bar_sync();
+                bar_sync(2, SH::kThreads);
                 noise_ready = true;
             }
             int ok = 1;
@@ -269,18 +308,22 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     const uint32_t full = bar0 + 8 * stg;
                     const uint32_t dk = smem_u32(smem + stg * kStageBytes);
                     const uint32_t dv = dk + kTileBytes;
-                    mbar_expect_tx(full, kStageBytes);
+                    const uint32_t nbits = flag == 2 ? (uint32_t)qw * 8u : 0u;
+                    mbar_expect_tx(full, kStageBytes + nbits);
                     tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
                     tma_load_3d(dk + kHalfBox, &tm_k, 64, t * kTile, zrow, full);
                     tma_load_3d(dv, &tm_v, 0, t * kTile, zrow, full);
                     tma_load_3d(dv + kHalfBox, &tm_v, 64, t * kTile, zrow, full);
+                    if (nbits)
+                        bulk_g2s(smem_u32(smem + kOffBits + stg * kBitsPerStage),
+                                 m.maskbits + (fbase + t) * qw, nbits, full);
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ++it;
         }
         __syncwarp();
-        if (!noise_ready) noise_bar_sync();
+        if (!noise_ready) bar_sync(2, SH::kThreads);
         if (lane == 0) {
             // No copy may land after the CTA exits: wait for the last load of every stage.
             for (int k = max(0, it - kStages); k < it; ++k) {
@@ -293,17 +336,17 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         __syncwarp();
     } else {
         // ---------------- consumers ----------------
-        const int tid = threadIdx.x;    // 0..127
+        const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
         {   // queries of this kv head, RoPE at committed + i, F16, swizzled like K tiles.
             // Item u = (row, 4 consecutive pairs); every load is issued before any use.
             constexpr int kItems = kRows * (kHeadDim / 2) / 4;          // 512
-            constexpr int kPer = kItems / (kComputeWarps * 32);         // 4
+            constexpr int kPer = kItems / SH::kConsumers;
             float4 xa[kPer], xb[kPer], ca[kPer], cb[kPer];
 #pragma unroll
             for (int b = 0; b < kPer; ++b) {
-                const int u = b * kComputeWarps * 32 + tid;
+                const int u = b * SH::kConsumers + tid;
                 const int r = u >> 4, j0 = (u & 15) * 4;
                 if (r < d.rows) {
                     const int hh = r / d.q_len, i = r - hh * d.q_len;
@@ -318,7 +361,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
 #pragma unroll
             for (int b = 0; b < kPer; ++b) {
-                const int u = b * kComputeWarps * 32 + tid;
+                const int u = b * SH::kConsumers + tid;
                 const int r = u >> 4, j0 = (u & 15) * 4;
                 const float x1[4] = {xa[b].x, xa[b].y, xa[b].z, xa[b].w};
                 const float x2[4] = {xb[b].x, xb[b].y, xb[b].z, xb[b].w};
@@ -343,7 +386,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             // (noise row, 8 consecutive pairs); loads first, then stores.
             const int64_t head = ((int64_t)s * d.n_layer + layer) * d.n_head_kv + gk;
             const int n_items = d.q_len * (half / 8);
-            for (int u = tid; u < n_items; u += kComputeWarps * 32) {
+            for (int u = tid; u < n_items; u += SH::kConsumers) {
                 const int i = u / (half / 8), jc = u - i * (half / 8);
                 const uint16_t *ks = k_noise + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + jc * 8;
                 const uint16_t *vs = v_noise + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + jc * 8;
@@ -377,9 +420,12 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-        noise_bar_arrive();
-        named_bar_sync(1, kComputeWarps * 32);
+        bar_arrive(2, SH::kThreads);
+        bar_sync(1, SH::kConsumers);
 
+        const int mb = warp & 1, ksl = warp >> 1;
+        const int g = lane >> 2, c = lane & 3;
+        const int r0 = mb * 16 + g, r1 = r0 + 8;
         uint32_t qf[8][4];
         {
             const uint32_t sqa = smem_u32(sq);
@@ -392,11 +438,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         float oacc[16][4];
 #pragma unroll
         for (int n = 0; n < 16; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
-
+        float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
         const int i0 = r0 < d.rows ? r0 % d.q_len : 0;
         const int i1 = r1 < d.rows ? r1 % d.q_len : 0;
-        const float *mrow0 = maskp + (int64_t)i0 * d.kv_total;
-        const float *mrow1 = maskp + (int64_t)i1 * d.kv_total;
+        const int key0 = ksl * SH::kKeys;
 
         int it = 0;
         for (int t = t0; t < t1; ++t) {
@@ -414,15 +459,15 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const uint32_t sk = smem_u32(smem + stg * kStageBytes);
             const uint32_t sv = sk + kTileBytes;
 
-            // S = Q K^T over this warp's 32 keys (4 n-tiles of 8)
-            float sc[4][4];
+            // S = Q K^T over this warp's keys
+            float sc[SH::kNT][4];
 #pragma unroll
-            for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            for (int n = 0; n < SH::kNT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    const int key = kh * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                for (int np = 0; np < SH::kNT / 2; ++np) {
+                    const int key = key0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(sk + swz(key, ks * 16 + (((lane >> 3) & 1) << 3), kTile), b0, b1, b2, b3);
                     mma16816(sc[np * 2], qf[ks], b0, b1);
@@ -430,58 +475,66 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
             }
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+            for (int n = 0; n < SH::kNT; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[n][e] *= scale_log2;
             if (flag == 2) {
+                // per-row visibility bits of this tile arrived with it
+                const uint64_t w0 = sbits[stg * kMaxQWords + i0], w1 = sbits[stg * kMaxQWords + i1];
 #pragma unroll
-                for (int n = 0; n < 4; ++n)
+                for (int n = 0; n < SH::kNT; ++n)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int slot = t * kTile + kh * 32 + n * 8 + 2 * c + e;
-                        const bool ok = slot < d.kv_total;
-                        sc[n][e] += ok ? __ldg(mrow0 + slot) : -INFINITY;
-                        sc[n][2 + e] += ok ? __ldg(mrow1 + slot) : -INFINITY;
+                        const int bit = key0 + n * 8 + 2 * c + e;
+                        if (!((w0 >> bit) & 1ull)) sc[n][e] = -INFINITY;
+                        if (!((w1 >> bit) & 1ull)) sc[n][2 + e] = -INFINITY;
                     }
             }
 
             // online softmax (log2 domain), rows r0 (j = 0) and r1 (j = 1)
+            float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(fmaxf(sc[0][2 * j], sc[0][2 * j + 1]), fmaxf(sc[1][2 * j], sc[1][2 * j + 1]));
-                mx = fmaxf(mx, fmaxf(fmaxf(sc[2][2 * j], sc[2][2 * j + 1]), fmaxf(sc[3][2 * j], sc[3][2 * j + 1])));
+                float mx = -INFINITY;
+#pragma unroll
+                for (int n = 0; n < SH::kNT; ++n) mx = fmaxf(mx, fmaxf(sc[n][2 * j], sc[n][2 * j + 1]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float mnew = fmaxf(mrow[j], mx);
                 const float muse = mnew == -INFINITY ? 0.f : mnew;
-                const float alpha = exp2f(mrow[j] - muse);
+                alpha[j] = exp2f(mrow[j] - muse);
                 mrow[j] = mnew;
                 float rs = 0.f;
 #pragma unroll
-                for (int n = 0; n < 4; ++n) {
+                for (int n = 0; n < SH::kNT; ++n) {
                     const float p0 = exp2f(sc[n][2 * j] - muse);
                     const float p1 = exp2f(sc[n][2 * j + 1] - muse);
                     sc[n][2 * j] = p0;
                     sc[n][2 * j + 1] = p1;
                     rs += p0 + p1;
                 }
-                lrow[j] = lrow[j] * alpha + rs;
+                lrow[j] = lrow[j] * alpha[j] + rs;
+            }
+            // rescale the numerators only when some row's maximum moved
+            if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
-                    oacc[n][2 * j] *= alpha;
-                    oacc[n][2 * j + 1] *= alpha;
+                    oacc[n][0] *= alpha[0];
+                    oacc[n][1] *= alpha[0];
+                    oacc[n][2] *= alpha[1];
+                    oacc[n][3] *= alpha[1];
                 }
             }
 
-            // O += P V over the same 32 keys (2 k-steps of 16)
+            // O += P V over the same keys
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < SH::kKK; ++kk) {
                 uint32_t pa[4];
                 pa[0] = pack_half2(sc[2 * kk][0], sc[2 * kk][1]);
                 pa[1] = pack_half2(sc[2 * kk][2], sc[2 * kk][3]);
                 pa[2] = pack_half2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
                 pa[3] = pack_half2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-                const int key = kh * 32 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int key = key0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
                 for (int dp = 0; dp < 8; ++dp) {
                     uint32_t b0, b1, b2, b3;
@@ -500,125 +553,121 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             lrow[j] += __shfl_xor_sync(0xffffffffu, lrow[j], 1);
             lrow[j] += __shfl_xor_sync(0xffffffffu, lrow[j], 2);
         }
-
-        // merge the two key halves through stage buffer 0 (idle now)
-        named_bar_sync(1, kComputeWarps * 32);
-        float *xo = reinterpret_cast<float *>(smem);          // [2 mb][64][32 lanes]
-        float *xm = xo + 2 * 64 * 32;                          // [2 mb][2 j][32 lanes]
-        float *xl = xm + 2 * 2 * 32;
-        if (kh == 1) {
-#pragma unroll
-            for (int n = 0; n < 16; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) xo[(mb * 64 + n * 4 + e) * 32 + lane] = oacc[n][e];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                xm[(mb * 2 + j) * 32 + lane] = mrow[j];
-                xl[(mb * 2 + j) * 32 + lane] = lrow[j];
-            }
-        }
-        named_bar_sync(1, kComputeWarps * 32);
-        if (kh == 0) {
+        if constexpr (CLUSTER) {
+            // push this warp's rows to the CTA of the cluster that finishes them
             const int rr[2] = {r0, r1};
-            const bool clustered = cluster_size() > 1;
+            const int slot_p = (int)rank * SH::kSlices + ksl;     // this warp's partial index
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const float m1 = xm[(mb * 2 + j) * 32 + lane], l1 = xl[(mb * 2 + j) * 32 + lane];
-                const float mm = fmaxf(mrow[j], m1);
-                const float muse = mm == -INFINITY ? 0.f : mm;
-                const float a0 = exp2f(mrow[j] - muse), a1 = exp2f(m1 - muse);
-                const float ll = lrow[j] * a0 + l1 * a1;
-                float vals[32];
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    vals[2 * n] = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
-                    vals[2 * n + 1] = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
-                }
                 const int r = rr[j];
-                if (clustered) {
-                    // to this CTA's shared memory; the cluster merges below
-                    float *dst = pacc + r * kPartStride;
+                const int owner = r / rows_per, lr = r - owner * rows_per;
+                float *acc_row = recv_acc + ((int64_t)slot_p * rows_per + lr) * kHeadDim;
+                const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
 #pragma unroll
-                    for (int n = 0; n < 16; ++n)
-                        *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(vals[2 * n], vals[2 * n + 1]);
-                    if (c == 0) {
-                        pml[2 * r] = mm;
-                        pml[2 * r + 1] = ll;
+                for (int n = 0; n < 16; ++n)
+                    st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), oacc[n][2 * j], oacc[n][2 * j + 1]);
+                if (c == 0)
+                    st_cluster_v2(map_rank(smem_u32(recv_ml + slot_p * rows_per + lr), (uint32_t)owner),
+                                  mrow[j], lrow[j]);
+            }
+        } else {
+            // merge the two key halves through stage buffer 0 (idle now), then write this
+            // CTA's rows straight from registers
+            bar_sync(1, SH::kConsumers);
+            float *xo = reinterpret_cast<float *>(smem);          // [2 mb][64][32 lanes]
+            float *xm = xo + 2 * 64 * 32;                          // [2 mb][2 j][32 lanes]
+            float *xl = xm + 2 * 2 * 32;
+            if (ksl == 1) {
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) xo[(mb * 64 + n * 4 + e) * 32 + lane] = oacc[n][e];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    xm[(mb * 2 + j) * 32 + lane] = mrow[j];
+                    xl[(mb * 2 + j) * 32 + lane] = lrow[j];
+                }
+            }
+            bar_sync(1, SH::kConsumers);
+            if (ksl == 0) {
+                const int rr[2] = {r0, r1};
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float m1 = xm[(mb * 2 + j) * 32 + lane], l1 = xl[(mb * 2 + j) * 32 + lane];
+                    const float mm = fmaxf(mrow[j], m1);
+                    const float muse = mm == -INFINITY ? 0.f : mm;
+                    const float a0 = exp2f(mrow[j] - muse), a1 = exp2f(m1 - muse);
+                    const float ll = lrow[j] * a0 + l1 * a1;
+                    const int r = rr[j];
+                    if (d.groups == 1) {
+                        // the only CTA of this (sequence, kv head): final output
+                        if (r < d.rows) {
+                            const int hh = r / d.q_len, i = r - hh * d.q_len;
+                            const int h = gk * d.group + hh;
+                            const float inv = ll > 0.f ? 1.f / ll : 0.f;
+                            float *dst = o + (((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim;
+#pragma unroll
+                            for (int n = 0; n < 16; ++n) {
+                                const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
+                                const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
+                                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0 * inv, v1 * inv);
+                            }
+                        }
+                    } else {
+                        // one of several independent CTAs: partial for the combine kernel
+                        const int64_t base = (((int64_t)s * d.n_head_kv + gk) * d.groups + sp) * kRows + r;
+                        float *dst = m.part_acc + base * kHeadDim;
+#pragma unroll
+                        for (int n = 0; n < 16; ++n) {
+                            const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
+                            const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
+                            *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0, v1);
+                        }
+                        if (c == 0) m.part_ml[base] = make_float2(mm, ll);
                     }
-                } else if (d.groups == 1) {
-                    // the only CTA of this (sequence, kv head): final output
-                    if (r < d.rows) {
-                        const int hh = r / d.q_len, i = r - hh * d.q_len;
-                        const int h = gk * d.group + hh;
-                        const float inv = ll > 0.f ? 1.f / ll : 0.f;
-                        float *dst = o + (((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim;
-#pragma unroll
-                        for (int n = 0; n < 16; ++n)
-                            *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) =
-                                make_float2(vals[2 * n] * inv, vals[2 * n + 1] * inv);
-                    }
-                } else {
-                    // one of several independent CTAs: partial for the combine kernel
-                    const int64_t base = (((int64_t)s * d.n_head_kv + gk) * d.groups + sp) * kRows + r;
-                    float *dst = m.part_acc + base * kHeadDim;
-#pragma unroll
-                    for (int n = 0; n < 16; ++n)
-                        *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(vals[2 * n], vals[2 * n + 1]);
-                    if (c == 0) m.part_ml[base] = make_float2(mm, ll);
                 }
             }
         }
     }
+    if constexpr (!CLUSTER) return;
 
-    const uint32_t nct = cluster_size();
-    if (nct == 1) return;
-    cluster_sync();     // every CTA's merged partial is in its shared memory
-
-    // ---------------- cluster merge: this CTA finishes 32 / cluster rows ----------------
-    const uint32_t rank = cluster_rank();
-    const int rows_per = kRows / (int)nct;
-    if (threadIdx.x < kHeadDim) {
-        const int col = threadIdx.x;
-        const uint32_t pacc_a = smem_u32(pacc), pml_a = smem_u32(pml);
-        const int group = sp / (int)nct;
-        for (int rr = (int)rank * rows_per; rr < ((int)rank + 1) * rows_per; ++rr) {
-            float mv[16], lv[16], av[16];
-#pragma unroll
-            for (int cr = 0; cr < 16; ++cr) {
-                if (cr < (int)nct) {
-                    mv[cr] = ld_cluster(map_rank(pml_a + 8 * rr, cr));
-                    lv[cr] = ld_cluster(map_rank(pml_a + 8 * rr + 4, cr));
-                    av[cr] = ld_cluster(map_rank(pacc_a + 4 * (rr * kPartStride + col), cr));
-                }
+    // ---------------- cluster merge: this CTA finishes rows [rank * rows_per, +rows_per) ----
+    cluster_sync();     // every partial of this CTA's rows is in its receive buffer
+    const int n_part = (int)nct * SH::kSlices;
+    const int items = rows_per * (kHeadDim / 4);
+    for (int u = threadIdx.x; u < items; u += SH::kThreads) {
+        const int lr = u / (kHeadDim / 4), c4 = (u % (kHeadDim / 4)) * 4;
+        float mm = -INFINITY;
+        for (int p = 0; p < n_part; ++p) mm = fmaxf(mm, recv_ml[p * rows_per + lr].x);
+        const float muse = mm == -INFINITY ? 0.f : mm;
+        float l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < n_part; ++p) {
+            const float2 ml = recv_ml[p * rows_per + lr];
+            const float w = exp2f(ml.x - muse);
+            l += w * ml.y;
+            const float4 v = *reinterpret_cast<const float4 *>(recv_acc + ((int64_t)p * rows_per + lr) * kHeadDim + c4);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const int r = (int)rank * rows_per + lr;
+        if (d.groups == 1) {
+            if (r < d.rows) {
+                const int hh = r / d.q_len, i = r - hh * d.q_len;
+                const int h = gk * d.group + hh;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                *reinterpret_cast<float4 *>(o + (((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim + c4) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             }
-            float mm = -INFINITY;
-#pragma unroll
-            for (int cr = 0; cr < 16; ++cr)
-                if (cr < (int)nct) mm = fmaxf(mm, mv[cr]);
-            const float muse = mm == -INFINITY ? 0.f : mm;
-            float l = 0.f, acc = 0.f;
-#pragma unroll
-            for (int cr = 0; cr < 16; ++cr) {
-                if (cr < (int)nct) {
-                    const float w = exp2f(mv[cr] - muse);
-                    l += w * lv[cr];
-                    acc += w * av[cr];
-                }
-            }
-            if (d.groups == 1) {
-                if (rr < d.rows) {
-                    const int hh = rr / d.q_len, i = rr - hh * d.q_len;
-                    const int h = gk * d.group + hh;
-                    o[(((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim + col] = l > 0.f ? acc / l : 0.f;
-                }
-            } else {
-                const int64_t base = (((int64_t)s * d.n_head_kv + gk) * d.groups + group) * kRows + rr;
-                m.part_acc[base * kHeadDim + col] = acc;
-                if (col == 0) m.part_ml[base] = make_float2(mm, l);
-            }
+        } else {
+            const int group = sp / (int)nct;
+            const int64_t base = (((int64_t)s * d.n_head_kv + gk) * d.groups + group) * kRows + r;
+            *reinterpret_cast<float4 *>(m.part_acc + base * kHeadDim + c4) = acc;
+            if (c4 == 0) m.part_ml[base] = make_float2(mm, l);
         }
     }
-    cluster_sync();     // keep this CTA's shared memory alive until the cluster has read it
 }
 
 // ---------------------------------------------------------------------------------
@@ -665,25 +714,35 @@ k_attend_combine(RingDims d, RingDev m, float *o) {
 
 }  // namespace
 
-size_t attend_smem_bytes() { return (size_t)kSmemBytes; }
+size_t attend_smem_bytes() { return (size_t)Shape<true>::kSmem; }
 
 cudaError_t attend_kernels_init() {
-    cudaError_t e = cudaFuncSetAttribute(k_attend, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_attend<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Shape<true>::kSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attend, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(k_attend<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attend<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Shape<false>::kSmem);
     return e;
 }
 
-int attend_max_cluster() {
+int attend_cluster_capacity(int cluster) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    int n = 1;
-    if (cudaOccupancyMaxPotentialClusterSize(&n, k_attend, &cfg) != cudaSuccess) {
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(Shape<true>::kThreads);
+    cfg.dynamicSmemBytes = Shape<true>::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_attend<true>, &cfg) != cudaSuccess) {
         cudaGetLastError();
-        return 1;
+        return 0;
     }
     return n;
 }
@@ -692,22 +751,33 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
                           const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
                           float *o, bool pdl, cudaStream_t st) {
+    const bool clustered = d.cluster > 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.n_splits, d.n_head_kv, d.n_seq);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(clustered ? Shape<true>::kThreads : Shape<false>::kThreads);
+    cfg.dynamicSmemBytes = clustered ? Shape<true>::kSmem : Shape<false>::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = d.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    int na = 0;
+    if (clustered) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = d.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_attend, *tm_k, *tm_v, d, m, layer, kind, scale_log2, q,
-                              k_noise, v_noise, o);
+    cfg.numAttrs = na;
+    if (clustered)
+        return cudaLaunchKernelEx(&cfg, k_attend<true>, *tm_k, *tm_v, d, m, layer, kind,
+                                  scale_log2, q, k_noise, v_noise, o);
+    return cudaLaunchKernelEx(&cfg, k_attend<false>, *tm_k, *tm_v, d, m, layer, kind, scale_log2,
+                              q, k_noise, v_noise, o);
 }
 
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,

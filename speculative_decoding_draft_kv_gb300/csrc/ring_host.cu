@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -173,30 +174,34 @@ int pow2_ceil(int x) {
 
 // Work split of the attention kernel.  A thread-block cluster holds every one of its SM
 // slots until its slowest CTA is done, so clusters (merging through distributed shared
-// memory, no second kernel) are used only when the whole grid fits in one wave of two
-// CTAs per SM -- the few-sequence case, where latency rules.  Otherwise each CTA is its
-// own group: about four waves of independent CTAs stream the tiles and a small combine
-// kernel merges the per-CTA partials.
+// memory, no second kernel) are used only when the whole grid fits in one wave of one
+// CTA per SM -- the few-sequence case, where latency rules.  Otherwise each CTA is its
+// own group: about four waves of independent CTAs (two per SM) stream the tiles and a
+// small combine kernel merges the per-CTA partials.
 void choose_split(RingDims &d, int sms, int max_cluster, int tps_req) {
     const int cmax = std::max(1, std::min(16, pow2_floor(std::max(1, max_cluster))));
-    const int slots = 2 * std::max(sms, 1);
     const int pairs = d.n_seq * d.n_head_kv;
     if (tps_req > 0) {
         const int tps = std::min(tps_req, d.n_tiles);
         const int ns = (d.n_tiles + tps - 1) / tps;
         d.cluster = std::min(cmax, pow2_floor(ns));
+        while (d.cluster > 1 && attend_cluster_capacity(d.cluster) < 1) d.cluster /= 2;
         d.groups = (ns + d.cluster - 1) / d.cluster;
         d.tiles_per_split = tps;
         d.n_splits = d.cluster * d.groups;
         return;
     }
-    int c = std::min(cmax, pow2_floor(std::max(1, slots / pairs)));
-    c = std::min(c, pow2_ceil(d.n_tiles));
+    // widest cluster whose whole grid (pairs clusters) is resident at once
+    int c = std::min(cmax, pow2_ceil(d.n_tiles));
+    while (c > 1 && ((int64_t)attend_cluster_capacity(c) < pairs ||
+                     (int64_t)pairs * c > std::max(sms, 1)))
+        c /= 2;
     if (c >= 2 && (d.n_tiles + c - 1) / c <= 128) {
         d.cluster = c;
         d.groups = 1;
         d.tiles_per_split = (d.n_tiles + c - 1) / c;
     } else {
+        const int slots = 2 * std::max(sms, 1);
         const int64_t work = (int64_t)pairs * d.n_tiles;
         int64_t tps = (work + 4LL * slots - 1) / (4LL * slots);
         tps = std::max<int64_t>(2, std::min<int64_t>(64, tps));
@@ -244,7 +249,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         return fail(nullptr, RING_EINVAL, "ring_init: head_dim %d unsupported (needs %d)",
                     p->head_dim, kHeadDim);
     const int group = p->n_head / p->n_head_kv;
-    if ((int64_t)group * p->q_len > kRows)
+    if ((int64_t)group * p->q_len > kRows || p->q_len > kMaxQWords)
         return fail(nullptr, RING_EINVAL,
                     "ring_init: (n_head/n_head_kv)*q_len = %d exceeds %d query rows per kv head",
                     group * p->q_len, kRows);
@@ -287,10 +292,13 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         delete r;
         return rc;
     }
-    int max_cluster = attend_max_cluster();
-    if (p->max_cluster > 0) max_cluster = std::min(max_cluster, p->max_cluster);
+    int max_cluster = p->max_cluster > 0 ? p->max_cluster : 16;
     choose_split(d, sms, max_cluster, p->tiles_per_split);
-    d.single_wave = (int64_t)d.n_splits * d.n_head_kv * d.n_seq <= 2LL * std::max(sms, 1) ? 1 : 0;
+    {
+        const int64_t ctas = (int64_t)d.n_splits * d.n_head_kv * d.n_seq;
+        const int64_t resident = (d.cluster > 1 ? 1LL : 2LL) * std::max(sms, 1);
+        d.single_wave = ctas <= resident ? 1 : 0;
+    }
 
     const size_t kv_elems = (size_t)d.n_seq * d.n_layer * d.n_head_kv * d.kv_total * d.head_dim;
     RingDev &m = r->m;
@@ -308,6 +316,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     ALLOC(m.slot_pos, int32_t, (size_t)d.n_seq * d.cap);
     ALLOC(m.mask, float, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total);
     ALLOC(m.flags, uint8_t, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
+    ALLOC(m.maskbits, uint64_t, (size_t)d.n_seq * d.n_kinds * d.n_tiles * ((d.q_len + 1) & ~1));
     ALLOC(m.steps, SeqStep, d.n_seq);
     ALLOC(m.rope32, float2, (size_t)d.n_seq * d.q_len * d.head_dim / 2);
     ALLOC(m.part_acc, float, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows * kHeadDim);
@@ -326,6 +335,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     zero(m.slot_pos, 0xff, (size_t)d.n_seq * d.cap * 4);
     zero(m.mask, 0, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total * 4);
     zero(m.flags, 0, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
+    zero(m.maskbits, 0, (size_t)d.n_seq * d.n_kinds * d.n_tiles * ((d.q_len + 1) & ~1) * 8);
     zero(m.steps, 0, sizeof(SeqStep) * d.n_seq);
     zero(m.rope32, 0, (size_t)d.n_seq * d.q_len * d.head_dim / 2 * sizeof(float2));
     zero(m.err, 0, 4);

@@ -7,6 +7,9 @@
 //   slot_pos  I32  [n_seq][cap]                         -1 = never written
 //   mask      F32  [n_seq][n_kinds][q_len][kv_total]    0 or -inf
 //   flags     U8   [n_seq][n_kinds][n_tiles]            0 none / 1 all / 2 mixed visible
+//   maskbits  U64  [n_seq][n_kinds][n_tiles][qw]        bit b of row i: slot 64*tile + b
+//                                                       visible to query i (qw = q_len
+//                                                       rounded up to even)
 //   steps     SeqStep[n_seq]                            this step's window, per sequence
 //   rope32    F32x2[n_seq][q_len][head_dim/2]           cos, sin of the noise positions
 //   part_acc  F32  [n_seq][n_head_kv][groups][32][head_dim]  cluster-group partial numerators
@@ -30,6 +33,7 @@ constexpr int kHeadDim = 128;     // head_dim supported by the attention kernel
 constexpr int kTile = 64;         // slots per attention tile
 constexpr int kRows = 32;         // query rows per kv head held by one CTA (G * q_len, padded)
 constexpr int kMaxKinds = 2;      // mask_full, mask_swa
+constexpr int kMaxQWords = 32;    // visibility words per tile (q_len <= 32, rounded to even)
 
 // Device error bits.
 constexpr uint32_t kErrWaitFull = 1u;     // consumer timed out on a stage's load
@@ -51,7 +55,7 @@ struct RingDims {
     int a_step, trash_slot, kv_total, kv_row, group, rows;
     int n_tiles, tiles_per_split, n_splits, n_kinds, bulk_chunk;
     int cluster, groups;
-    int single_wave;      // attention grid fits in one wave of two CTAs per SM
+    int single_wave;      // attention grid fits in one wave (all its CTAs resident at once)
 };
 
 struct RingDev {
@@ -59,6 +63,7 @@ struct RingDev {
     int32_t *slot_pos;
     float *mask;
     uint8_t *flags;
+    uint64_t *maskbits;
     SeqStep *steps;
     float2 *rope32;
     float *part_acc;
@@ -106,7 +111,8 @@ cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_
 
 // ---- launchers (attn_kernels.cu) ----
 cudaError_t attend_kernels_init();   // per device, before the first launch
-int attend_max_cluster();            // largest cluster the attention kernel can launch with
+// clusters of `cluster` CTAs that can be resident at once (0 if none)
+int attend_cluster_capacity(int cluster);
 // scale_log2 = log2(e) / sqrt(head_dim): the softmax runs in base 2.
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,

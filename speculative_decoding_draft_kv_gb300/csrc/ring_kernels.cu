@@ -97,14 +97,17 @@ __device__ void pad_row(const RingDims &d, const RingDev &m, int s) {
     }
 }
 
-// Masks and flags of one 64-slot tile.  The slot_pos a slot holds after this step is
-// computed here rather than read back: a slot written by this step's fold-in rows holds
-// start + k with k = (slot - start) mod cap < fold_rows; any other slot keeps its value
-// (already updated by the bulk kernels, which run before this one).
+// Masks, visibility bits and flags of one 64-slot tile.  The slot_pos a slot holds after
+// this step is computed here rather than read back: a slot written by this step's
+// fold-in rows holds start + k with k = (slot - start) mod cap < fold_rows; any other
+// slot keeps its value (already updated by the bulk kernels, which run before this one).
+// Threads 0-63 own one slot each (warps 0 and 1); warps 2 and 3 only join the barriers.
 __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, const SeqStep &st) {
     const int slot = tile * kTile + (int)threadIdx.x;
     const bool active = threadIdx.x < kTile;
     const bool in_range = active && slot < d.kv_total;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qw = (d.q_len + 1) & ~1;
     bool ctx_full = false, ctx_swa = false;
     int noise_j = -1;
     if (active && slot < d.cap) {
@@ -117,30 +120,32 @@ __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, 
         noise_j = slot - d.cap;
     }
     const float ninf = __int_as_float(0xff800000);
-    {   // mask_full: the same row for every query (noise block bidirectional)
-        float *mk = m.mask + (int64_t)s * d.n_kinds * d.q_len * d.kv_total;
-        const bool vis = ctx_full || noise_j >= 0;
-        if (in_range)
-            for (int i = 0; i < d.q_len; ++i) mk[(int64_t)i * d.kv_total + slot] = vis ? 0.f : ninf;
-        const int all = __syncthreads_and(!active || (in_range && vis));
-        const int any = __syncthreads_or(in_range && vis);
-        if (threadIdx.x == 0)
-            m.flags[((int64_t)s * d.n_kinds) * d.n_tiles + tile] = any ? (all ? 1 : 2) : 0;
-    }
-    if (d.n_kinds > 1) {
-        // mask_swa: window anchored at committed for every row; noise causal (j <= i)
-        float *mk = m.mask + ((int64_t)s * d.n_kinds + 1) * d.q_len * d.kv_total;
+    for (int kind = 0; kind < d.n_kinds; ++kind) {
+        const int64_t fi = ((int64_t)s * d.n_kinds + kind) * d.n_tiles + tile;
+        float *mk = m.mask + ((int64_t)s * d.n_kinds + kind) * d.q_len * d.kv_total;
+        uint32_t *bits = reinterpret_cast<uint32_t *>(m.maskbits + fi * qw);
         bool all_rows = true, any_row = false;
-        for (int i = 0; i < d.q_len; ++i) {
-            const bool vis = ctx_swa || (noise_j >= 0 && noise_j <= i);
-            if (in_range) mk[(int64_t)i * d.kv_total + slot] = vis ? 0.f : ninf;
-            all_rows = all_rows && vis;
-            any_row = any_row || vis;
+        for (int i = 0; i < qw; ++i) {
+            // mask_full: window [lo, c), noise bidirectional; mask_swa: window anchored at
+            // committed for every row, noise causal (j <= i)
+            bool vis = false;
+            if (i < d.q_len)
+                vis = kind == 0 ? (ctx_full || noise_j >= 0)
+                                : (ctx_swa || (noise_j >= 0 && noise_j <= i));
+            vis = vis && in_range;
+            if (in_range && i < d.q_len) mk[(int64_t)i * d.kv_total + slot] = vis ? 0.f : ninf;
+            if (warp < 2) {
+                const uint32_t b = __ballot_sync(0xffffffffu, vis);
+                if (lane == 0) bits[2 * i + warp] = b;
+            }
+            if (i < d.q_len) {
+                all_rows = all_rows && vis;
+                any_row = any_row || vis;
+            }
         }
-        const int all = __syncthreads_and(!active || (in_range && all_rows));
-        const int any = __syncthreads_or(in_range && any_row);
-        if (threadIdx.x == 0)
-            m.flags[((int64_t)s * d.n_kinds + 1) * d.n_tiles + tile] = any ? (all ? 1 : 2) : 0;
+        const int all = __syncthreads_and(!active || all_rows);
+        const int any = __syncthreads_or(active && any_row);
+        if (threadIdx.x == 0) m.flags[fi] = any ? (all ? 1 : 2) : 0;
     }
 }
 
