@@ -211,8 +211,43 @@ int ring_profile_read(ring_t *r, ring_profile *out);
 /* ring_launch_count -- kernels this ring has launched since ring_init. */
 int64_t ring_launch_count(const ring_t *r);
 
+/*
+ * ring_attend_static -- the attention of ring_attend for callers that cannot allocate
+ * device memory (no counterpart on the page: it exists for hosts whose framework owns
+ * every device allocation, or that run where a runtime allocation is not allowed, and
+ * so cannot create a ring).  Every buffer comes from the caller; nothing is allocated.
+ *
+ *   k, v       device F16 [n_seq][n_head_kv][kv_total][head_dim]: one layer's ring K/V,
+ *              kv_total = align_up(cap + q_len + 1, 32).  In/out: the noise block's rows
+ *              are written to slots cap .. cap+q_len-1 exactly as ring_attend writes them.
+ *   mask       device F32 [n_seq][q_len][kv_total]: 0 = visible, -inf = hidden (the
+ *              layout ring_get_mask returns).
+ *   committed  host int64[n_seq]: queries and noise keys turn by RoPE at committed + i.
+ *   q, k_noise, v_noise, o   as for ring_attend.
+ *
+ * Scratch (tile flags, visibility bits, the RoPE table, split partials) lives in one
+ * static device array of 16 MiB, which every GPU that loads this library holds until the
+ * process exits.  The first call on a device looks up that array's device address (with
+ * that device current); make that first call before any stream capture.  Every call on a
+ * device shares the array, so calls that overlap on the GPU race: issue them on one
+ * stream.  Shapes whose scratch exceeds 16 MiB, or n_seq above 256, fail with
+ * RING_ERANGE.  Errors: EINVAL, ERANGE, ECUDA (message in ring_last_error(NULL)).
+ */
+typedef struct ring_attend_static_args {
+    int32_t cap, q_len, head_dim, n_head_kv, n_head, n_seq;
+    float rope_theta;
+    const int64_t *committed;
+    void *k, *v;
+    const float *mask;
+    const float *q;
+    const void *k_noise, *v_noise;
+    float *o;
+} ring_attend_static_args;
+
+int ring_attend_static(const ring_attend_static_args *args, void *stream);
+
 /* ring_last_error -- message of the last failing call on r (or of the last failed
- * ring_init when r is NULL).  Never NULL. */
+ * ring_init or ring_attend_static when r is NULL).  Never NULL. */
 const char *ring_last_error(const ring_t *r);
 
 #ifdef __cplusplus

@@ -14,6 +14,7 @@ from .ring import (  # noqa: F401
     Ring,
     RingError,
     ring_attend,
+    ring_attend_static,
     ring_begin_step,
     ring_describe,
     ring_destroy,

@@ -1,6 +1,6 @@
 """Build the ring's CUDA library in-tree (``_lib/libdflash_ring.so``) with nvcc for sm_103a.
 
-Three translation units are compiled in parallel and linked into one shared library
+The translation units are compiled in parallel and linked into one shared library
 with the CUDA runtime linked statically; nothing else (no PyTorch, no cmake) is needed.
 """
 
@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libdflash_ring.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 
-SOURCES = ["ring_host.cu", "ring_kernels.cu", "attn_kernels.cu"]
+SOURCES = ["ring_host.cu", "ring_kernels.cu", "attn_kernels.cu", "static_attend.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -217,6 +217,13 @@ bool check_seq(ring_t *r, int32_t seq) { return r && seq >= 0 && seq < r->d.n_se
 
 }  // namespace
 
+namespace dflash {
+bool encode_kv_tensor_map(CUtensorMap *tm, void *base, const RingDims &d) {
+    return encode_kv_map(tm, base, d);
+}
+void set_global_error(const char *msg) { g_init_error = msg; }
+}  // namespace dflash
+
 extern "C" {
 
 int ring_init(ring_t **out, int32_t cap, int32_t q_len, int32_t head_dim, int32_t n_head_kv,

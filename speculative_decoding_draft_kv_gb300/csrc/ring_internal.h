@@ -109,6 +109,13 @@ cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
                               cudaStream_t st);
 
+// ---- shared host helpers (ring_host.cu) ----
+// 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],
+// 64 x 64 boxes, 128-byte swizzle.
+bool encode_kv_tensor_map(CUtensorMap *tm, void *base, const RingDims &d);
+// Message returned by ring_last_error(NULL) on this thread.
+void set_global_error(const char *msg);
+
 // ---- launchers (attn_kernels.cu) ----
 cudaError_t attend_kernels_init();   // per device, before the first launch
 // clusters of `cluster` CTAs that can be resident at once (0 if none)

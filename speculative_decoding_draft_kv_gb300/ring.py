@@ -32,7 +32,8 @@ EXPORTED = (
     "ring_init", "ring_init_ex", "ring_destroy", "ring_get_geometry", "ring_rows_needed",
     "ring_begin_step", "ring_attend", "ring_get_slot_pos", "ring_get_mask",
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
-    "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_last_error",
+    "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
+    "ring_last_error",
 )
 
 
@@ -57,6 +58,17 @@ class RingGeometry(ctypes.Structure):
         "n_head", "n_layer", "n_seq", "swa_window", "bulk_chunk", "tile_slots", "n_tiles",
         "tiles_per_split", "n_splits", "cluster", "groups")] + [("cache_bytes", ctypes.c_int64),
                                            ("device_bytes", ctypes.c_int64)]
+
+
+class RingAttendStaticArgs(ctypes.Structure):
+    _fields_ = [("cap", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_head_kv", ctypes.c_int32),
+                ("n_head", ctypes.c_int32), ("n_seq", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float),
+                ("committed", ctypes.POINTER(ctypes.c_int64)),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("k_noise", ctypes.c_void_p),
+                ("v_noise", ctypes.c_void_p), ("o", ctypes.c_void_p)]
 
 
 class RingProfile(ctypes.Structure):
@@ -98,6 +110,7 @@ def _load():
         "ring_profile_enable": ([vp, i32], ctypes.c_int),
         "ring_profile_read": ([vp, ctypes.POINTER(RingProfile)], ctypes.c_int),
         "ring_launch_count": ([vp], ctypes.c_int64),
+        "ring_attend_static": ([ctypes.POINTER(RingAttendStaticArgs), vp], ctypes.c_int),
         "ring_last_error": ([vp], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -281,6 +294,27 @@ def ring_profile_read(h) -> dict:
 
 def ring_launch_count(h) -> int:
     return int(_load().ring_launch_count(h))
+
+
+def ring_attend_static(cap, q_len, n_head_kv, n_head, rope_theta, committed, k, v, mask, q,
+                       k_noise, v_noise, o, head_dim=128, stream=None):
+    """One layer's attention over caller-owned buffers, allocating nothing.
+
+    k, v: CUDA float16 [n_seq, n_head_kv, kv_total, head_dim] (noise rows written back);
+    mask: CUDA float32 [n_seq, q_len, kv_total]; q, o: CUDA float32
+    [n_seq, q_len, n_head, head_dim]; noise rows: CUDA float16 [n_seq, q_len, kv_row].
+    """
+    import torch
+    n_seq = int(q.shape[0])
+    c_arr, c_ptr = _i64_array(committed, n_seq, "committed")
+    args = RingAttendStaticArgs(cap, q_len, head_dim, n_head_kv, n_head, n_seq, float(rope_theta),
+                                c_ptr, _dev_ptr(k, torch.float16, "k"), _dev_ptr(v, torch.float16, "v"),
+                                _dev_ptr(mask, torch.float32, "mask"), _dev_ptr(q, torch.float32, "q"),
+                                _dev_ptr(k_noise, torch.float16, "k_noise"),
+                                _dev_ptr(v_noise, torch.float16, "v_noise"),
+                                _dev_ptr(o, torch.float32, "o"))
+    _check(_load().ring_attend_static(ctypes.byref(args), _stream(stream)), None,
+           "ring_attend_static")
 
 
 class Ring:
