@@ -36,7 +36,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_117_184, "kernel": "3a842b1bf64ebf66",
+                                    "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
+}
 
 
 def _kernel_source_hash() -> str:
@@ -120,56 +123,55 @@ class Prepared:
     pass
 
 
-def prepare(w, n_steps, mask, rank, dev, pool):
+def prepare(w, n_steps, rank, dev):
+    """Everything the timed steps read, resident in HBM: one buffer with every step's new
+    context rows (a step addresses its rows through row_off), fixed per-layer query,
+    noise-row and output buffers."""
     import numpy as np
     import torch
 
     import synth
 
-    sched = synth.commit_schedule(w, n_steps)          # row 0: prefill
+    # row 0 is the untimed first call (the prefill where the workload has one)
+    sched = synth.commit_schedule(w, n_steps + (0 if w.kind in ("decode", "batched", "large") else 1))
     P = Prepared()
     P.sched = sched
     S, L = w.n_seq, w.n_layer
     seq_ids = [rank * S + s for s in range(S)]
-    # per-step new rows [start, c) for every sequence, concatenated
     next_pos = np.zeros(S, np.int64)
-    steps = []
+    plan = []
+    total = 0
     for t in range(sched.shape[0]):
         c = sched[t]
-        win = np.minimum(c, w.cap)
-        start = np.maximum(next_pos, c - win)
+        start = np.maximum(next_pos, c - np.minimum(c, w.cap))
         counts = (c - start).astype(np.int64)
-        n_rows = int(counts.sum())
-        row_off = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
-        k_rows = v_rows = None
-        if n_rows:
-            k_rows = torch.empty((L, n_rows, w.kv_row), dtype=torch.float16, device=dev)
-            v_rows = torch.empty_like(k_rows)
-            for s in range(S):
-                if counts[s] == 0:
-                    continue
-                pos = torch.arange(int(start[s]), int(c[s]), device=dev)
-                a, b = int(row_off[s]), int(row_off[s] + counts[s])
-                for layer in range(L):
-                    k, v = synth.context_rows(w.seed, seq_ids[s], layer, pos, w.kv_row, w.sigma, device=dev)
-                    k_rows[layer, a:b] = k
-                    v_rows[layer, a:b] = v
-        steps.append((c.copy(), k_rows, v_rows, row_off, start.copy(), int(counts.sum())))
+        row_off = total + np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
+        plan.append((c.copy(), row_off, start.copy(), counts))
+        total += int(counts.sum())
         next_pos = c.copy()
-    P.steps = steps
-    # a pool of distinct per-step layer inputs (queries and noise rows), cycled
-    P.inputs = []
-    for j in range(pool):
-        per_layer = []
-        for layer in range(L):
-            q = torch.stack([synth.query_block(w.seed, j, sid, layer, w.q_len, w.n_head, w.head_dim,
-                                               w.sigma, device=dev) for sid in seq_ids])
-            kn, vn = zip(*[synth.noise_rows(w.seed, j, sid, layer, w.q_len, w.kv_row, w.sigma,
-                                            device=dev) for sid in seq_ids])
-            per_layer.append((q, torch.stack(kn), torch.stack(vn)))
-        P.inputs.append(per_layer)
-    P.outputs = [torch.empty((S, w.q_len, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
-                 for _ in range(L)]
+    P.k_all = torch.empty((L, max(total, 1), w.kv_row), dtype=torch.float16, device=dev)
+    P.v_all = torch.empty_like(P.k_all)
+    for c, row_off, start, counts in plan:
+        for s in range(S):
+            if counts[s] == 0:
+                continue
+            pos = torch.arange(int(start[s]), int(c[s]), device=dev)
+            a, b = int(row_off[s]), int(row_off[s] + counts[s])
+            for layer in range(L):
+                k, v = synth.context_rows(w.seed, seq_ids[s], layer, pos, w.kv_row, w.sigma, device=dev)
+                P.k_all[layer, a:b] = k
+                P.v_all[layer, a:b] = v
+    P.plan = plan
+    P.q, P.kn, P.vn = [], [], []
+    for layer in range(L):
+        P.q.append(torch.stack([synth.query_block(w.seed, 0, sid, layer, w.q_len, w.n_head, w.head_dim,
+                                                  w.sigma, device=dev) for sid in seq_ids]))
+        kn, vn = zip(*[synth.noise_rows(w.seed, 0, sid, layer, w.q_len, w.kv_row, w.sigma, device=dev)
+                       for sid in seq_ids])
+        P.kn.append(torch.stack(kn))
+        P.vn.append(torch.stack(vn))
+    P.o = [torch.empty((S, w.q_len, w.n_head, w.head_dim), dtype=torch.float32, device=dev)
+           for _ in range(L)]
     return P
 
 
@@ -182,6 +184,33 @@ def visible_rows(w, committed, mask):
             win = min(win, w.swa_window)
         tot += win + w.q_len
     return tot
+
+
+def shard_sequences(rank: int, world: int, n_seq: int):
+    """Weak scaling: every rank owns n_seq independent rings of its own, numbered
+    rank * n_seq + s in the seeded generator (no data is exchanged between ranks)."""
+    return [rank * n_seq + s for s in range(n_seq)]
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The job's time is its slowest rank's time."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _workload(args):
+    import synth
+    w = synth.workload(args.workload)
+    if args.mask == "swa" and not w.swa_window:
+        w = synth.workload(args.workload, swa_window=2048)
+    if args.n_seq:
+        w = synth.workload(args.workload, n_seq=args.n_seq, swa_window=w.swa_window,
+                           name=w.name.replace(f"_s{w.n_seq}_", f"_s{args.n_seq}_"))
+    return w
 
 
 def run_gb300(args):
@@ -200,12 +229,9 @@ def run_gb300(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     B.build()
-    w = synth.workload(args.workload)
-    if args.mask == "swa" and not w.swa_window:
-        w = synth.workload(args.workload, swa_window=2048)
+    w = _workload(args)
     K, W = args.steps, args.warmup
-    pool = min(K + W, args.pool)
-    P = prepare(w, K + W, args.mask, rank, dev, pool)
+    P = prepare(w, K + W, rank, dev)
     stream = torch.cuda.current_stream()
     kind = args.mask
 
@@ -213,8 +239,8 @@ def run_gb300(args):
         r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
                    n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
                    max_cluster=args.max_cluster)
-        c, k_rows, v_rows, row_off, start, _ = P.steps[0]      # prefill (bulk path), untimed
-        r.begin_step(c, k_rows, v_rows, row_off, start, stream)
+        c, row_off, start, _ = P.plan[0]             # prefill (bulk path), untimed
+        r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
         torch.cuda.synchronize()
         return r
 
@@ -223,15 +249,17 @@ def run_gb300(args):
     flush = g["cache_bytes"] * w.n_seq < 2 * L2_BYTES
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
 
-    def step(r, t):
-        c, k_rows, v_rows, row_off, start, _ = P.steps[t]
-        r.begin_step(c, k_rows, v_rows, row_off, start, stream)
-        inp = P.inputs[t % pool]
-        for layer in range(w.n_layer):
-            q, kn, vn = inp[layer]
-            r.attend(layer, kind, q, kn, vn, P.outputs[layer], stream)
+    def step_graph(r, t):
+        c, row_off, start, _ = P.plan[t]
+        r.step(c, P.k_all, P.v_all, row_off, start, kind, P.q, P.kn, P.vn, P.o, stream)
 
-    def timed_loop(r, t0, n, pre=None, post=None):
+    def step_calls(r, t):
+        c, row_off, start, _ = P.plan[t]
+        r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
+        for layer in range(w.n_layer):
+            r.attend(layer, kind, P.q[layer], P.kn[layer], P.vn[layer], P.o[layer], stream)
+
+    def timed_loop(r, step, t0, n, pre=None, post=None):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for j in range(n):
@@ -247,8 +275,11 @@ def run_gb300(args):
                 flush_buf.fill_(j & 0xFF)
         return evs
 
-    # ---- pass 1: warm-up, then exactly K timed steps ----
-    timed_loop(ring, 1, W)
+    def ms_of(evs):
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    # ---- pass 1: the step graph; warm-up, then exactly K timed steps ----
+    timed_loop(ring, step_graph, 1, W)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -257,94 +288,107 @@ def run_gb300(args):
     if rank == 0:
         sampler.start()
     launches0 = ring.launch_count()
-    evs = timed_loop(ring, 1 + W, K)
+    evs = timed_loop(ring, step_graph, 1 + W, K)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     launches = ring.launch_count() - launches0
     clocks = sampler.stop() if rank == 0 else None
-    ms_total = sum(a.elapsed_time(b) for a, b in evs)
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
-    ms_per_step = ms_total / K
+    ms_per_step = max_over_ranks(ms_of(evs), dist, dev) / K
     assert ring.device_error() == 0
     ring.close()
 
-    # ---- pass 2: the same steps again on a fresh ring, events around each attention launch ----
-    n_prof = min(K + W, 400)
+    # ---- pass 2: the same steps as separate calls (begin_step + attend per layer) ----
+    n2 = min(K + W, 400)
+    ring = new_ring()
+    evs = timed_loop(ring, step_calls, 1, n2)
+    torch.cuda.synchronize()
+    ms_calls = max_over_ranks(ms_of(evs), dist, dev) / n2
+    ring.close()
+
+    # ---- pass 3: separate calls with events around every kernel launch ----
     ring = new_ring()
     R.ring_profile_enable(ring.h, True)
-    timed_loop(ring, 1, n_prof)
+    timed_loop(ring, step_calls, 1, n2)
     torch.cuda.synchronize()
     prof = R.ring_profile_read(ring.h)
     R.ring_profile_enable(ring.h, False)
     ring.close()
     attn = prof["attend"]
     attn_ms = attn["total_ms"] / max(attn["launches"], 1)
-    vis = float(np.mean([visible_rows(w, P.steps[1 + j][0], kind) for j in range(n_prof)]))
+    vis = float(np.mean([visible_rows(w, P.plan[1 + j][0], kind) for j in range(n2)]))
     kv_bytes = vis * w.kv_row * 2 * 2
-    q_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 2
+    q_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
     o_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
     alg_bytes = kv_bytes + q_bytes + o_bytes
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (attn_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes"] if tr and tr.get("kernel") == _kernel_source_hash() else None
-    shares = {k: v["total_ms"] for k, v in prof.items()}
+    shares = {k: v["total_ms"] for k, v in prof.items() if k != "step_graph"}
     tot = sum(shares.values()) or 1.0
     shares = {k: round(v / tot, 4) for k, v in shares.items()}
 
-    # ---- pass 3: end to end with host buffers (pinned H2D of each step's rows, queries and
-    # noise rows; D2H of every layer's output), on a fresh ring ----
+    # ---- pass 4: end to end through ring_step with host buffers: every step copies its
+    # new rows, queries and noise rows from pinned host memory and reads every layer's
+    # output back ----
     e2e_obj = None
     if not args.no_e2e:
-        n_e2e = min(K + W, 400)
-        host_rows = {}
-        for t in range(1, 1 + n_e2e):
-            _, k_rows, v_rows, _, _, _ = P.steps[t]
-            if k_rows is not None:
-                host_rows[t] = (k_rows.cpu().pin_memory(), v_rows.cpu().pin_memory())
-        host_inp = [[tuple(x.cpu().pin_memory() for x in trip) for trip in per_layer]
-                    for per_layer in P.inputs]
-        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in P.outputs]
-        h2d = []
+        n4 = min(K + W, 400)
+        R_max = max(1, max(int(P.plan[t][3].sum()) for t in range(1, 1 + n4)))
+        k_stage = torch.zeros((w.n_layer, R_max, w.kv_row), dtype=torch.float16, device=dev)
+        v_stage = torch.zeros_like(k_stage)
+        host_rows = []
+        for t in range(1, 1 + n4):
+            c, row_off, start, counts = P.plan[t]
+            n = int(counts.sum())
+            hk = torch.zeros((w.n_layer, R_max, w.kv_row), dtype=torch.float16).pin_memory()
+            hv = torch.zeros_like(hk).pin_memory()
+            if n:
+                a = int(row_off[0])
+                hk[:, :n] = P.k_all[:, a:a + n].cpu()
+                hv[:, :n] = P.v_all[:, a:a + n].cpu()
+            host_rows.append((hk, hv, (row_off - row_off[0]).astype(np.int64)))
+        host_in = [(x.cpu().pin_memory(), y.cpu().pin_memory(), z.cpu().pin_memory())
+                   for x, y, z in zip(P.q, P.kn, P.vn)]
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in P.o]
+        h2d_bytes = 2 * k_stage.numel() * 2 + sum(x.numel() * 4 + y.numel() * 2 + z.numel() * 2
+                                                  for x, y, z in host_in)
+        d2h_bytes = sum(o.numel() * 4 for o in P.o)
 
-        def pre(t):
-            nb = 0
-            if t in host_rows:
-                _, k_rows, v_rows, _, _, _ = P.steps[t]
-                k_rows.copy_(host_rows[t][0], non_blocking=True)
-                v_rows.copy_(host_rows[t][1], non_blocking=True)
-                nb += 2 * host_rows[t][0].numel() * 2
-            for layer, trip in enumerate(host_inp[t % pool]):
-                for src, dst in zip(trip, P.inputs[t % pool][layer]):
-                    dst.copy_(src, non_blocking=True)
-                    nb += src.numel() * src.element_size()
-            h2d.append(nb)
-
-        def post(t):
-            for src, dst in zip(P.outputs, host_out):
-                dst.copy_(src, non_blocking=True)
+        def step_e2e(r, t):
+            hk, hv, rel_off = host_rows[t - 1]
+            k_stage.copy_(hk, non_blocking=True)
+            v_stage.copy_(hv, non_blocking=True)
+            for (hq, hkn, hvn), q, kn, vn in zip(host_in, P.q, P.kn, P.vn):
+                q.copy_(hq, non_blocking=True)
+                kn.copy_(hkn, non_blocking=True)
+                vn.copy_(hvn, non_blocking=True)
+            c, _, start, _ = P.plan[t]
+            r.step(c, k_stage, v_stage, rel_off, start, kind, P.q, P.kn, P.vn, P.o, stream)
+            for o, ho in zip(P.o, host_out):
+                ho.copy_(o, non_blocking=True)
 
         ring = new_ring()
-        evs = timed_loop(ring, 1, n_e2e, pre=pre, post=post)
+        timed_loop(ring, step_e2e, 1, min(W, n4))        # warm-up (captures the graph)
         torch.cuda.synchronize()
         ring.close()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in evs) / n_e2e
+        ring = new_ring()
+        evs = timed_loop(ring, step_e2e, 1, n4)
+        torch.cuda.synchronize()
+        ring.close()
+        e2e_ms = max_over_ranks(ms_of(evs), dist, dev) / n4
         e2e_obj = {"value": 1000.0 / e2e_ms * world, "unit": UNIT,
-                   "h2d_bytes_per_step": int(np.mean(h2d)),
-                   "d2h_bytes_per_step": int(sum(o.numel() * 4 for o in P.outputs)),
-                   "steps": n_e2e}
+                   "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
+                   "steps": n4, "api": "ring_step"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, kind, budget_s=args.cpu_seconds)
 
     if rank == 0:
-        vis_step = visible_rows(w, P.steps[1][0], kind) * w.kv_row * 4 * w.n_layer
+        vis_step = visible_rows(w, P.plan[1][0], kind) * w.kv_row * 4 * w.n_layer
         line = {
             "metric": METRIC,
             "value": 1000.0 / ms_per_step * world,
@@ -366,16 +410,19 @@ def run_gb300(args):
                 "cluster": g["cluster"], "groups": g["groups"],
                 "l2": ("flushed between steps (512 MiB write, untimed)" if flush
                        else "inputs larger than L2"),
-                "query_pool": pool, "parallelism": f"independent rings x{world}",
+                "api": "ring_step (one CUDA graph per step)",
+                "parallelism": f"independent rings x{world}",
             },
             "gpu_launches": int(launches),
+            "separate_calls": {"value": 1000.0 / ms_calls * world, "ms_per_step": ms_calls,
+                               "api": "ring_begin_step + ring_attend per layer"},
             "step_kv_gbs": vis_step / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "k_attend", "peak_source": f"{peak_kind} hbm_gbs",
                          "alg_bytes_per_launch": alg_bytes, "launch_ms": attn_ms,
                          "timing": "CUDA events around each launch on its stream, "
-                                   "instrumented repeat of the timed steps",
+                                   "instrumented repeat of the timed steps as separate calls",
                          "kernel_time_share": shares},
             "clocks": clocks,
             "e2e": e2e_obj,
@@ -463,10 +510,7 @@ def run_reference(args):
     rank, world, _ = _dist_env()
     if rank != 0:
         return
-    import synth
-    w = synth.workload(args.workload)
-    if args.mask == "swa" and not w.swa_window:
-        w = synth.workload(args.workload, swa_window=2048)
+    w = _workload(args)
     budget = max(5.0, min(150.0, 0.6 * (args.steps + args.warmup)))
     cpu = cpu_baseline(w, args.mask, budget_s=budget, max_steps=args.steps + args.warmup)
     line = {
@@ -495,9 +539,9 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--mask", choices=["full", "swa"], default="full")
-    ap.add_argument("--pool", type=int, default=64)
     ap.add_argument("--tiles-per-split", type=int, default=0)
     ap.add_argument("--max-cluster", type=int, default=0)
+    ap.add_argument("--n-seq", type=int, default=0, help="override the workload's sequence count")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

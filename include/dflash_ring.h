@@ -100,7 +100,7 @@ typedef struct ring_geometry {
 typedef struct ring_profile {
     int64_t launches[5];     /* 0 bulk append chunk, 1 begin-step kernel (fold-in append,
                                 slot_pos, masks, flags, RoPE table), 2 attention, 3 group
-                                combine, 4 unused                                            */
+                                combine, 4 whole-step graph replay (ring_step)             */
     double total_ms[5];      /* summed event time per kernel class                          */
 } ring_profile;
 
@@ -176,6 +176,23 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows,
  */
 int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q,
                 const void *k_noise, const void *v_noise, float *o, void *stream);
+
+/*
+ * ring_step -- one whole step as a fixed-topology CUDA graph: ring_begin_step followed by
+ * ring_attend for layers 0 .. n_layer-1 with mask `mask_kind`, the layer inputs and
+ * outputs given by host arrays of n_layer device pointers (q[l], k_noise[l], v_noise[l],
+ * o[l], layouts as for ring_attend).  The page builds its step graph once and replays it
+ * every step, feeding new inputs through dedicated buffers (section 1.5); here the graph
+ * is captured on the first call and replayed on later ones as long as k_rows, v_rows,
+ * n_rows, mask_kind and the layer pointers stay the same (a change re-captures it).  The
+ * per-step values (committed counts, row offsets) are staged to the device before the
+ * replay; bulk-append chunks, when a sequence needs them, run just before it.  Results
+ * equal those of the separate calls.  Errors: as ring_begin_step and ring_attend.
+ */
+int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
+              const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+              int32_t mask_kind, const float *const *q, const void *const *k_noise,
+              const void *const *v_noise, float *const *o, void *stream);
 
 /* ring_get_slot_pos -- host int32[cap] of sequence `seq` (-1 = never written).  Syncs. */
 int ring_get_slot_pos(ring_t *r, int32_t seq, int32_t *out);

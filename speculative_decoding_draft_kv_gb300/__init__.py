@@ -31,4 +31,5 @@ from .ring import (  # noqa: F401
     ring_profile_enable,
     ring_profile_read,
     ring_rows_needed,
+    ring_step,
 )

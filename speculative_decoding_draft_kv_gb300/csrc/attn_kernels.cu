@@ -671,45 +671,38 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 // ---------------------------------------------------------------------------------
-// Combine the per-group partials (log-sum-exp merge) when one cluster does not cover a
-// (sequence, kv head).  Grid (n_head_kv, n_seq), 256 threads: thread -> (row r = tid / 8,
-// 16 columns).
+// Combine the per-group partials (log-sum-exp merge) of every (sequence, kv head).
+// Grid (4, n_head_kv, n_seq) of 128 threads: block x covers rows 8x .. 8x+7, thread ->
+// (row, 8 columns).  The group loop is unrolled so that its loads overlap.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 k_attend_combine(RingDims d, RingDev m, float *o) {
-    const int gk = blockIdx.x, s = blockIdx.y;
-    const int r = threadIdx.x >> 3, c0 = (threadIdx.x & 7) * 16;
+    const int gk = blockIdx.y, s = blockIdx.z;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 4), c0 = (threadIdx.x & 15) * 8;
     if (r >= d.rows) return;
     const int64_t base = ((int64_t)s * d.n_head_kv + gk) * d.groups;
     float mm = -INFINITY;
-    for (int sp = 0; sp < d.groups; ++sp) mm = fmaxf(mm, m.part_ml[(base + sp) * kRows + r].x);
+#pragma unroll 4
+    for (int g = 0; g < d.groups; ++g) mm = fmaxf(mm, m.part_ml[(base + g) * kRows + r].x);
     const float muse = mm == -INFINITY ? 0.f : mm;
-    float acc[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
     float l = 0.f;
-    for (int sp = 0; sp < d.groups; ++sp) {
-        const float2 ml = m.part_ml[(base + sp) * kRows + r];
+#pragma unroll 4
+    for (int g = 0; g < d.groups; ++g) {
+        const float2 ml = m.part_ml[(base + g) * kRows + r];
+        const float4 *src = reinterpret_cast<const float4 *>(m.part_acc + ((base + g) * kRows + r) * kHeadDim + c0);
+        const float4 v0 = src[0], v1 = src[1];
         const float w = exp2f(ml.x - muse);
         l += w * ml.y;
-        const float4 *src = reinterpret_cast<const float4 *>(m.part_acc + ((base + sp) * kRows + r) * kHeadDim + c0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 v = src[k];
-            acc[4 * k + 0] += w * v.x;
-            acc[4 * k + 1] += w * v.y;
-            acc[4 * k + 2] += w * v.z;
-            acc[4 * k + 3] += w * v.w;
-        }
+        a0.x += w * v0.x; a0.y += w * v0.y; a0.z += w * v0.z; a0.w += w * v0.w;
+        a1.x += w * v1.x; a1.y += w * v1.y; a1.z += w * v1.z; a1.w += w * v1.w;
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const int hh = r / d.q_len, i = r - hh * d.q_len;
     const int h = gk * d.group + hh;
     float4 *dst = reinterpret_cast<float4 *>(o + (((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim + c0);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        dst[k] = make_float4(acc[4 * k] * inv, acc[4 * k + 1] * inv, acc[4 * k + 2] * inv,
-                             acc[4 * k + 3] * inv);
+    dst[0] = make_float4(a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv);
+    dst[1] = make_float4(a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv);
 }
 
 }  // namespace
@@ -782,7 +775,7 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
 
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,
                                   cudaStream_t st) {
-    k_attend_combine<<<dim3(d.n_head_kv, d.n_seq), 256, 0, st>>>(d, m, o);
+    k_attend_combine<<<dim3(kRows / 8, d.n_head_kv, d.n_seq), 128, 0, st>>>(d, m, o);
     return cudaGetLastError();
 }
 

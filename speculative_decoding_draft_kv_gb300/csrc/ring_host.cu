@@ -32,6 +32,17 @@ struct EventRec {
     cudaEvent_t a, b;
 };
 
+struct GraphKey {
+    const void *k_rows = nullptr, *v_rows = nullptr;
+    int64_t n_rows = -1;
+    int kind = -1;
+    std::vector<const void *> ptrs;
+    bool operator==(const GraphKey &o) const {
+        return k_rows == o.k_rows && v_rows == o.v_rows && n_rows == o.n_rows && kind == o.kind &&
+               ptrs == o.ptrs;
+    }
+};
+
 thread_local std::string g_init_error = "no error";
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -69,6 +80,10 @@ struct dflash_ring {
     std::vector<cudaEvent_t> ev_pool;
     std::string err = "no error";
     std::vector<void *> allocs;
+    cudaStream_t cap_stream = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    GraphKey graph_key;
+    int64_t graph_kernels = 0;
 };
 
 namespace {
@@ -142,6 +157,8 @@ void release(ring_t *r) {
         cudaEventDestroy(rec.b);
     }
     for (auto e : r->ev_pool) cudaEventDestroy(e);
+    if (r->graph_exec) cudaGraphExecDestroy(r->graph_exec);
+    if (r->cap_stream) cudaStreamDestroy(r->cap_stream);
     delete r;
 }
 
@@ -421,24 +438,27 @@ int ring_rows_needed(const ring_t *r, int32_t seq, int64_t committed, int64_t *s
     return RING_OK;
 }
 
-int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
-                    const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
-                    void *stream) {
-    if (!r) return RING_EINVAL;
-    if (!committed) return fail(r, RING_EINVAL, "ring_begin_step: committed is NULL");
+}  // extern "C"
+
+namespace {
+
+// Section 1.3 window arithmetic and every argument check of one begin_step; fills the
+// per-sequence step records.  Touches no state.
+int validate_step(ring_t *r, const char *who, const int64_t *committed, const void *k_rows,
+                  const void *v_rows, const int64_t *row_off, const int64_t *first_pos,
+                  int64_t n_rows, std::vector<SeqStep> &st, int64_t &max_bulk) {
+    if (!committed) return fail(r, RING_EINVAL, "%s: committed is NULL", who);
     const RingDims &d = r->d;
     const int64_t pos_limit = (int64_t)INT32_MAX - d.q_len - 1;
-    std::vector<SeqStep> st(d.n_seq);
-    int64_t max_bulk = 0;
+    st.assign(d.n_seq, SeqStep{});
+    max_bulk = 0;
     bool any_rows = false;
     for (int s = 0; s < d.n_seq; ++s) {
         const int64_t c = committed[s];
         if (c < 0 || c > pos_limit)
-            return fail(r, RING_ERANGE, "ring_begin_step: committed[%d] = %lld out of range", s,
-                        (long long)c);
+            return fail(r, RING_ERANGE, "%s: committed[%d] = %lld out of range", who, s, (long long)c);
         if (c < r->next_pos[s])
-            return fail(r, RING_ERANGE,
-                        "ring_begin_step: committed[%d] = %lld went below %lld", s,
+            return fail(r, RING_ERANGE, "%s: committed[%d] = %lld went below %lld", who, s,
                         (long long)c, (long long)r->next_pos[s]);
         const int64_t win = std::min<int64_t>(c, d.cap);
         const int64_t lo = c - win;
@@ -454,86 +474,205 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
         x.src_row = 0;
         if (n_new > 0) {
             any_rows = true;
-            if (!row_off || !first_pos)
-                return fail(r, RING_EINVAL, "ring_begin_step: row_off/first_pos are NULL");
+            if (!row_off || !first_pos) return fail(r, RING_EINVAL, "%s: row_off/first_pos are NULL", who);
             if (first_pos[s] > start || first_pos[s] < 0)
-                return fail(r, RING_ERANGE,
-                            "ring_begin_step: rows of seq %d start at %lld, after start %lld", s,
+                return fail(r, RING_ERANGE, "%s: rows of seq %d start at %lld, after start %lld", who, s,
                             (long long)first_pos[s], (long long)start);
             if (row_off[s] < 0 || row_off[s] + (c - first_pos[s]) > n_rows)
-                return fail(r, RING_ERANGE,
-                            "ring_begin_step: rows of seq %d run past n_rows %lld", s,
+                return fail(r, RING_ERANGE, "%s: rows of seq %d run past n_rows %lld", who, s,
                             (long long)n_rows);
             x.src_row = row_off[s] + (start - first_pos[s]);
             if (n_new > d.a_step) max_bulk = std::max(max_bulk, n_new);
         }
     }
     if (any_rows) {
-        if (!k_rows || !v_rows) return fail(r, RING_EINVAL, "ring_begin_step: rows are NULL");
+        if (!k_rows || !v_rows) return fail(r, RING_EINVAL, "%s: rows are NULL", who);
         if ((reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows)) & 15)
-            return fail(r, RING_EINVAL, "ring_begin_step: rows must be 16-byte aligned");
+            return fail(r, RING_EINVAL, "%s: rows must be 16-byte aligned", who);
     }
+    return RING_OK;
+}
 
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+// The step records go to the device through a rotating pinned slot; then the bulk chunks
+// (slot_pos of those slots is read by the begin kernel, which runs after them).
+int stage_and_bulk(ring_t *r, const char *who, const std::vector<SeqStep> &st, const void *k_rows,
+                   const void *v_rows, int64_t n_rows, int64_t max_bulk, cudaStream_t cs) {
+    const RingDims &d = r->d;
     const int slot = r->slot_next;
     r->slot_next = (slot + 1) % kStagingSlots;
     if (r->slot_used[slot]) {
         cudaError_t e = cudaEventSynchronize(r->slot_ev[slot]);
-        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: staging event");
+        if (e != cudaSuccess) return cuda_fail(r, e, who);
     }
     SeqStep *h = r->h_steps + (size_t)slot * d.n_seq;
     std::memcpy(h, st.data(), sizeof(SeqStep) * d.n_seq);
-    cudaError_t e = cudaMemcpyAsync(r->m.steps, h, sizeof(SeqStep) * d.n_seq,
-                                    cudaMemcpyHostToDevice, cs);
-    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: staging copy");
+    cudaError_t e = cudaMemcpyAsync(r->m.steps, h, sizeof(SeqStep) * d.n_seq, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return cuda_fail(r, e, who);
     cudaEventRecord(r->slot_ev[slot], cs);
     r->slot_used[slot] = true;
-
     const auto *kr = static_cast<const uint16_t *>(k_rows);
     const auto *vr = static_cast<const uint16_t *>(v_rows);
-    // bulk chunks first (slot_pos of those slots is then read by the begin kernel)
     const int n_chunks = (int)((max_bulk + d.bulk_chunk - 1) / d.bulk_chunk);
     for (int c = 0; c < n_chunks && e == cudaSuccess; ++c)
         e = timed(r, 0, cs, [&] { return launch_bulk_append(d, r->m, kr, vr, n_rows, c, cs); });
-    if (e == cudaSuccess)
-        e = timed(r, 1, cs, [&] {
-            return launch_begin_step(d, r->m, kr, vr, n_rows, !r->profiling, cs);
-        });
-    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
-    for (int s = 0; s < d.n_seq; ++s) {
+    return e == cudaSuccess ? RING_OK : cuda_fail(r, e, who);
+}
+
+void commit_host(ring_t *r, const int64_t *committed) {
+    for (int s = 0; s < r->d.n_seq; ++s) {
         r->next_pos[s] = committed[s];
         r->committed[s] = committed[s];
     }
     r->have_step = true;
+}
+
+int validate_attend(ring_t *r, const char *who, int32_t layer, int32_t mask_kind, const void *q,
+                    const void *k_noise, const void *v_noise, const void *o) {
+    const RingDims &d = r->d;
+    if (layer < 0 || layer >= d.n_layer) return fail(r, RING_EINVAL, "%s: layer %d out of range", who, layer);
+    if (mask_kind != RING_MASK_FULL && mask_kind != RING_MASK_SWA)
+        return fail(r, RING_EINVAL, "%s: unknown mask kind %d", who, mask_kind);
+    if (mask_kind == RING_MASK_SWA && d.n_kinds < 2)
+        return fail(r, RING_EINVAL, "%s: SWA mask needs swa_window > 0 at init", who);
+    if (!q || !k_noise || !v_noise || !o) return fail(r, RING_EINVAL, "%s: NULL input or output", who);
+    if ((reinterpret_cast<uintptr_t>(k_noise) | reinterpret_cast<uintptr_t>(v_noise) |
+         reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(q)) & 15)
+        return fail(r, RING_EINVAL, "%s: inputs and output must be 16-byte aligned", who);
+    return RING_OK;
+}
+
+cudaError_t launch_layer(ring_t *r, int32_t layer, int32_t mask_kind, const float *q,
+                         const void *k_noise, const void *v_noise, float *o, bool pdl,
+                         cudaStream_t cs) {
+    const RingDims &d = r->d;
+    const auto *kn = static_cast<const uint16_t *>(k_noise);
+    const auto *vn = static_cast<const uint16_t *>(v_noise);
+    cudaError_t e = timed(r, 2, cs, [&] {
+        return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q, kn, vn,
+                             o, pdl, cs);
+    });
+    if (e == cudaSuccess && d.groups > 1)
+        e = timed(r, 3, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
+                    const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                    void *stream) {
+    if (!r) return RING_EINVAL;
+    std::vector<SeqStep> st;
+    int64_t max_bulk = 0;
+    int rc = validate_step(r, "ring_begin_step", committed, k_rows, v_rows, row_off, first_pos,
+                           n_rows, st, max_bulk);
+    if (rc != RING_OK) return rc;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    rc = stage_and_bulk(r, "ring_begin_step", st, k_rows, v_rows, n_rows, max_bulk, cs);
+    if (rc != RING_OK) return rc;
+    const auto *kr = static_cast<const uint16_t *>(k_rows);
+    const auto *vr = static_cast<const uint16_t *>(v_rows);
+    cudaError_t e = timed(r, 1, cs, [&] {
+        return launch_begin_step(r->d, r->m, kr, vr, n_rows, !r->profiling, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
+    commit_host(r, committed);
     return RING_OK;
 }
 
 int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q, const void *k_noise,
                 const void *v_noise, float *o, void *stream) {
     if (!r) return RING_EINVAL;
-    const RingDims &d = r->d;
-    if (layer < 0 || layer >= d.n_layer)
-        return fail(r, RING_EINVAL, "ring_attend: layer %d out of range", layer);
-    if (mask_kind != RING_MASK_FULL && mask_kind != RING_MASK_SWA)
-        return fail(r, RING_EINVAL, "ring_attend: unknown mask kind %d", mask_kind);
-    if (mask_kind == RING_MASK_SWA && d.n_kinds < 2)
-        return fail(r, RING_EINVAL, "ring_attend: SWA mask needs swa_window > 0 at init");
-    if (!q || !k_noise || !v_noise || !o)
-        return fail(r, RING_EINVAL, "ring_attend: NULL input or output");
-    if ((reinterpret_cast<uintptr_t>(k_noise) | reinterpret_cast<uintptr_t>(v_noise) |
-         reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(q)) & 15)
-        return fail(r, RING_EINVAL, "ring_attend: inputs and output must be 16-byte aligned");
+    int rc = validate_attend(r, "ring_attend", layer, mask_kind, q, k_noise, v_noise, o);
+    if (rc != RING_OK) return rc;
     if (!r->have_step) return fail(r, RING_ESTATE, "ring_attend: no ring_begin_step yet");
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const auto *kn = static_cast<const uint16_t *>(k_noise);
-    const auto *vn = static_cast<const uint16_t *>(v_noise);
-    cudaError_t e = timed(r, 2, cs, [&] {
-        return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q,
-                             kn, vn, o, !r->profiling, cs);
-    });
-    if (e == cudaSuccess && d.groups > 1)
-        e = timed(r, 3, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
+    cudaError_t e = launch_layer(r, layer, mask_kind, q, k_noise, v_noise, o, !r->profiling,
+                                 static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_attend: launch");
+    return RING_OK;
+}
+
+int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
+              const int64_t *row_off, const int64_t *first_pos, int64_t n_rows, int32_t mask_kind,
+              const float *const *q, const void *const *k_noise, const void *const *v_noise,
+              float *const *o, void *stream) {
+    if (!r) return RING_EINVAL;
+    const RingDims &d = r->d;
+    if (!q || !k_noise || !v_noise || !o)
+        return fail(r, RING_EINVAL, "ring_step: per-layer pointer arrays are NULL");
+    for (int l = 0; l < d.n_layer; ++l) {
+        int rc = validate_attend(r, "ring_step", l, mask_kind, q[l], k_noise[l], v_noise[l], o[l]);
+        if (rc != RING_OK) return rc;
+    }
+    std::vector<SeqStep> st;
+    int64_t max_bulk = 0;
+    int rc = validate_step(r, "ring_step", committed, k_rows, v_rows, row_off, first_pos, n_rows,
+                           st, max_bulk);
+    if (rc != RING_OK) return rc;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    rc = stage_and_bulk(r, "ring_step", st, k_rows, v_rows, n_rows, max_bulk, cs);
+    if (rc != RING_OK) return rc;
+
+    // the fixed-topology step graph: captured once, re-captured only when a pointer the
+    // kernels take as a parameter changes
+    GraphKey key;
+    key.k_rows = k_rows;
+    key.v_rows = v_rows;
+    key.n_rows = n_rows;
+    key.kind = mask_kind;
+    for (int l = 0; l < d.n_layer; ++l) {
+        key.ptrs.push_back(q[l]);
+        key.ptrs.push_back(k_noise[l]);
+        key.ptrs.push_back(v_noise[l]);
+        key.ptrs.push_back(o[l]);
+    }
+    cudaError_t e = cudaSuccess;
+    if (!r->graph_exec || !(key == r->graph_key)) {
+        if (!r->cap_stream) {
+            e = cudaStreamCreateWithFlags(&r->cap_stream, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return cuda_fail(r, e, "ring_step: capture stream");
+        }
+        const bool prof = r->profiling;
+        r->profiling = false;              // no events inside the graph
+        e = cudaStreamBeginCapture(r->cap_stream, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            const auto *kr = static_cast<const uint16_t *>(k_rows);
+            const auto *vr = static_cast<const uint16_t *>(v_rows);
+            cudaError_t le = launch_begin_step(d, r->m, kr, vr, n_rows, true, r->cap_stream);
+            for (int l = 0; l < d.n_layer && le == cudaSuccess; ++l)
+                le = launch_layer(r, l, mask_kind, q[l], k_noise[l], v_noise[l], o[l], true, r->cap_stream);
+            cudaGraph_t graph = nullptr;
+            e = cudaStreamEndCapture(r->cap_stream, &graph);
+            if (le != cudaSuccess) e = le;
+            if (e == cudaSuccess) {
+                bool updated = false;
+                if (r->graph_exec) {
+                    cudaGraphExecUpdateResultInfo info;
+                    updated = cudaGraphExecUpdate(r->graph_exec, graph, &info) == cudaSuccess;
+                    if (!updated) {
+                        cudaGetLastError();
+                        cudaGraphExecDestroy(r->graph_exec);
+                        r->graph_exec = nullptr;
+                    }
+                }
+                if (!updated) e = cudaGraphInstantiate(&r->graph_exec, graph, 0);
+            }
+            if (graph) cudaGraphDestroy(graph);
+        }
+        r->profiling = prof;
+        if (e != cudaSuccess) {
+            r->graph_exec = nullptr;
+            return cuda_fail(r, e, "ring_step: graph capture");
+        }
+        r->graph_key = key;
+        r->graph_kernels = 1 + d.n_layer * (d.groups > 1 ? 2 : 1);
+    }
+    e = timed(r, 4, cs, [&] { return cudaGraphLaunch(r->graph_exec, cs); });
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_step: graph launch");
+    r->launches += r->graph_kernels - 1;   // timed() counted the launch itself once
+    commit_host(r, committed);
     return RING_OK;
 }
 

@@ -30,7 +30,7 @@ MASK_KINDS = {"full": RING_MASK_FULL, "swa": RING_MASK_SWA}
 # C symbols the header declares (checked by the test-suite against the shared object).
 EXPORTED = (
     "ring_init", "ring_init_ex", "ring_destroy", "ring_get_geometry", "ring_rows_needed",
-    "ring_begin_step", "ring_attend", "ring_get_slot_pos", "ring_get_mask",
+    "ring_begin_step", "ring_attend", "ring_step", "ring_get_slot_pos", "ring_get_mask",
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
     "ring_last_error",
@@ -75,7 +75,7 @@ class RingProfile(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int64 * 5), ("total_ms", ctypes.c_double * 5)]
 
 
-PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "unused")
+PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "step_graph")
 
 _LIB = None
 _N_SEQ = {}      # handle -> n_seq, so per-step calls skip a geometry query
@@ -101,6 +101,8 @@ def _load():
         "ring_rows_needed": ([vp, i32, i64, p64, ctypes.POINTER(i32)], ctypes.c_int),
         "ring_begin_step": ([vp, p64, vp, vp, p64, p64, i64, vp], ctypes.c_int),
         "ring_attend": ([vp, i32, i32, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ring_step": ([vp, p64, vp, vp, p64, p64, i64, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                       ctypes.POINTER(vp), ctypes.POINTER(vp), vp], ctypes.c_int),
         "ring_get_slot_pos": ([vp, i32, vp], ctypes.c_int),
         "ring_get_mask": ([vp, i32, i32, vp], ctypes.c_int),
         "ring_get_tile_flags": ([vp, i32, i32, vp], ctypes.c_int),
@@ -231,6 +233,32 @@ def ring_attend(h, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
     _check(rc, h, "ring_attend")
 
 
+def ring_step(h, committed, k_rows, v_rows, row_off, first_pos, mask_kind, q, k_noise, v_noise,
+              o, stream=None):
+    """One begin_step plus every layer's attention, replayed as one CUDA graph.
+
+    ``q``, ``k_noise``, ``v_noise``, ``o``: sequences of n_layer CUDA tensors (layouts as
+    for :func:`ring_attend`); ``k_rows``/``v_rows`` as for :func:`ring_begin_step`.
+    """
+    import torch
+    n_seq = _N_SEQ.get(getattr(h, "value", h)) or ring_get_geometry(h)["n_seq"]
+    c_arr, c_ptr = _i64_array(committed, n_seq, "committed")
+    o_arr, o_ptr = _i64_array(row_off, n_seq, "row_off")
+    f_arr, f_ptr = _i64_array(first_pos, n_seq, "first_pos")
+    n_rows = 0 if k_rows is None else int(k_rows.shape[1])
+    n_layer = len(q)
+    arr = ctypes.c_void_p * n_layer
+    qp = arr(*[_dev_ptr(t, torch.float32, "q").value for t in q])
+    kp = arr(*[_dev_ptr(t, torch.float16, "k_noise").value for t in k_noise])
+    vp_ = arr(*[_dev_ptr(t, torch.float16, "v_noise").value for t in v_noise])
+    op = arr(*[_dev_ptr(t, torch.float32, "o").value for t in o])
+    kind = MASK_KINDS.get(mask_kind, mask_kind)
+    rc = _load().ring_step(h, c_ptr, _dev_ptr(k_rows, torch.float16, "k_rows"),
+                           _dev_ptr(v_rows, torch.float16, "v_rows"), o_ptr, f_ptr, n_rows, kind,
+                           qp, kp, vp_, op, _stream(stream))
+    _check(rc, h, "ring_step")
+
+
 def ring_get_slot_pos(h, seq) -> np.ndarray:
     g = ring_get_geometry(h)
     out = np.empty(g["cap"], np.int32)
@@ -334,6 +362,11 @@ class Ring:
 
     def attend(self, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
         ring_attend(self.h, layer, mask_kind, q, k_noise, v_noise, o, stream)
+
+    def step(self, committed, k_rows, v_rows, row_off, first_pos, mask_kind, q, k_noise, v_noise,
+             o, stream=None):
+        ring_step(self.h, committed, k_rows, v_rows, row_off, first_pos, mask_kind, q, k_noise,
+                  v_noise, o, stream)
 
     def slot_pos(self, seq=0):
         return ring_get_slot_pos(self.h, seq)

@@ -279,3 +279,53 @@ def test_noise_tiles_and_small_rings(cap, tps):
         assert run.ring.device_error() == 0
     finally:
         run.close()
+
+
+def test_step_graph_matches_separate_calls():
+    """ring_step (one replayed CUDA graph per step) gives the same outputs and the same
+    ring state as ring_begin_step + ring_attend per layer, through fold-in steps, a bulk
+    step, a change of the layer buffers (re-capture) and both masks."""
+    w = synth.workload(3, cap=512, n_layer=3, n_seq=2, swa_window=100,
+                       extra={"jump_max": 3000, "fold_max": 18, "p_jump": 0.3})
+    a, b = GpuRun(w), GpuRun(w)
+    try:
+        L = w.n_layer
+        outs = [[torch.empty((w.n_seq, w.q_len, w.n_head, w.head_dim), device=a.dev) for _ in range(L)]
+                for _ in range(2)]
+        for t, c in enumerate(synth.commit_schedule(w, 8)):
+            kind = "swa" if t % 3 == 2 else "full"
+            # rows for both rings (same values); b takes them through ring_step
+            a.begin_step(c)
+            k_rows, v_rows = a._keep
+            row_off, first = [], []
+            n = 0
+            for s in range(w.n_seq):
+                st, nn = b.ring.rows_needed(s, int(c[s]))
+                row_off.append(n)
+                first.append(st)
+                n += nn
+            ins = [a.inputs(t, layer, a.dev) for layer in range(L)]
+            o_ref = []
+            for layer in range(L):
+                o = torch.empty_like(ins[layer][0])
+                a.ring.attend(layer, kind, *ins[layer], o)
+                o_ref.append(o)
+            o_graph = outs[t % 2]                       # alternate buffers: forces re-capture
+            b.ring.step(c, k_rows, v_rows, row_off, first, kind, [x[0] for x in ins],
+                        [x[1] for x in ins], [x[2] for x in ins], o_graph)
+            z = [np.zeros((1, int(c[s]) - first[s], 2), np.float16) for s in range(w.n_seq)]
+            for s in range(w.n_seq):
+                b.book[s].begin_step(int(c[s]), z[s], z[s], first[s])
+            torch.cuda.synchronize()
+            for layer in range(L):
+                assert torch.equal(o_graph[layer], o_ref[layer]), (t, layer)
+            b.check_slots_and_masks()
+            for s in range(w.n_seq):
+                ka, va = a.ring.kv(s, L - 1)
+                kb, vb = b.ring.kv(s, L - 1)
+                assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16))
+                assert np.array_equal(va.view(np.uint16), vb.view(np.uint16))
+        assert a.ring.device_error() == 0 and b.ring.device_error() == 0
+    finally:
+        a.close()
+        b.close()

@@ -145,6 +145,8 @@ PINS = [
     pins.test_softmax_scale_is_one_over_sqrt_head_dim,
     pins.test_gqa_head_map,
     pins.test_masked_attention_core_closed_form,
+    lambda: pins.test_dense_route_zero_query_closed_form("full"),
+    lambda: pins.test_dense_route_zero_query_closed_form("swa"),
     eqv.test_ring_equals_dense_window_tiny_workload,
 ]
 

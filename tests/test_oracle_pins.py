@@ -315,3 +315,28 @@ def test_masked_attention_core_closed_form():
     w = math.exp(2) / (math.exp(2) + 1)
     np.testing.assert_allclose(orc.masked_attention(q, k, v, mask, 1.0), [[w, 1 - w]],
                                atol=1e-15)
+
+
+@pytest.mark.parametrize("kind", ["full", "swa"])
+def test_dense_route_zero_query_closed_form(kind):
+    """The dense-window route on its own: with Q = 0 and V rows holding their position,
+    every output is the mean position of exactly the window plus the visible noise."""
+    cap, q_len, swa, d, hkv, nh = 16, 4, 6, 4, 2, 4
+
+    def rows_fn(pos):
+        pos = np.asarray(pos)
+        k = np.zeros((len(pos), hkv * d), np.float16)
+        v = np.repeat(pos.astype(np.float16)[:, None], hkv * d, axis=1)
+        return k, v
+
+    for c in (0, 3, 16, 40, 41):
+        kn = np.zeros((q_len, hkv * d), np.float16)
+        vn = np.repeat(np.arange(c, c + q_len, dtype=np.float16)[:, None], hkv * d, axis=1)
+        o = orc.attend_dense(c, cap, rows_fn, np.zeros((q_len, nh, d)), kn, vn, d, hkv, nh,
+                             10000.0, kind=kind, swa_window=swa)
+        for i in range(q_len):
+            if kind == "full":
+                want = (c - min(c, cap) + c + q_len - 1) / 2.0
+            else:
+                want = (c - min(swa, min(c, cap)) + c + i) / 2.0
+            np.testing.assert_allclose(o[i], want, rtol=0, atol=1e-12)
