@@ -42,7 +42,7 @@ struct Shape {
     static constexpr int CW = CLUSTER ? 8 : 4;      // consumer warps
     static constexpr int kConsumers = CW * 32;
     static constexpr int kThreads = kConsumers + 32;
-    static constexpr int kStages = 3;
+    static constexpr int kStages = CLUSTER ? 4 : 3;
     static constexpr int kSlices = CW / 2;          // key slices per tile
     static constexpr int kKeys = kTile / kSlices;   // keys per warp per tile (32 or 16)
     static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
@@ -52,9 +52,14 @@ struct Shape {
     static constexpr int kOffBits = kOffQ + kQBytes;
     static constexpr int kOffBars = kOffBits + kStages * kBitsPerStage;
     static constexpr int kOffRecv = kOffBars + 2 * kStages * 8 + 16;
-    // cluster receive buffer: kSlices * 32 rows of partial numerators + (max, sum) per row
-    static constexpr int kRecvAcc = kSlices * kRows * kHeadDim * 4;
-    static constexpr int kRecvBytes = kRecvAcc + kSlices * kRows * 8;
+    // cluster receive buffer: one partial per CTA of the cluster for each of this CTA's
+    // 32 / cluster rows -- 32 rows of numerators + (max, sum) per row in all
+    static constexpr int kRecvAcc = kRows * kHeadDim * 4;
+    static constexpr int kRecvBytes = kRecvAcc + kRows * 8;
+    // key-slice pre-merge scratch (in the idle stage buffers): slices 1.. of both row
+    // blocks, 64 numerators + 2 maxima + 2 sums per lane
+    static constexpr int kXPer = 68 * 32;
+    static_assert((kSlices - 1) * 2 * kXPer * 4 <= kStages * kStageBytes, "pre-merge scratch");
     static constexpr int kSmem = 1024 + kOffRecv + (CLUSTER ? kRecvBytes : 0);
 };
 static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStageBytes,
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(Shape<CLUSTER>::kThreads, Shape<CLUSTER>::kMin
 k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          RingDims d, RingDev m, int layer, int kind, float scale_log2,
          const float *__restrict__ q, const uint16_t *__restrict__ k_noise,
-         const uint16_t *__restrict__ v_noise, float *__restrict__ o) {
+         const uint16_t *__restrict__ v_noise, float *__restrict__ o, int preload) {
     using SH = Shape<CLUSTER>;
     constexpr int CW = SH::CW;
     constexpr int kStages = SH::kStages;
@@ -274,10 +279,6 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
-    pdl_wait();   // ring state written by begin_step (and earlier kernels) is visible
-    // A grid that fits in one wave lets the next kernel's CTAs settle onto idle SMs now;
-    // a multi-wave grid must not, or they would take slots its own later CTAs need.
-    if (d.single_wave) pdl_trigger();
 
     if (warp == CW) {
         // ---------------- producer ----------------
@@ -286,7 +287,40 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const int zrow = (s * d.n_layer + layer) * d.n_head_kv + gk;
         bool noise_ready = false;
         int it = 0;
-        for (int t = t0; t < t1; ++t) {
+        int t = t0;
+        if (preload) {
+            // The kernel before this one (an attention kernel of another layer, or one
+            // that does not overlap this grid at all) writes none of this layer's context
+            // tiles, flags or bits, so the first stages can be filled before the grid
+            // dependency resolves.  The host never asks for this right after begin_step.
+            // A tile holding noise slots is not touched before the noise rows are written.
+            for (; t < t1 && it < kStages; ++t) {
+                const int flag = flags[t];
+                if (flag == 0) continue;
+                if (t >= tn0 && t <= tn1) break;
+                if (lane == 0) {
+                    const uint32_t full = bar0 + 8 * it;
+                    const uint32_t dk = smem_u32(smem + it * kStageBytes);
+                    const uint32_t dv = dk + kTileBytes;
+                    const uint32_t nbits = flag == 2 ? (uint32_t)qw * 8u : 0u;
+                    mbar_expect_tx(full, kStageBytes + nbits);
+                    tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
+                    tma_load_3d(dk + kHalfBox, &tm_k, 64, t * kTile, zrow, full);
+                    tma_load_3d(dv, &tm_v, 0, t * kTile, zrow, full);
+                    tma_load_3d(dv + kHalfBox, &tm_v, 64, t * kTile, zrow, full);
+                    if (nbits)
+                        bulk_g2s(smem_u32(smem + kOffBits + it * kBitsPerStage),
+                                 m.maskbits + (fbase + t) * qw, nbits, full);
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        pdl_wait();
+        // A grid that fits in one wave lets the next kernel's CTAs settle onto idle SMs
+        // now; a multi-wave grid must not, or they would take slots its own later CTAs need.
+        if (d.single_wave) pdl_trigger();
+        for (; t < t1; ++t) {
             const int flag = flags[t];
             if (flag == 0) continue;
             if (!noise_ready && t >= tn0 && t <= tn1) {
@@ -336,6 +370,8 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         __syncwarp();
     } else {
         // ---------------- consumers ----------------
+        pdl_wait();   // ring state written by begin_step (and earlier kernels) is visible
+        if (d.single_wave) pdl_trigger();
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
@@ -554,21 +590,62 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             lrow[j] += __shfl_xor_sync(0xffffffffu, lrow[j], 2);
         }
         if constexpr (CLUSTER) {
-            // push this warp's rows to the CTA of the cluster that finishes them
-            const int rr[2] = {r0, r1};
-            const int slot_p = (int)rank * SH::kSlices + ksl;     // this warp's partial index
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = rr[j];
-                const int owner = r / rows_per, lr = r - owner * rows_per;
-                float *acc_row = recv_acc + ((int64_t)slot_p * rows_per + lr) * kHeadDim;
-                const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
+            // Merge the key slices of each row block inside this CTA (through the idle
+            // stage buffers), then push one partial per row to the CTA of the cluster
+            // that finishes that row.
+            bar_sync(1, SH::kConsumers);
+            float *xs = reinterpret_cast<float *>(smem);
+            if (ksl > 0) {
+                float *x = xs + ((ksl - 1) * 2 + mb) * SH::kXPer;
 #pragma unroll
                 for (int n = 0; n < 16; ++n)
-                    st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), oacc[n][2 * j], oacc[n][2 * j + 1]);
-                if (c == 0)
-                    st_cluster_v2(map_rank(smem_u32(recv_ml + slot_p * rows_per + lr), (uint32_t)owner),
-                                  mrow[j], lrow[j]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x[(n * 4 + e) * 32 + lane] = oacc[n][e];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    x[(64 + j) * 32 + lane] = mrow[j];
+                    x[(66 + j) * 32 + lane] = lrow[j];
+                }
+            }
+            bar_sync(1, SH::kConsumers);
+            if (ksl == 0) {
+                const int rr[2] = {r0, r1};
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float mk[SH::kSlices], wk[SH::kSlices];
+                    mk[0] = mrow[j];
+                    float mm = mrow[j];
+#pragma unroll
+                    for (int k = 1; k < SH::kSlices; ++k) {
+                        mk[k] = xs[((k - 1) * 2 + mb) * SH::kXPer + (64 + j) * 32 + lane];
+                        mm = fmaxf(mm, mk[k]);
+                    }
+                    const float muse = mm == -INFINITY ? 0.f : mm;
+                    float ll = 0.f;
+#pragma unroll
+                    for (int k = 0; k < SH::kSlices; ++k) {
+                        wk[k] = exp2f(mk[k] - muse);
+                        ll += wk[k] * (k == 0 ? lrow[j] : xs[((k - 1) * 2 + mb) * SH::kXPer + (66 + j) * 32 + lane]);
+                    }
+                    const int r = rr[j];
+                    const int owner = r / rows_per, lr = r - owner * rows_per;
+                    float *acc_row = recv_acc + ((int64_t)rank * rows_per + lr) * kHeadDim;
+                    const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        float v0 = oacc[n][2 * j] * wk[0], v1 = oacc[n][2 * j + 1] * wk[0];
+#pragma unroll
+                        for (int k = 1; k < SH::kSlices; ++k) {
+                            const float *x = xs + ((k - 1) * 2 + mb) * SH::kXPer;
+                            v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
+                            v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
+                        }
+                        st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
+                    }
+                    if (c == 0)
+                        st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rows_per + lr), (uint32_t)owner),
+                                      mm, ll);
+                }
             }
         } else {
             // merge the two key halves through stage buffer 0 (idle now), then write this
@@ -633,7 +710,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
     // ---------------- cluster merge: this CTA finishes rows [rank * rows_per, +rows_per) ----
     cluster_sync();     // every partial of this CTA's rows is in its receive buffer
-    const int n_part = (int)nct * SH::kSlices;
+    const int n_part = (int)nct;
     const int items = rows_per * (kHeadDim / 4);
     for (int u = threadIdx.x; u < items; u += SH::kThreads) {
         const int lr = u / (kHeadDim / 4), c4 = (u % (kHeadDim / 4)) * 4;
@@ -743,7 +820,7 @@ int attend_cluster_capacity(int cluster) {
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
                           const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
-                          float *o, bool pdl, cudaStream_t st) {
+                          float *o, bool pdl, bool preload, cudaStream_t st) {
     const bool clustered = d.cluster > 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.n_splits, d.n_head_kv, d.n_seq);
@@ -768,9 +845,9 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     cfg.numAttrs = na;
     if (clustered)
         return cudaLaunchKernelEx(&cfg, k_attend<true>, *tm_k, *tm_v, d, m, layer, kind,
-                                  scale_log2, q, k_noise, v_noise, o);
+                                  scale_log2, q, k_noise, v_noise, o, (int)(preload && pdl));
     return cudaLaunchKernelEx(&cfg, k_attend<false>, *tm_k, *tm_v, d, m, layer, kind, scale_log2,
-                              q, k_noise, v_noise, o);
+                              q, k_noise, v_noise, o, 0);
 }
 
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,

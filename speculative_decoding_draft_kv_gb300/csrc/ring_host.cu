@@ -84,6 +84,7 @@ struct dflash_ring {
     cudaGraphExec_t graph_exec = nullptr;
     GraphKey graph_key;
     int64_t graph_kernels = 0;
+    bool last_was_begin = false;   // the ring's last kernel launch was the begin-step kernel
 };
 
 namespace {
@@ -547,9 +548,13 @@ cudaError_t launch_layer(ring_t *r, int32_t layer, int32_t mask_kind, const floa
     const RingDims &d = r->d;
     const auto *kn = static_cast<const uint16_t *>(k_noise);
     const auto *vn = static_cast<const uint16_t *>(v_noise);
+    // preloading before the grid dependency is safe unless the ring's previous launch was
+    // the begin-step kernel, which writes context rows, flags and bits
+    const bool preload = !r->last_was_begin;
+    r->last_was_begin = false;
     cudaError_t e = timed(r, 2, cs, [&] {
         return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q, kn, vn,
-                             o, pdl, cs);
+                             o, pdl, preload, cs);
     });
     if (e == cudaSuccess && d.groups > 1)
         e = timed(r, 3, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
@@ -578,6 +583,7 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
         return launch_begin_step(r->d, r->m, kr, vr, n_rows, !r->profiling, cs);
     });
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
+    r->last_was_begin = true;
     commit_host(r, committed);
     return RING_OK;
 }
@@ -641,6 +647,7 @@ int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const voi
             const auto *kr = static_cast<const uint16_t *>(k_rows);
             const auto *vr = static_cast<const uint16_t *>(v_rows);
             cudaError_t le = launch_begin_step(d, r->m, kr, vr, n_rows, true, r->cap_stream);
+            r->last_was_begin = true;
             for (int l = 0; l < d.n_layer && le == cudaSuccess; ++l)
                 le = launch_layer(r, l, mask_kind, q[l], k_noise[l], v_noise[l], o[l], true, r->cap_stream);
             cudaGraph_t graph = nullptr;

@@ -121,10 +121,14 @@ cudaError_t attend_kernels_init();   // per device, before the first launch
 // clusters of `cluster` CTAs that can be resident at once (0 if none)
 int attend_cluster_capacity(int cluster);
 // scale_log2 = log2(e) / sqrt(head_dim): the softmax runs in base 2.
+// preload: the kernel may fill its first pipeline stages before its grid dependency
+// resolves -- only valid when the kernel launched just before it (if it overlaps at all)
+// writes none of this layer's context K/V, flags or visibility bits (so: not right after
+// the begin-step kernel).
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
                           const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
-                          float *o, bool pdl, cudaStream_t st);
+                          float *o, bool pdl, bool preload, cudaStream_t st);
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,
                                   cudaStream_t st);
 size_t attend_smem_bytes();
