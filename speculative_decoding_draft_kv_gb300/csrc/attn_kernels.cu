@@ -56,10 +56,10 @@ struct Shape {
     // 32 / cluster rows -- 32 rows of numerators + (max, sum) per row in all
     static constexpr int kRecvAcc = kRows * kHeadDim * 4;
     static constexpr int kRecvBytes = kRecvAcc + kRows * 8;
-    // key-slice pre-merge scratch (in the idle stage buffers): slices 1.. of both row
-    // blocks, 64 numerators + 2 maxima + 2 sums per lane
+    // key-slice pre-merge scratch (in the idle stage buffers): every warp's partial,
+    // 64 numerators + 2 maxima + 2 sums per lane
     static constexpr int kXPer = 68 * 32;
-    static_assert((kSlices - 1) * 2 * kXPer * 4 <= kStages * kStageBytes, "pre-merge scratch");
+    static_assert(kSlices * 2 * kXPer * 4 <= kStages * kStageBytes, "pre-merge scratch");
     static constexpr int kSmem = 1024 + kOffRecv + (CLUSTER ? kRecvBytes : 0);
 };
 static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStageBytes,
@@ -211,6 +211,10 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -288,6 +292,24 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         bool noise_ready = false;
         int it = 0;
         int t = t0;
+        {
+            // L2 prefetch of this CTA's query rows, the step's RoPE table and the noise
+            // rows: a hint only (L2 is coherent), so it is safe whatever runs before
+            const int half = kHeadDim / 2;
+            for (int u = lane; u < d.rows * 4; u += 32) {
+                const int r = u >> 2, hh = r / d.q_len, i = r - hh * d.q_len;
+                prefetch_l2(q + (((int64_t)s * d.q_len + i) * d.n_head + gk * d.group + hh) * kHeadDim + (u & 3) * 32);
+            }
+            for (int u = lane; u < d.q_len * half * 8 / 128; u += 32)
+                prefetch_l2(reinterpret_cast<const uint8_t *>(m.rope32 + (int64_t)s * d.q_len * half) + u * 128);
+            if (owns_noise)
+                for (int u = lane; u < d.q_len * 2; u += 32) {
+                    const int i = u >> 1;
+                    const uint16_t *base = (u & 1) ? v_noise : k_noise;
+                    prefetch_l2(base + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim);
+                    prefetch_l2(base + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + 64);
+                }
+        }
         if (preload) {
             // The kernel before this one (an attention kernel of another layer, or one
             // that does not overlap this grid at all) writes none of this layer's context
@@ -590,13 +612,14 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             lrow[j] += __shfl_xor_sync(0xffffffffu, lrow[j], 2);
         }
         if constexpr (CLUSTER) {
-            // Merge the key slices of each row block inside this CTA (through the idle
-            // stage buffers), then push one partial per row to the CTA of the cluster
-            // that finishes that row.
+            // Merge the key slices of each row block inside this CTA, then push one partial
+            // per row to the CTA of the cluster that finishes that row.  Every warp first
+            // publishes its partial (in the idle stage buffers); warp (mb, ksl) then merges
+            // columns [32 ksl, 32 ksl + 32) of its row block and pushes them.
             bar_sync(1, SH::kConsumers);
             float *xs = reinterpret_cast<float *>(smem);
-            if (ksl > 0) {
-                float *x = xs + ((ksl - 1) * 2 + mb) * SH::kXPer;
+            {
+                float *x = xs + (mb * SH::kSlices + ksl) * SH::kXPer;
 #pragma unroll
                 for (int n = 0; n < 16; ++n)
 #pragma unroll
@@ -608,44 +631,41 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
             }
             bar_sync(1, SH::kConsumers);
-            if (ksl == 0) {
-                const int rr[2] = {r0, r1};
+            const int rr[2] = {r0, r1};
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float mk[SH::kSlices], wk[SH::kSlices];
-                    mk[0] = mrow[j];
-                    float mm = mrow[j];
+            for (int j = 0; j < 2; ++j) {
+                float wk[SH::kSlices];
+                float mm = -INFINITY;
 #pragma unroll
-                    for (int k = 1; k < SH::kSlices; ++k) {
-                        mk[k] = xs[((k - 1) * 2 + mb) * SH::kXPer + (64 + j) * 32 + lane];
-                        mm = fmaxf(mm, mk[k]);
-                    }
-                    const float muse = mm == -INFINITY ? 0.f : mm;
-                    float ll = 0.f;
+                for (int k = 0; k < SH::kSlices; ++k)
+                    mm = fmaxf(mm, xs[(mb * SH::kSlices + k) * SH::kXPer + (64 + j) * 32 + lane]);
+                const float muse = mm == -INFINITY ? 0.f : mm;
+                float ll = 0.f;
+#pragma unroll
+                for (int k = 0; k < SH::kSlices; ++k) {
+                    const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
+                    wk[k] = exp2f(x[(64 + j) * 32 + lane] - muse);
+                    ll += wk[k] * x[(66 + j) * 32 + lane];
+                }
+                const int r = rr[j];
+                const int owner = r / rows_per, lr = r - owner * rows_per;
+                float *acc_row = recv_acc + ((int64_t)rank * rows_per + lr) * kHeadDim;
+                const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
+#pragma unroll
+                for (int nn = 0; nn < 16 / SH::kSlices; ++nn) {
+                    const int n = ksl * (16 / SH::kSlices) + nn;
+                    float v0 = 0.f, v1 = 0.f;
 #pragma unroll
                     for (int k = 0; k < SH::kSlices; ++k) {
-                        wk[k] = exp2f(mk[k] - muse);
-                        ll += wk[k] * (k == 0 ? lrow[j] : xs[((k - 1) * 2 + mb) * SH::kXPer + (66 + j) * 32 + lane]);
+                        const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
+                        v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
+                        v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
                     }
-                    const int r = rr[j];
-                    const int owner = r / rows_per, lr = r - owner * rows_per;
-                    float *acc_row = recv_acc + ((int64_t)rank * rows_per + lr) * kHeadDim;
-                    const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
-#pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        float v0 = oacc[n][2 * j] * wk[0], v1 = oacc[n][2 * j + 1] * wk[0];
-#pragma unroll
-                        for (int k = 1; k < SH::kSlices; ++k) {
-                            const float *x = xs + ((k - 1) * 2 + mb) * SH::kXPer;
-                            v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
-                            v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
-                        }
-                        st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
-                    }
-                    if (c == 0)
-                        st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rows_per + lr), (uint32_t)owner),
-                                      mm, ll);
+                    st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
                 }
+                if (ksl == 0 && c == 0)
+                    st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rows_per + lr), (uint32_t)owner),
+                                  mm, ll);
             }
         } else {
             // merge the two key halves through stage buffer 0 (idle now), then write this
