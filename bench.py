@@ -89,6 +89,14 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi's own start-up (driver and NVML initialisation) must not fall inside
+        # the timed region: wait for its first sample
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -262,6 +270,9 @@ def run_gb300(args):
     def timed_loop(r, step, t0, n, pre=None, post=None):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
+        # an untimed ~1 ms spin first lets the host queue steps ahead of the device, so a
+        # host hiccup never leaves the device idle inside a timed step
+        torch.cuda._sleep(2_000_000)
         for j in range(n):
             a, b = evs[j]
             a.record(stream)

@@ -3,7 +3,7 @@
 // Page "DFLASH2_RING_PORT.md", sections 1.1 and 1.4: the q_len noise queries attend to
 // all kv_total slots of the layer's F16 K/V tensors under mask_full or mask_swa.  The
 // kernel streams each kv head's visible 64-slot tiles with 3-D TMA boxes into a
-// 3-stage shared-memory ring (128-byte swizzle), guarded by mbarriers.  One producer
+// shared-memory ring of stages (128-byte swizzle), guarded by mbarriers.  One producer
 // warp issues the copies (plus a 16-byte-aligned bulk copy of the tile's per-row
 // visibility bits when the tile is only partly visible); the consumer warps compute
 // S = Q K^T and O += P V on the F16 tensor cores (m16n8k16, F32 accumulation) with an
@@ -33,16 +33,16 @@ constexpr int kQBytes = kRows * kHeadDim * 2;
 constexpr int kBitsPerStage = kMaxQWords * 8;      // visibility words of one tile
 constexpr uint64_t kWaitNs = 2000000000ull;        // bounded waits give up after 2 s
 
-// Two shapes of one kernel.  CLUSTER: 8 consumer warps (4 key slices), one CTA per SM,
-// partial states pushed to the owning CTA of the cluster.  Plain: 4 consumer warps (2 key
-// halves), two CTAs per SM, key halves merged in shared memory and the CTA's partial
-// written straight from registers.
+// Two shapes of one kernel.  CLUSTER: 8 consumer warps (4 key slices), 6 stages, one CTA
+// per SM, partial states pushed to the owning CTA of the cluster.  Plain: 4 consumer warps
+// (2 key halves), 3 stages, two CTAs per SM, key halves merged in shared memory and the
+// CTA's partial written straight from registers.
 template <bool CLUSTER>
 struct Shape {
     static constexpr int CW = CLUSTER ? 8 : 4;      // consumer warps
     static constexpr int kConsumers = CW * 32;
     static constexpr int kThreads = kConsumers + 32;
-    static constexpr int kStages = CLUSTER ? 4 : 3;
+    static constexpr int kStages = CLUSTER ? 6 : 3;
     static constexpr int kSlices = CW / 2;          // key slices per tile
     static constexpr int kKeys = kTile / kSlices;   // keys per warp per tile (32 or 16)
     static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
@@ -501,24 +501,38 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const int i1 = r1 < d.rows ? r1 % d.q_len : 0;
         const int key0 = ksl * SH::kKeys;
 
-        int it = 0;
-        for (int t = t0; t < t1; ++t) {
-            const int flag = flags[t];
-            if (flag == 0) continue;
-            const int stg = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            // every lane waits (each needs the barrier's acquire of the copied bytes); the
-            // vote keeps the warp together if the bounded wait ever gives up
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * stg, ph))) {
-                if (lane == 0) atomicOr(m.err, kErrWaitFull);
-                s_abort = 1;
-                break;
+        // Visible tiles of this split, 32 at a time: one flags load per chunk, then the
+        // set bits of two warp ballots (any visible / partly visible) give the tiles.
+        int cbase = t0;
+        uint32_t vis = 0u, part = 0u;
+        auto next_tile = [&](int &t, int &flag) -> bool {
+            while (vis == 0u) {
+                if (cbase >= t1) return false;
+                const int u = cbase + lane;
+                const int f = u < t1 ? (int)flags[u] : 0;
+                vis = __ballot_sync(0xffffffffu, f != 0);
+                part = __ballot_sync(0xffffffffu, f == 2);
+                cbase += 32;
             }
+            const int bit = __ffs(vis) - 1;
+            vis &= vis - 1u;
+            t = cbase - 32 + bit;
+            flag = ((part >> bit) & 1u) ? 2 : 1;
+            return true;
+        };
+        // every lane waits (each needs the barrier's acquire of the copied bytes); the
+        // vote keeps the warp together if the bounded wait ever gives up
+        auto wait_full = [&](int i) -> bool {
+            if (__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u)))
+                return true;
+            if (lane == 0) atomicOr(m.err, kErrWaitFull);
+            s_abort = 1;
+            return false;
+        };
+        // S = Q K^T over this warp's keys of stage `stg`, scaled to the log2 domain and
+        // masked by the tile's per-row visibility bits when it is only partly visible
+        auto qk = [&](int stg, int flag, float (&sc)[SH::kNT][4]) {
             const uint32_t sk = smem_u32(smem + stg * kStageBytes);
-            const uint32_t sv = sk + kTileBytes;
-
-            // S = Q K^T over this warp's keys
-            float sc[SH::kNT][4];
 #pragma unroll
             for (int n = 0; n < SH::kNT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
@@ -537,7 +551,6 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[n][e] *= scale_log2;
             if (flag == 2) {
-                // per-row visibility bits of this tile arrived with it
                 const uint64_t w0 = sbits[stg * kMaxQWords + i0], w1 = sbits[stg * kMaxQWords + i1];
 #pragma unroll
                 for (int n = 0; n < SH::kNT; ++n)
@@ -548,8 +561,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                         if (!((w1 >> bit) & 1ull)) sc[n][2 + e] = -INFINITY;
                     }
             }
-
-            // online softmax (log2 domain), rows r0 (j = 0) and r1 (j = 1)
+        };
+        // online softmax (log2 domain) of rows r0 (j = 0) and r1 (j = 1), then O += P V
+        // over the same keys of stage `stg`, then the stage goes back to the producer
+        auto softmax_pv = [&](int stg, float (&sc)[SH::kNT][4]) {
             float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -583,8 +598,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     oacc[n][3] *= alpha[1];
                 }
             }
-
-            // O += P V over the same keys
+            const uint32_t sv = smem_u32(smem + stg * kStageBytes) + kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < SH::kKK; ++kk) {
                 uint32_t pa[4];
@@ -603,6 +617,14 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar0 + 8 * (kStages + stg));
+        };
+
+        int it = 0, t = 0, flag = 0;
+        while (next_tile(t, flag)) {
+            if (!wait_full(it)) break;
+            float sc[SH::kNT][4];
+            qk(it % kStages, flag, sc);
+            softmax_pv(it % kStages, sc);
             ++it;
         }
 

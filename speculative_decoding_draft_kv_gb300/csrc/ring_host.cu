@@ -320,9 +320,15 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     int max_cluster = p->max_cluster > 0 ? p->max_cluster : 16;
     choose_split(d, sms, max_cluster, p->tiles_per_split);
     {
+        // one wave: every CTA (every cluster) of the attention grid resident at once; only
+        // then may the kernel release its dependents early (they would otherwise hold SMs
+        // that its own later CTAs wait for)
         const int64_t ctas = (int64_t)d.n_splits * d.n_head_kv * d.n_seq;
-        const int64_t resident = (d.cluster > 1 ? 1LL : 2LL) * std::max(sms, 1);
-        d.single_wave = ctas <= resident ? 1 : 0;
+        if (d.cluster > 1)
+            d.single_wave = ctas / d.cluster <= (int64_t)attend_cluster_capacity(d.cluster) &&
+                            ctas <= std::max(sms, 1);
+        else
+            d.single_wave = ctas <= 2LL * std::max(sms, 1) ? 1 : 0;
     }
 
     const size_t kv_elems = (size_t)d.n_seq * d.n_layer * d.n_head_kv * d.kv_total * d.head_dim;

@@ -184,9 +184,31 @@ def test_split_sizes_agree(tps, max_cluster):
         assert g["n_splits"] * g["tiles_per_split"] >= g["n_tiles"]
         for t, c in enumerate(synth.commit_schedule(w, 3)):
             run.begin_step(c)
-        for kind in ("full",):
+            if t >= 2:      # repeated launches reuse the partial buffers
+                for layer in (1, 0, 1):
+                    o = run.attend(t, layer, "full")
+                    assert_close(o[0], run.expected(t, layer, "full", 0),
+                                 f"tps {tps} cluster {g['cluster']} groups {g['groups']}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("q_len,n_head,max_cluster", [(1, 32, 0), (4, 32, 0), (5, 32, 0),
+                                                      (7, 32, 0), (8, 16, 0), (3, 64, 0),
+                                                      (5, 32, 1)])
+def test_query_row_shapes(q_len, n_head, max_cluster):
+    """Query blocks of G * q_len rows that fill one or both 16-row blocks of a CTA, or only
+    part of them, in clusters and in plain CTAs; SWA included."""
+    w = synth.workload(2, cap=1024, n_layer=2, q_len=q_len, n_head=n_head, swa_window=300)
+    run = GpuRun(w, max_cluster=max_cluster)
+    try:
+        for t, c in enumerate(synth.commit_schedule(w, 3)):
+            run.begin_step(c)
+        run.check_slots_and_masks()
+        for kind in ("full", "swa"):
             o = run.attend(3, 1, kind)
-            assert_close(o[0], run.expected(3, 1, kind, 0), f"tps {tps} cluster {g['cluster']}")
+            assert_close(o[0], run.expected(3, 1, kind, 0), f"q_len {q_len} heads {n_head} {kind}")
         assert run.ring.device_error() == 0
     finally:
         run.close()
