@@ -37,8 +37,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_117_184, "kernel": "3a842b1bf64ebf66",
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_130_368, "kernel": "6e70da9100971eb7",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
+    "batched_cap4096_s16_l5": {"bytes": 276_977_920, "kernel": "6e70da9100971eb7",
+                               "source": "profiles/attend_plain_batched_cap4096_s16_l5.md"},
 }
 
 
