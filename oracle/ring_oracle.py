@@ -30,6 +30,18 @@ Readings taken where the page is silent (each is listed in the design notes):
   R10 rows handed to begin_step cover [first_pos, committed); only [start, committed)
       is stored, positions below lo are ignored.
 
+The context-row producer (page "DFLASH2_RING_PORT.md", test 11, point 4 of the refuted
+hypotheses: the draft's context K/V come from a shallow injection of the fused target
+features, wk/wv times the features, then k_norm, then RoPE):
+  P1  the pre-RoPE context row of position p is K = k_norm(W_k x_p), V = W_v x_p, with
+      x_p the fused feature vector of p (F16, width ``hidden``, shared by the layers)
+      and W_k, W_v F16 [kv_row, hidden] per layer;
+  P2  k_norm is an RMS norm over each kv head's head_dim slice,
+      y = x / sqrt(mean(x^2) + eps) * w, with one learned weight w [head_dim] per layer
+      shared by the heads and eps = 1e-6;
+  P3  K then takes RoPE at p (R5, R6) and is rounded to F16; V is rounded to F16
+      straight from the product.
+
 Precision: float64 throughout, except for the F16 storage of K and V that the page
 fixes.  Parity pins for every function here live in tests/test_oracle_*.py.
 """
@@ -133,6 +145,36 @@ def rope_rows(rows, pos, n_heads: int, head_dim: int, theta: float) -> np.ndarra
     r = rows.reshape(shp[:-1] + (n_heads, head_dim))
     p = np.asarray(pos, dtype=np.float64)[..., None]        # same angle for every head
     return rope_neox(r, p, theta).reshape(shp)
+
+
+# ---------------------------------------------------------------------------
+# context-row producer (P1-P3): projection, per-head RMS norm
+# ---------------------------------------------------------------------------
+
+def rms_norm_heads(x, w, eps: float, n_heads: int, head_dim: int) -> np.ndarray:
+    """RMS norm of every head slice of rows [..., n_heads * head_dim] (P2), float64.
+
+    Each head's slice is divided by the root of its mean square plus ``eps`` and then
+    multiplied elementwise by ``w`` [head_dim].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    shp = x.shape
+    r = x.reshape(shp[:-1] + (n_heads, head_dim))
+    ms = np.mean(r * r, axis=-1, keepdims=True)
+    y = r / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
+    return y.reshape(shp)
+
+
+def produce_rows(feat, wk, wv, k_norm_w, eps: float, n_head_kv: int, head_dim: int):
+    """Context rows of fused features ``feat`` [n, hidden] for one layer (P1, P2).
+
+    Returns the pre-RoPE K rows (float64, not rounded: RoPE and the F16 rounding follow,
+    P3) and the V rows (F16), both [n, n_head_kv * head_dim].
+    """
+    x = np.asarray(feat, dtype=np.float64)
+    k = x @ np.asarray(wk, dtype=np.float64).T
+    v = x @ np.asarray(wv, dtype=np.float64).T
+    return rms_norm_heads(k, k_norm_w, eps, n_head_kv, head_dim), to_f16(v)
 
 
 # ---------------------------------------------------------------------------

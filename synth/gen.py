@@ -1,4 +1,5 @@
-"""Counter-based seeded generator for K/V rows, queries and noise-block rows.
+"""Counter-based seeded generator for K/V rows, queries, noise-block rows, fused features
+and the context-row producer's weights.
 
 Every value is a pure function of ``(seed, kind, seq, layer, index, column)``:
 
@@ -29,6 +30,10 @@ KIND_V_ROW = 2
 KIND_Q = 3
 KIND_K_NOISE = 4
 KIND_V_NOISE = 5
+KIND_FEATURE = 6        # fused target features, keyed by absolute position
+KIND_W_K = 7            # producer weights, keyed by output row
+KIND_W_V = 8
+KIND_K_NORM = 9
 
 # Standard deviation of a sum of four independent uniform integers on [0, 65535].
 _IRWIN_HALL4_STD = math.sqrt(4.0 * (65536.0 ** 2 - 1.0) / 12.0)
@@ -116,3 +121,25 @@ def noise_rows(seed: int, step: int, seq: int, layer: int, q_len: int, kv_row: i
     k = _rows(seed, KIND_K_NOISE, seq, layer, idx, kv_row, sigma).to(torch.float16)
     v = _rows(seed, KIND_V_NOISE, seq, layer, idx, kv_row, sigma).to(torch.float16)
     return k, v
+
+
+def feature_rows(seed: int, seq: int, positions, hidden: int, sigma: float, device=None,
+                 chunk_rows: int = 4096):
+    """Fused target features of absolute ``positions``, float16 ``[n, hidden]`` (the same
+    vector feeds every layer's producer)."""
+    pos = torch.as_tensor(positions, dtype=torch.int64, device=device)
+    return _rows(seed, KIND_FEATURE, seq, 0, pos, hidden, sigma, chunk_rows).to(torch.float16)
+
+
+def producer_weights(seed: int, layer: int, kv_row: int, hidden: int, head_dim: int,
+                     device=None):
+    """One layer's producer weights: W_k and W_v float16 ``[kv_row, hidden]`` with entries
+    of standard deviation 1/sqrt(hidden), and the k_norm weight float32 ``[head_dim]``
+    around 1 (standard deviation 0.1)."""
+    rows = torch.arange(kv_row, dtype=torch.int64, device=device)
+    sig = 1.0 / math.sqrt(hidden)
+    wk = _rows(seed, KIND_W_K, 0, layer, rows, hidden, sig).to(torch.float16)
+    wv = _rows(seed, KIND_W_V, 0, layer, rows, hidden, sig).to(torch.float16)
+    one = torch.zeros(1, dtype=torch.int64, device=device)
+    kn = 1.0 + _rows(seed, KIND_K_NORM, 0, layer, one, head_dim, 0.1)[0]
+    return wk, wv, kn

@@ -15,24 +15,41 @@ import synth
 from oracle import ring_oracle as orc
 
 
-def _rows_fn(w, seq, layer):
-    def fn(pos):
-        k, v = synth.context_rows(w.seed, seq, layer, torch.as_tensor(pos), w.kv_row, w.sigma)
-        return k.numpy(), v.numpy()
-    return fn
+def _context_rows(w, seq, layer, pos):
+    k, v = synth.context_rows(w.seed, seq, layer, torch.as_tensor(pos), w.kv_row, w.sigma)
+    return k.numpy(), v.numpy()
 
 
-def _step_rows(w, seq, start, c):
-    pos = torch.arange(start, c)
+def _produced_rows(hidden, eps):
+    """Rows made by the context-row producer from seeded features and weights."""
+    cache = {}
+
+    def rows(w, seq, layer, pos):
+        if layer not in cache:
+            cache[layer] = [x.numpy() for x in synth.producer_weights(w.seed, layer, w.kv_row,
+                                                                      hidden, w.head_dim)]
+        wk, wv, kn = cache[layer]
+        feat = synth.feature_rows(w.seed, seq, torch.as_tensor(pos, dtype=torch.int64), hidden,
+                                  w.sigma).numpy()
+        return orc.produce_rows(feat, wk, wv, kn, eps, w.n_head_kv, w.head_dim)
+    return rows
+
+
+def _rows_fn(w, seq, layer, source=_context_rows):
+    return lambda pos: source(w, seq, layer, np.asarray(pos))
+
+
+def _step_rows(w, seq, start, c, source=_context_rows):
+    pos = np.arange(start, c)
     ks, vs = [], []
     for layer in range(w.n_layer):
-        k, v = synth.context_rows(w.seed, seq, layer, pos, w.kv_row, w.sigma)
-        ks.append(k.numpy())
-        vs.append(v.numpy())
+        k, v = source(w, seq, layer, pos)
+        ks.append(k)
+        vs.append(v)
     return np.stack(ks), np.stack(vs)
 
 
-def _run_equivalence(w, n_steps, kinds):
+def _run_equivalence(w, n_steps, kinds, source=_context_rows):
     r = orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                        w.rope_theta, swa_window=w.swa_window)
     sched = synth.commit_schedule(w, n_steps)
@@ -40,14 +57,14 @@ def _run_equivalence(w, n_steps, kinds):
     for t, c in enumerate(sched[:, 0]):
         c = int(c)
         start, _ = r.rows_needed(c)
-        k, v = _step_rows(w, 0, start, c)
+        k, v = _step_rows(w, 0, start, c, source)
         r.begin_step(c, k, v, start)
         for layer in range(w.n_layer):
             q = synth.query_block(w.seed, t, 0, layer, w.q_len, w.n_head, w.head_dim, w.sigma)
             kn, vn = synth.noise_rows(w.seed, t, 0, layer, w.q_len, w.kv_row, w.sigma)
             for kind in kinds:
                 o1 = r.attend(layer, q.numpy(), kn.numpy(), vn.numpy(), kind)
-                o2 = orc.attend_dense(c, w.cap, _rows_fn(w, 0, layer), q.numpy(), kn.numpy(),
+                o2 = orc.attend_dense(c, w.cap, _rows_fn(w, 0, layer, source), q.numpy(), kn.numpy(),
                                       vn.numpy(), w.head_dim, w.n_head_kv, w.n_head,
                                       w.rope_theta, kind=kind, swa_window=w.swa_window)
                 worst = max(worst, float(np.abs(o1 - o2).max()))
@@ -63,6 +80,13 @@ def test_ring_equals_dense_window_with_bulk_jumps():
     w = synth.workload(3, cap=48, n_layer=2, head_dim=16, n_head_kv=2, n_head=4,
                        extra={"jump_max": 400, "fold_max": 18, "p_jump": 0.4})
     assert _run_equivalence(w, 30, ("full",)) < 1e-12
+
+
+def test_ring_equals_dense_window_with_produced_rows():
+    """The same equivalence when the context rows come from the producer (P1-P3)."""
+    w = synth.workload(3, cap=48, n_layer=2, head_dim=16, n_head_kv=2, n_head=4,
+                       extra={"jump_max": 200, "fold_max": 18, "p_jump": 0.3})
+    assert _run_equivalence(w, 20, ("full",), _produced_rows(64, 1e-6)) < 1e-12
 
 
 def test_naive_roll_differs_once_rows_are_evicted():

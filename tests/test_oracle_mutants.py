@@ -112,7 +112,53 @@ def _begin_step_no_pad_zero(self, committed, k_rows, v_rows, first_pos):
     return path
 
 
+_ORIG_RMS = orc.rms_norm_heads
+
+
+def _rms_whole_row(x, w, eps, n_heads, head_dim):
+    return _ORIG_RMS(x, np.tile(np.asarray(w, np.float64), n_heads), eps, 1, n_heads * head_dim)
+
+
+def _rms_eps_outside_root(x, w, eps, n_heads, head_dim):
+    x = np.asarray(x, np.float64)
+    r = x.reshape(x.shape[:-1] + (n_heads, head_dim))
+    ms = np.mean(r * r, axis=-1, keepdims=True)
+    return (r / (np.sqrt(ms) + eps) * np.asarray(w, np.float64)).reshape(x.shape)
+
+
+def _rms_weight_ignored(x, w, eps, n_heads, head_dim):
+    return _ORIG_RMS(x, np.ones(head_dim), eps, n_heads, head_dim)
+
+
+def _rms_mean_over_heads(x, w, eps, n_heads, head_dim):
+    x = np.asarray(x, np.float64)
+    r = x.reshape(x.shape[:-1] + (n_heads, head_dim))
+    ms = np.mean(r * r, axis=-2, keepdims=True)
+    return (r / np.sqrt(ms + eps) * np.asarray(w, np.float64)).reshape(x.shape)
+
+
+def _produce_transposed(feat, wk, wv, k_norm_w, eps, n_head_kv, head_dim):
+    x = np.asarray(feat, np.float64)
+    k = x @ np.asarray(wk, np.float64)
+    v = x @ np.asarray(wv, np.float64)
+    return orc.rms_norm_heads(k, k_norm_w, eps, n_head_kv, head_dim), orc.to_f16(v)
+
+
+def _produce_v_normalised(feat, wk, wv, k_norm_w, eps, n_head_kv, head_dim):
+    x = np.asarray(feat, np.float64)
+    k = x @ np.asarray(wk, np.float64).T
+    v = x @ np.asarray(wv, np.float64).T
+    return (orc.rms_norm_heads(k, k_norm_w, eps, n_head_kv, head_dim),
+            orc.to_f16(orc.rms_norm_heads(v, k_norm_w, eps, n_head_kv, head_dim)))
+
+
 MUTANTS = {
+    "k_norm over the whole row": ("rms_norm_heads", _rms_whole_row),
+    "k_norm eps outside the root": ("rms_norm_heads", _rms_eps_outside_root),
+    "k_norm weight ignored": ("rms_norm_heads", _rms_weight_ignored),
+    "k_norm mean across heads": ("rms_norm_heads", _rms_mean_over_heads),
+    "producer weights transposed": ("produce_rows", _produce_transposed),
+    "producer normalises V too": ("produce_rows", _produce_v_normalised),
     "slot map off by one": ("slot_of", lambda p, cap: (p + 1) % cap),
     "lo off by one": ("step_window", _step_window_lo_off_by_one),
     "mask_full shows empty slots": ("RingOracle.mask_full", _mask_full_shows_empty_slots),
@@ -148,6 +194,10 @@ PINS = [
     lambda: pins.test_dense_route_zero_query_closed_form("full"),
     lambda: pins.test_dense_route_zero_query_closed_form("swa"),
     eqv.test_ring_equals_dense_window_tiny_workload,
+    pins.test_k_norm_special_cases,
+    pins.test_k_norm_epsilon_inside_the_root,
+    pins.test_producer_brute_force_small_integers,
+    pins.test_producer_permutation_weights_pick_features,
 ]
 
 

@@ -340,3 +340,78 @@ def test_dense_route_zero_query_closed_form(kind):
             else:
                 want = (c - min(swa, min(c, cap)) + c + i) / 2.0
             np.testing.assert_allclose(o[i], want, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# context-row producer: k_norm(W_k x), W_v x (readings P1-P3)
+# ---------------------------------------------------------------------------
+
+def test_k_norm_special_cases():
+    """eps = 0: a constant head maps to w; a head with one non-zero entry a at index j
+    maps to sign(a) sqrt(head_dim) w_j there and 0 elsewhere; scaling a head changes
+    nothing; heads are normalised one by one (each head's mean square becomes 1)."""
+    d, nh = 8, 3
+    w = np.array([1.0, 2.0, -1.0, 0.5, 3.0, 1.5, -2.0, 0.25])
+    x = np.concatenate([np.full(d, 7.0), np.zeros(d), np.full(d, -0.5)])
+    x[d + 5] = -3.0
+    y = orc.rms_norm_heads(x, w, 0.0, nh, d)
+    np.testing.assert_allclose(y[:d], w, rtol=0, atol=1e-15)
+    e = np.zeros(d)
+    e[5] = -math.sqrt(d) * w[5]
+    np.testing.assert_allclose(y[d:2 * d], e, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(y[2 * d:], -w, rtol=0, atol=1e-15)
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((4, nh * d)) * np.array([1e-3] * d + [1.0] * d + [1e3] * d)
+    one = np.ones(d)
+    yz = orc.rms_norm_heads(z, one, 0.0, nh, d).reshape(4, nh, d)
+    np.testing.assert_allclose(np.mean(yz * yz, axis=-1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(orc.rms_norm_heads(z * 37.5, one, 0.0, nh, d),
+                               orc.rms_norm_heads(z, one, 0.0, nh, d), rtol=1e-13)
+
+
+def test_k_norm_epsilon_inside_the_root():
+    """A head whose mean square equals eps is divided by sqrt(2 eps)."""
+    d = 4
+    x = np.full(d, 1e-3)                       # mean square 1e-6
+    y = orc.rms_norm_heads(x, np.ones(d), 1e-6, 1, d)
+    np.testing.assert_allclose(y, 1e-3 / math.sqrt(2e-6), rtol=1e-14)
+
+
+def test_producer_brute_force_small_integers():
+    """Small integer features and weights: every product is exact, so V equals the
+    brute-force triple loop exactly; K's heads each have mean square 1 (w = 1, eps = 0)
+    and point the same way as the brute-force projection."""
+    rng = np.random.default_rng(11)
+    n, hidden, nh, d = 5, 12, 2, 4
+    feat = rng.integers(-2, 3, (n, hidden)).astype(np.float16)
+    wk = rng.integers(-1, 2, (nh * d, hidden)).astype(np.float16)
+    wv = rng.integers(-1, 2, (nh * d, hidden)).astype(np.float16)
+    k, v = orc.produce_rows(feat, wk, wv, np.ones(d), 0.0, nh, d)
+    for r in range(n):
+        for o in range(nh * d):
+            acc_v = 0.0
+            acc_k = 0.0
+            for i in range(hidden):
+                acc_v += float(feat[r, i]) * float(wv[o, i])
+                acc_k += float(feat[r, i]) * float(wk[o, i])
+            assert float(v[r, o]) == acc_v
+    kb = np.array([[sum(float(feat[r, i]) * float(wk[o, i]) for i in range(hidden))
+                    for o in range(nh * d)] for r in range(n)]).reshape(n, nh, d)
+    kk = k.reshape(n, nh, d)
+    for r in range(n):
+        for h in range(nh):
+            if np.any(kb[r, h]):
+                np.testing.assert_allclose(np.mean(kk[r, h] ** 2), 1.0, rtol=1e-13)
+                cosang = kk[r, h] @ kb[r, h] / (np.linalg.norm(kk[r, h]) * np.linalg.norm(kb[r, h]))
+                np.testing.assert_allclose(cosang, 1.0, rtol=1e-13)
+
+
+def test_producer_permutation_weights_pick_features():
+    """W_v a permutation matrix (not symmetric): V row = the permuted features, exactly."""
+    hidden = 8
+    perm = np.array([3, 0, 6, 1, 7, 2, 5, 4])
+    P = np.zeros((hidden, hidden), np.float16)
+    P[np.arange(hidden), perm] = 1.0
+    feat = (np.arange(2 * hidden, dtype=np.float64).reshape(2, hidden) - 5.0).astype(np.float16)
+    _, v = orc.produce_rows(feat, P, P, np.ones(4), 0.0, 2, 4)
+    np.testing.assert_array_equal(v, feat[:, perm])

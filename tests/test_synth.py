@@ -67,3 +67,17 @@ def test_schedules_follow_their_workload():
     assert s4.shape == (11, 64) and s4[0].min() >= 1 and s4[0].max() <= 131072
     s5 = synth.commit_schedule(synth.workload(5), 10)
     assert s5.shape == (11, 16) and s5[0].min() >= 131072
+
+
+def test_feature_rows_and_producer_weights_are_pure_functions():
+    a = synth.feature_rows(7, 1, torch.arange(10, 20), 256, 0.5)
+    b = synth.feature_rows(7, 1, torch.tensor([15, 12]), 256, 0.5)
+    assert torch.equal(a[5], b[0]) and torch.equal(a[2], b[1])
+    assert not torch.equal(a[0], synth.feature_rows(7, 2, torch.tensor([10]), 256, 0.5)[0])
+    wk, wv, kn = synth.producer_weights(7, 3, 64, 256, 16)
+    wk2, wv2, kn2 = synth.producer_weights(7, 3, 64, 256, 16)
+    assert torch.equal(wk, wk2) and torch.equal(wv, wv2) and torch.equal(kn, kn2)
+    assert wk.dtype == torch.float16 and kn.dtype == torch.float32 and kn.shape == (16,)
+    assert not torch.equal(wk, wv)
+    assert abs(float(wk.float().std()) - 1 / 16) < 0.01
+    assert not torch.equal(wk, synth.producer_weights(7, 4, 64, 256, 16)[0])
