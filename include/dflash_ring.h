@@ -98,10 +98,11 @@ typedef struct ring_geometry {
 
 /* Per-kernel timing collected while profiling is on (CUDA events on the launch stream). */
 typedef struct ring_profile {
-    int64_t launches[5];     /* 0 bulk append chunk, 1 begin-step kernel (fold-in append,
+    int64_t launches[6];     /* 0 bulk append chunk, 1 begin-step kernel (fold-in append,
                                 slot_pos, masks, flags, RoPE table), 2 attention, 3 group
-                                combine, 4 whole-step graph replay (ring_step)             */
-    double total_ms[5];      /* summed event time per kernel class                          */
+                                combine, 4 whole-step graph replay (ring_step), 5 context-
+                                row producer (ring_begin_step_features)                     */
+    double total_ms[6];      /* summed event time per kernel class                          */
 } ring_profile;
 
 /*
@@ -155,6 +156,49 @@ int ring_rows_needed(const ring_t *r, int32_t seq, int64_t committed, int64_t *s
 int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows,
                     const void *v_rows, const int64_t *row_off, const int64_t *first_pos,
                     int64_t n_rows, void *stream);
+
+/*
+ * Context-row producer -- page "DFLASH2_RING_PORT.md", test 11, point 4 of the refuted
+ * hypotheses: the draft's context K/V rows come from the fused target features by
+ * W_k / W_v times the feature vector, then k_norm, then RoPE.  Readings: k_norm is an RMS
+ * norm over each kv head's head_dim slice, x / sqrt(mean(x^2) + eps) times one learned
+ * weight [head_dim] per layer; V is not normalised; both round once to F16.
+ *
+ *   hidden   width of one fused feature row; a positive multiple of 64.
+ *   eps      k_norm epsilon (>= 0; 1e-6 for the drafts on the page).
+ *   wk, wv   device F16 [n_layer][kv_row][hidden], row-major, 16-byte aligned.
+ *   k_norm   device F32 [n_layer][head_dim].
+ *
+ * The ring keeps the pointers (the caller owns the memory and keeps it alive and unchanged
+ * while steps run); p == NULL detaches the producer.  Errors: EINVAL, ECUDA.
+ */
+typedef struct ring_producer {
+    int32_t hidden;
+    float eps;
+    const void *wk;
+    const void *wv;
+    const float *k_norm;
+} ring_producer;
+int ring_set_producer(ring_t *r, const ring_producer *p);
+
+/*
+ * ring_begin_step_features -- ring_begin_step with the context rows made on the device
+ * from fused features: for every new position p of every sequence (the same window
+ * arithmetic, fold-in and bulk), K = RoPE_p(k_norm(W_k x_p)) and V = W_v x_p of every
+ * layer are computed on the tensor cores and written straight into slot p % cap
+ * (F16, round to nearest even), with slot_pos; pad rows of the fold-in path still go to
+ * trash_slot as zeros; masks and flags as in ring_begin_step.
+ *
+ *   feat       device F16 [n_rows][hidden], 16-byte aligned: one fused feature row per
+ *              position, shared by every layer.
+ *   row_off, first_pos, n_rows  as in ring_begin_step (rows of sequence s cover
+ *              [first_pos[s], committed[s]) from row row_off[s]).
+ *
+ * Errors: ESTATE (no producer set), EINVAL, ERANGE (state unchanged), ECUDA.
+ */
+int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *feat,
+                             const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                             void *stream);
 
 /*
  * ring_attend -- one draft layer's masked attention, enqueued on `stream`.

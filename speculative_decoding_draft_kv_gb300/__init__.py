@@ -16,6 +16,7 @@ from .ring import (  # noqa: F401
     ring_attend,
     ring_attend_static,
     ring_begin_step,
+    ring_begin_step_features,
     ring_describe,
     ring_destroy,
     ring_device_error,
@@ -31,5 +32,6 @@ from .ring import (  # noqa: F401
     ring_profile_enable,
     ring_profile_read,
     ring_rows_needed,
+    ring_set_producer,
     ring_step,
 )

@@ -124,10 +124,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -181,6 +177,15 @@ __device__ __forceinline__ uint32_t cluster_size() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
     return r;
+}
+
+// A CTA may write into a peer's shared memory only once the peer runs: every thread
+// arrives here right after start-up and waits before its first remote store.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -283,6 +288,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    if constexpr (CLUSTER) cluster_arrive_relaxed();
 
     if (warp == CW) {
         // ---------------- producer ----------------
@@ -390,6 +396,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
         }
         __syncwarp();
+        if constexpr (CLUSTER) cluster_wait();
     } else {
         // ---------------- consumers ----------------
         pdl_wait();   // ring state written by begin_step (and earlier kernels) is visible
@@ -634,6 +641,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             lrow[j] += __shfl_xor_sync(0xffffffffu, lrow[j], 2);
         }
         if constexpr (CLUSTER) {
+            cluster_wait();     // every CTA of the cluster has started (see cluster_arrive_relaxed)
             // Merge the key slices of each row block inside this CTA, then push one partial
             // per row to the CTA of the cluster that finishes that row.  Every warp first
             // publishes its partial (in the idle stage buffers); warp (mb, ksl) then merges

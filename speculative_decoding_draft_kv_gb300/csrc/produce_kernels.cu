@@ -1,0 +1,397 @@
+// Context-row producer: fused target features -> ring K/V rows, one kernel.
+//
+// Page "DFLASH2_RING_PORT.md", test 11 (point 4 of the refuted hypotheses): the draft's
+// context K/V rows are a shallow injection of the fused target features -- W_k and W_v
+// times the feature vector, then k_norm, then RoPE -- and section 1.2 puts the row of
+// position p into slot p % cap.  Here the projection, the per-head RMS norm, RoPE at p,
+// the F16 rounding and the scatter into the ring are one kernel, so the pre-RoPE rows
+// never make a round trip through HBM.
+//
+// Shape: a CTA owns 32 feature rows (the step's new positions, packed across sequences)
+// and one 128-wide head of K or of V of one layer.  C = X W^T runs on the F16 tensor cores
+// (m16n8k16, F32 accumulation): W tiles (128 x 64) arrive by TMA, the gathered feature
+// rows (32 x 64) by 16-byte cp.async, both into a 4-stage shared-memory ring guarded by
+// mbarriers.  With few rows the kernel streams weights, so the hidden dimension is split
+// over a thread-block cluster of `ks` CTAs whose partial tiles are summed in the shared
+// memory of the CTA that owns each row (distributed shared memory stores).  The owner then
+// normalises, turns and stores its rows: one warp per row, lane l holding columns
+// l, l+32, l+64, l+96, so both members of every rotary pair sit in one lane.
+#include "ring_internal.h"
+
+#include <cuda_fp16.h>
+
+namespace dflash {
+namespace {
+
+constexpr int kPM = 32;                    // feature rows per CTA
+constexpr int kPN = 128;                   // output columns per CTA: one head of K or V
+constexpr int kPK = 64;                    // hidden columns per stage
+constexpr int kPStages = 4;
+constexpr int kPBBytes = kPN * kPK * 2;    // W tile, 16 KiB (TMA box 64 x 128, 128B swizzle)
+constexpr int kPABytes = kPM * kPK * 2;    // feature tile, 4 KiB (same swizzle, by hand)
+constexpr int kPStage = kPBBytes + kPABytes;
+constexpr int kPConsumers = 128;           // 4 warps, warp w -> columns [32 w, 32 w + 32)
+constexpr int kPThreads = kPConsumers + 32;
+constexpr int kPMaxSplit = 8;
+constexpr int kPOffRecv = kPStages * kPStage;                 // [ks][rows_per][128] f32
+constexpr int kPOffBars = kPOffRecv + kPM * kPN * 4;
+constexpr int kPOffMap = kPOffBars + 2 * kPStages * 8;
+constexpr int kPSmem = 1024 + kPOffMap + kPM * 16;
+constexpr uint64_t kPWaitNs = 2000000000ull;
+static_assert(kPSmem <= 113 * 1024, "two producer CTAs per SM");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// bounded: false after kPWaitNs (or 2^30 polls), never an endless spin
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > kPWaitNs) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+// 16 bytes global -> shared; src_bytes 0 fills the destination with zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// arrive on `bar` once this thread's earlier cp.async copies have landed (the barrier's
+// expected count includes this arrival)
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// byte offset of (row r, 16-byte chunk holding column dcol) in a 128-byte-swizzled tile of
+// 64 columns
+__device__ __forceinline__ uint32_t swz64(int r, int dcol) {
+    return (uint32_t)(r * 128 + (((dcol >> 3) ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Remote shared-memory stores wait until every CTA of the cluster runs: all threads
+// arrive right after start-up and wait before the first remote store.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
+                 : "memory");
+}
+
+// Grid (ks * m_tiles, 2 * n_head_kv, n_layer); clusters of ks CTAs along x when ks > 1.
+// blockIdx.y < n_head_kv: K head y; else V head y - n_head_kv.
+__global__ void __launch_bounds__(kPThreads, 2)
+k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
+          RingDims d, RingDev m, const uint16_t *__restrict__ feat, int hidden, int ks,
+          int64_t m_total, const float *__restrict__ k_norm, float eps) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *recv = reinterpret_cast<float *>(smem + kPOffRecv);
+    const uint32_t bar0 = smem_u32(smem + kPOffBars);     // full[0..3], empty[0..3]
+    int64_t *map_pos = reinterpret_cast<int64_t *>(smem + kPOffMap);
+    int64_t *map_frow = map_pos + kPM;                    // -1: padding row
+    __shared__ int map_seq[kPM];
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ks > 1 ? cluster_rank() : 0u;
+    const int64_t tile = (int64_t)blockIdx.x / ks;
+    const int yk = blockIdx.y, layer = blockIdx.z;
+    const bool is_v = yk >= d.n_head_kv;
+    const int head = is_v ? yk - d.n_head_kv : yk;
+    const int nkt = hidden / kPK;
+    const int per = (nkt + ks - 1) / ks;
+    const int kt0 = min(nkt, (int)rank * per), kt1 = min(nkt, kt0 + per);
+    const int rows_per = kPM / ks;
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kPStages; ++k) {
+            mbar_init(bar0 + 8 * k, 1 + 32);     // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(bar0 + 8 * (kPStages + k), kPConsumers / 32);
+        }
+        s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        // row map: packed row index -> (sequence, position, feature row).  Sequence s owns
+        // rows [prod_base, prod_base + n_new) of the packed list.
+        const int64_t mr = tile * kPM + lane;
+        int sq = -1;
+        int64_t pos = 0, frow = -1;
+        if (mr < m_total) {
+            int lo = 0, hi = d.n_seq - 1;
+            while (lo < hi) {                       // last s with prod_base <= mr
+                const int mid = (lo + hi + 1) >> 1;
+                if (m.steps[mid].prod_base <= mr) lo = mid;
+                else hi = mid - 1;
+            }
+            const SeqStep st = m.steps[lo];
+            const int64_t i = mr - st.prod_base;
+            if (i < st.n_new) {
+                sq = lo;
+                pos = st.start + i;
+                frow = st.src_row + i;
+            }
+        }
+        map_seq[lane] = sq;
+        map_pos[lane] = pos;
+        map_frow[lane] = frow;
+    }
+    __syncthreads();
+    if (ks > 1) cluster_arrive_relaxed();
+
+    if (warp == kPConsumers / 32) {
+        // ---------------- producer warp ----------------
+        const CUtensorMap *tm = is_v ? &tm_wv : &tm_wk;
+        const int wrow = layer * d.kv_row + head * kPN;
+        int it = 0;
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+            const int stg = it % kPStages;
+            const uint32_t ph = (uint32_t)(it / kPStages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kPStages + stg), ph ^ 1u))) {
+                if (lane == 0) {
+                    atomicOr(m.err, kErrWaitEmpty);
+                    s_fail = 1;
+                }
+                break;
+            }
+            const uint32_t sb = smem_u32(smem + stg * kPStage);
+            const uint32_t sa = sb + kPBBytes;
+            const uint32_t full = bar0 + 8 * stg;
+            if (lane == 0) {
+                mbar_expect_tx(full, kPBBytes);
+                tma_load_2d(sb, tm, kt * kPK, wrow, full);
+            }
+#pragma unroll
+            for (int j = 0; j < (kPM * kPK / 8) / 32; ++j) {
+                const int u = j * 32 + lane;
+                const int r = u >> 3, c = u & 7;
+                const int64_t fr = map_frow[r];
+                const uint16_t *src = fr >= 0 ? feat + fr * hidden + kt * kPK + c * 8 : feat;
+                cp_async16(sa + swz64(r, c * 8), src, fr >= 0 ? 16u : 0u);
+            }
+            cp_async_arrive(full);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (ks > 1) cluster_wait();
+    } else {
+        // ---------------- consumer warps: C[32][32 w .. 32 w + 32) ----------------
+        float acc[2][4][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b][0] = acc[a][b][1] = acc[a][b][2] = acc[a][b][3] = 0.f;
+        int it = 0;
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
+            const int stg = it % kPStages;
+            const uint32_t ph = (uint32_t)(it / kPStages) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * stg, ph))) {
+                if (lane == 0) {
+                    atomicOr(m.err, kErrWaitFull);
+                    s_fail = 1;
+                }
+                break;
+            }
+            const uint32_t sb = smem_u32(smem + stg * kPStage);
+            const uint32_t sa = sb + kPBBytes;
+#pragma unroll
+            for (int ks16 = 0; ks16 < kPK / 16; ++ks16) {
+                uint32_t af[2][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+                    ldsm_x4(sa + swz64(mt * 16 + (lane & 15), ks16 * 16 + ((lane >> 4) << 3)),
+                            af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    const int n = warp * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(sb + swz64(n, ks16 * 16 + (((lane >> 3) & 1) << 3)), b0, b1, b2, b3);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        mma16816(acc[mt][np * 2], af[mt], b0, b1);
+                        mma16816(acc[mt][np * 2 + 1], af[mt], b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (kPStages + stg));
+        }
+        // partial tile -> the receive buffer of the CTA owning each row:
+        // recv[src rank][local row][128]
+        if (ks > 1) cluster_wait();
+        const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                const int r = mt * 16 + g + 8 * h8;
+                const int owner = r / rows_per, lr = r - owner * rows_per;
+                float *row = recv + ((int64_t)rank * rows_per + lr) * kPN;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int col = warp * 32 + nt * 8 + 2 * c;
+                    const float v0 = acc[mt][nt][2 * h8], v1 = acc[mt][nt][2 * h8 + 1];
+                    if (ks > 1) {
+                        st_cluster_v2(map_rank(smem_u32(row + col), (uint32_t)owner), v0, v1);
+                    } else {
+                        row[col] = v0;
+                        row[col + 1] = v1;
+                    }
+                }
+            }
+    }
+    if (ks > 1) cluster_sync();
+    else __syncthreads();
+    if (warp >= kPConsumers / 32 || s_fail) return;
+
+    // ---------------- epilogue: rows [rank * rows_per, +rows_per) of the tile ----------
+    const int half = kPN / 2;
+    for (int lr = warp; lr < rows_per; lr += kPConsumers / 32) {
+        const int r = (int)rank * rows_per + lr;
+        const int s = map_seq[r];
+        if (s < 0) continue;
+        const int64_t p = map_pos[r];
+        float v[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float a = 0.f;
+            for (int src = 0; src < ks; ++src) a += recv[((int64_t)src * rows_per + lr) * kPN + lane + 32 * q4];
+            v[q4] = a;
+        }
+        const int slot = (int)(p % d.cap);
+        const int64_t base = ((((int64_t)s * d.n_layer + layer) * d.n_head_kv + head) * d.kv_total + slot) * kHeadDim;
+        if (is_v) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) m.v[base + lane + 32 * q4] = __half_as_ushort(__float2half_rn(v[q4]));
+            continue;
+        }
+        // k_norm: RMS over the head, then the per-layer weight
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = rsqrtf(ss / (float)kPN + eps);
+        const float *w = k_norm + (int64_t)layer * kPN;
+        float y[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) y[q4] = v[q4] * inv * w[lane + 32 * q4];
+        // RoPE at p: pairs (i, i + 64) for i = lane and lane + 32
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            const int i = lane + 32 * q2;
+            const float2 cs = rope_angle_cs(p, m.inv_freq[i]);
+            const float x1 = y[q2], x2 = y[q2 + 2];
+            m.k[base + i] = __half_as_ushort(__float2half_rn(fmaf(x1, cs.x, -x2 * cs.y)));
+            m.k[base + i + half] = __half_as_ushort(__float2half_rn(fmaf(x1, cs.y, x2 * cs.x)));
+        }
+        // section 1.2: slot_pos[slot] = p (the begin-step kernel that follows reads it)
+        if (layer == 0 && head == 0 && lane == 0) m.slot_pos[(int64_t)s * d.cap + slot] = (int32_t)p;
+    }
+}
+
+}  // namespace
+
+size_t produce_smem_bytes() { return (size_t)kPSmem; }
+
+cudaError_t produce_kernels_init() {
+    return cudaFuncSetAttribute(k_produce, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
+}
+
+int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms) {
+    const int64_t tiles = (m_total + kPM - 1) / kPM;
+    const int64_t base = tiles * 2 * d.n_head_kv * d.n_layer;
+    const int nkt = hidden / kPK;
+    int ks = 1;
+    while (ks < kPMaxSplit && base * ks * 2 <= 2LL * sms && ks * 2 <= nkt) ks *= 2;
+    return ks;
+}
+
+cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_wk,
+                           const CUtensorMap *tm_wv, const uint16_t *feat, int hidden,
+                           int64_t m_total, int ks, const float *k_norm, float eps,
+                           cudaStream_t st) {
+    const int64_t tiles = (m_total + kPM - 1) / kPM;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * ks), 2 * d.n_head_kv, d.n_layer);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = ks;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, k_produce, *tm_wk, *tm_wv, d, m, feat, hidden, ks, m_total,
+                              k_norm, eps);
+}
+
+}  // namespace dflash

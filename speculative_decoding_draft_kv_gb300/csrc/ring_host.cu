@@ -25,7 +25,7 @@ using namespace dflash;
 namespace {
 
 constexpr int kStagingSlots = 8;
-constexpr int kKinds = 5;
+constexpr int kKinds = 6;
 
 struct EventRec {
     int cls;
@@ -85,6 +85,14 @@ struct dflash_ring {
     GraphKey graph_key;
     int64_t graph_kernels = 0;
     bool last_was_begin = false;   // the ring's last kernel launch was the begin-step kernel
+    // context-row producer (ring_set_producer); caller-owned device weights
+    bool has_producer = false;
+    int hidden = 0;
+    float eps = 0.f;
+    const uint16_t *feat_wk = nullptr, *feat_wv = nullptr;
+    const float *k_norm = nullptr;
+    CUtensorMap tm_wk{}, tm_wv{};
+    int sms = 0;
 };
 
 namespace {
@@ -174,6 +182,20 @@ bool encode_kv_map(CUtensorMap *tm, void *base, const RingDims &d) {
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// 2-D TMA map over F16 weights [rows][hidden]: 64 x 128 boxes, 128-byte swizzle.
+bool encode_weight_map(CUtensorMap *tm, const void *base, int hidden, int64_t rows) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
 }
@@ -311,7 +333,9 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, r->device);
+    r->sms = sms;
     e = attend_kernels_init();
+    if (e == cudaSuccess) e = produce_kernels_init();
     if (e != cudaSuccess) {
         int rc = cuda_fail(nullptr, e, "ring_init: kernel attributes");
         delete r;
@@ -589,6 +613,72 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
         return launch_begin_step(r->d, r->m, kr, vr, n_rows, !r->profiling, cs);
     });
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
+    r->last_was_begin = true;
+    commit_host(r, committed);
+    return RING_OK;
+}
+
+int ring_set_producer(ring_t *r, const ring_producer *p) {
+    if (!r) return RING_EINVAL;
+    if (!p) {
+        r->has_producer = false;
+        return RING_OK;
+    }
+    const RingDims &d = r->d;
+    if (p->hidden <= 0 || p->hidden % 64)
+        return fail(r, RING_EINVAL, "ring_set_producer: hidden %d must be a positive multiple of 64",
+                    p->hidden);
+    if (!p->wk || !p->wv || !p->k_norm)
+        return fail(r, RING_EINVAL, "ring_set_producer: weights are NULL");
+    if ((reinterpret_cast<uintptr_t>(p->wk) | reinterpret_cast<uintptr_t>(p->wv)) & 15)
+        return fail(r, RING_EINVAL, "ring_set_producer: weights must be 16-byte aligned");
+    if (!(p->eps >= 0.f)) return fail(r, RING_EINVAL, "ring_set_producer: eps must be >= 0");
+    const int64_t rows = (int64_t)d.n_layer * d.kv_row;
+    if (!encode_weight_map(&r->tm_wk, p->wk, p->hidden, rows) ||
+        !encode_weight_map(&r->tm_wv, p->wv, p->hidden, rows))
+        return fail(r, RING_ECUDA, "ring_set_producer: cuTensorMapEncodeTiled failed");
+    r->hidden = p->hidden;
+    r->eps = p->eps;
+    r->feat_wk = static_cast<const uint16_t *>(p->wk);
+    r->feat_wv = static_cast<const uint16_t *>(p->wv);
+    r->k_norm = p->k_norm;
+    r->has_producer = true;
+    return RING_OK;
+}
+
+int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *feat,
+                             const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                             void *stream) {
+    if (!r) return RING_EINVAL;
+    if (!r->has_producer)
+        return fail(r, RING_ESTATE, "ring_begin_step_features: no producer set (ring_set_producer)");
+    std::vector<SeqStep> st;
+    int64_t max_bulk = 0;
+    int rc = validate_step(r, "ring_begin_step_features", committed, feat, feat, row_off, first_pos,
+                           n_rows, st, max_bulk);
+    if (rc != RING_OK) return rc;
+    int64_t m_total = 0;
+    for (auto &x : st) {
+        x.prod_base = m_total;
+        m_total += x.n_new;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    rc = stage_and_bulk(r, "ring_begin_step_features", st, nullptr, nullptr, n_rows, 0, cs);
+    if (rc != RING_OK) return rc;
+    cudaError_t e = cudaSuccess;
+    if (m_total > 0) {
+        const int ks = produce_split(m_total, r->d, r->hidden, r->sms);
+        e = timed(r, 5, cs, [&] {
+            return launch_produce(r->d, r->m, &r->tm_wk, &r->tm_wv,
+                                  static_cast<const uint16_t *>(feat), r->hidden, m_total, ks,
+                                  r->k_norm, r->eps, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: producer launch");
+    }
+    e = timed(r, 1, cs, [&] {
+        return launch_begin_step(r->d, r->m, nullptr, nullptr, n_rows, !r->profiling, cs);
+    });
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: launch");
     r->last_was_begin = true;
     commit_host(r, committed);
     return RING_OK;

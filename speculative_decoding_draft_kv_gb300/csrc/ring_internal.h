@@ -48,6 +48,7 @@ struct SeqStep {
     int64_t src_row;     // row (within the caller's k_rows/v_rows) of position `start`
     int32_t n_new;       // rows appended by this step
     int32_t fold_rows;   // n_new on the fold-in path, 0 on the bulk path
+    int64_t prod_base;   // rows of earlier sequences in the producer's packed row list
 };
 
 struct RingDims {
@@ -108,6 +109,20 @@ cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16
 cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
                               cudaStream_t st);
+
+// ---- launchers (produce_kernels.cu) ----
+cudaError_t produce_kernels_init();   // per device, before the first launch
+size_t produce_smem_bytes();
+// split of the hidden dimension over a cluster (1, 2, 4 or 8 CTAs) for m_total rows
+int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms);
+// Context rows of the step's m_total new positions (packed over sequences by
+// SeqStep::prod_base) from F16 features [rows][hidden]: K = RoPE(k_norm(W_k x)), V = W_v x,
+// both rounded to F16 and stored in their ring slots, with slot_pos.  tm_wk / tm_wv: 2-D
+// TMA maps over W [n_layer * kv_row][hidden], 64 x 128 boxes, 128-byte swizzle.
+cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_wk,
+                           const CUtensorMap *tm_wv, const uint16_t *feat, int hidden,
+                           int64_t m_total, int ks, const float *k_norm, float eps,
+                           cudaStream_t st);
 
 // ---- shared host helpers (ring_host.cu) ----
 // 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],

@@ -165,6 +165,7 @@ k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
     const SeqStep st = m.steps[s];
     if (b < d.a_step) {
         if (b < st.fold_rows) {
+            if (!k_rows) return;        // the producer kernel already wrote the row and slot_pos
             const int64_t p = st.start + b;
             rope_table(cs, p, m.inv_freq, d.head_dim / 2);
             __syncthreads();

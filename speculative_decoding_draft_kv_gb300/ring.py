@@ -33,7 +33,7 @@ EXPORTED = (
     "ring_begin_step", "ring_attend", "ring_step", "ring_get_slot_pos", "ring_get_mask",
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
-    "ring_last_error",
+    "ring_last_error", "ring_set_producer", "ring_begin_step_features",
 )
 
 
@@ -72,10 +72,15 @@ class RingAttendStaticArgs(ctypes.Structure):
 
 
 class RingProfile(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_int64 * 5), ("total_ms", ctypes.c_double * 5)]
+    _fields_ = [("launches", ctypes.c_int64 * 6), ("total_ms", ctypes.c_double * 6)]
 
 
-PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "step_graph")
+class RingProducer(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("eps", ctypes.c_float), ("wk", ctypes.c_void_p),
+                ("wv", ctypes.c_void_p), ("k_norm", ctypes.c_void_p)]
+
+
+PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "step_graph", "produce")
 
 _LIB = None
 _N_SEQ = {}      # handle -> n_seq, so per-step calls skip a geometry query
@@ -114,6 +119,8 @@ def _load():
         "ring_launch_count": ([vp], ctypes.c_int64),
         "ring_attend_static": ([ctypes.POINTER(RingAttendStaticArgs), vp], ctypes.c_int),
         "ring_last_error": ([vp], ctypes.c_char_p),
+        "ring_set_producer": ([vp, ctypes.POINTER(RingProducer)], ctypes.c_int),
+        "ring_begin_step_features": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -220,6 +227,34 @@ def ring_begin_step(h, committed, k_rows, v_rows, row_off, first_pos, stream=Non
                                  _dev_ptr(v_rows, torch.float16, "v_rows"), o_ptr, f_ptr,
                                  n_rows, _stream(stream))
     _check(rc, h, "ring_begin_step")
+
+
+def ring_set_producer(h, hidden, eps, wk, wv, k_norm):
+    """wk, wv: CUDA float16 [n_layer, kv_row, hidden]; k_norm: CUDA float32
+    [n_layer, head_dim].  All None detaches the producer.  The caller keeps the tensors
+    alive while steps run."""
+    import torch
+    if wk is None and wv is None and k_norm is None:
+        _check(_load().ring_set_producer(h, None), h, "ring_set_producer")
+        return
+    p = RingProducer(int(hidden), float(eps), _dev_ptr(wk, torch.float16, "wk"),
+                     _dev_ptr(wv, torch.float16, "wv"), _dev_ptr(k_norm, torch.float32, "k_norm"))
+    _check(_load().ring_set_producer(h, ctypes.byref(p)), h, "ring_set_producer")
+
+
+def ring_begin_step_features(h, committed, feat, row_off, first_pos, stream=None):
+    """``feat``: CUDA float16 [n_rows, hidden] or None (no sequence appends)."""
+    import torch
+    n_seq = _N_SEQ.get(getattr(h, "value", h)) or ring_get_geometry(h)["n_seq"]
+    c_arr, c_ptr = _i64_array(committed, n_seq, "committed")
+    o_arr, o_ptr = _i64_array(row_off, n_seq, "row_off")
+    f_arr, f_ptr = _i64_array(first_pos, n_seq, "first_pos")
+    n_rows = 0 if feat is None else int(feat.shape[0])
+    if feat is not None and feat.dim() != 2:
+        raise ValueError("feat must be [n_rows, hidden]")
+    rc = _load().ring_begin_step_features(h, c_ptr, _dev_ptr(feat, torch.float16, "feat"), o_ptr,
+                                          f_ptr, n_rows, _stream(stream))
+    _check(rc, h, "ring_begin_step_features")
 
 
 def ring_attend(h, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
@@ -359,6 +394,13 @@ class Ring:
 
     def begin_step(self, committed, k_rows, v_rows, row_off, first_pos, stream=None):
         ring_begin_step(self.h, committed, k_rows, v_rows, row_off, first_pos, stream)
+
+    def set_producer(self, hidden, eps, wk, wv, k_norm):
+        self._producer = (wk, wv, k_norm)          # keep the weights alive
+        ring_set_producer(self.h, hidden, eps, wk, wv, k_norm)
+
+    def begin_step_features(self, committed, feat, row_off, first_pos, stream=None):
+        ring_begin_step_features(self.h, committed, feat, row_off, first_pos, stream)
 
     def attend(self, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
         ring_attend(self.h, layer, mask_kind, q, k_noise, v_noise, o, stream)

@@ -50,6 +50,32 @@ def k_within_tolerance(got, want):
     return ok, int((d > 0).sum())
 
 
+def f16_spacing(x) -> np.ndarray:
+    """Distance between adjacent binary16 values at magnitude |x| (subnormal spacing below
+    2^-14)."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
+def projection_error_bound(feat, w) -> np.ndarray:
+    """Bound on |(X W^T) accumulated in float32 - exact|, elementwise.  Each F16 x F16
+    product is exact in float32; each of the at most `hidden` additions is off by at most
+    one float32 unit (2^-23 relative, so truncating adders are covered) of a partial sum
+    no larger than sum |x w|."""
+    feat = np.asarray(feat, np.float64)
+    w = np.asarray(w, np.float64)
+    return feat.shape[-1] * 2.0 ** -23 * (np.abs(feat) @ np.abs(w).T)
+
+
+def f16_within(got, want_exact, bound) -> bool:
+    """F16 values `got` against exact values: |got - exact| <= bound + spacing, i.e. the
+    F16 rounding of a value within `bound` of the exact one."""
+    got = np.asarray(got, np.float64)
+    want_exact = np.asarray(want_exact, np.float64)
+    return bool(np.all(np.abs(got - want_exact) <= bound + f16_spacing(np.abs(want_exact) + bound)))
+
+
 class RowSource:
     """Pre-RoPE context rows by absolute position, drawn on the CPU and cached per
     (seq, layer) as one contiguous window that slides with the requests."""

@@ -1,0 +1,253 @@
+"""Parity of the context-row producer (ring_begin_step_features) with the float64 oracle.
+
+The CUDA path projects seeded fused features with seeded weights on the tensor cores,
+normalises K per head, turns it by RoPE and writes both rows into the ring; the oracle
+does the same in float64 (readings P1-P3 of oracle/ring_oracle.py) and is fed the same
+features and weights, drawn on the CPU by the same counter-based generator.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ring_oracle as orc
+from speculative_decoding_draft_kv_gb300 import ring as R
+from tests.ring_harness import (assert_close, expected_tile_flags, f16_within,
+                                projection_error_bound)
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+class ProducerRun:
+    """A CUDA ring fed by the producer, plus per-sequence bookkeeping oracles."""
+
+    def __init__(self, w, hidden, swa_window=None, tiles_per_split=0):
+        self.w, self.hidden = w, hidden
+        self.swa = w.swa_window if swa_window is None else swa_window
+        self.dev = torch.device("cuda")
+        self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
+                           w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
+                           tiles_per_split=tiles_per_split)
+        self.g = self.ring.geometry
+        cpu = [synth.producer_weights(w.seed, l, w.kv_row, hidden, w.head_dim)
+               for l in range(w.n_layer)]
+        self.wk = [x[0].numpy() for x in cpu]
+        self.wv = [x[1].numpy() for x in cpu]
+        self.kn = [x[2].numpy() for x in cpu]
+        gpu = [synth.producer_weights(w.seed, l, w.kv_row, hidden, w.head_dim, device=self.dev)
+               for l in range(w.n_layer)]
+        self.gwk = torch.stack([x[0] for x in gpu]).contiguous()
+        self.gwv = torch.stack([x[1] for x in gpu]).contiguous()
+        self.gkn = torch.stack([x[2] for x in gpu]).contiguous()
+        self.ring.set_producer(hidden, EPS, self.gwk, self.gwv, self.gkn)
+        self.book = [orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta,
+                                    swa_window=self.swa) for _ in range(w.n_seq)]
+        self.committed = np.zeros(w.n_seq, np.int64)
+        self._keep = None
+
+    def close(self):
+        self.ring.close()
+
+    def feat(self, seq, pos):
+        return synth.feature_rows(self.w.seed, seq, torch.as_tensor(np.asarray(pos, np.int64)),
+                                  self.hidden, self.w.sigma).numpy()
+
+    def rows(self, seq, layer, pos):
+        """Oracle rows (pre-RoPE K float64, V F16) of positions ``pos``."""
+        return orc.produce_rows(self.feat(seq, pos), self.wk[layer], self.wv[layer],
+                                self.kn[layer], EPS, self.w.n_head_kv, self.w.head_dim)
+
+    def begin_step(self, committed):
+        w = self.w
+        committed = np.asarray(committed, np.int64)
+        starts, counts = [], []
+        for s in range(w.n_seq):
+            st, nn = self.book[s].rows_needed(int(committed[s]))
+            starts.append(st)
+            counts.append(nn)
+        n_rows = int(sum(counts))
+        row_off = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
+        feat = None
+        if n_rows:
+            feat = torch.empty((n_rows, self.hidden), dtype=torch.float16, device=self.dev)
+            for s in range(w.n_seq):
+                if counts[s]:
+                    a = int(row_off[s])
+                    feat[a:a + counts[s]] = synth.feature_rows(
+                        w.seed, s, torch.arange(starts[s], committed[s], device=self.dev),
+                        self.hidden, w.sigma, device=self.dev)
+        self.ring.begin_step_features(committed, feat, row_off, np.asarray(starts, np.int64))
+        self._keep = feat
+        paths = []
+        for s in range(w.n_seq):
+            z = np.zeros((1, counts[s], 2), np.float16)
+            paths.append(self.book[s].begin_step(int(committed[s]), z, z, starts[s]))
+        self.committed = committed.copy()
+        return paths
+
+    def check_state(self, seqs=None):
+        for s in (range(self.w.n_seq) if seqs is None else seqs):
+            b = self.book[s]
+            np.testing.assert_array_equal(self.ring.slot_pos(s), b.slot_pos.astype(np.int32))
+            for kind in ["full"] + (["swa"] if self.swa else []):
+                want = b.mask(kind)
+                assert self.ring.mask(s, kind).view(np.uint32).tobytes() == \
+                    want.view(np.uint32).tobytes(), (s, kind)
+                np.testing.assert_array_equal(self.ring.tile_flags(s, kind),
+                                              expected_tile_flags(want, self.g["tile_slots"]))
+
+    def check_kv(self, seq, layer, slots=None):
+        """K and V of (sampled) filled slots against the oracle's produced rows."""
+        k, v = self.ring.kv(seq, layer)
+        sp = self.book[seq].slot_pos
+        slots = np.flatnonzero(sp >= 0) if slots is None else np.asarray(
+            [s for s in slots if sp[s] >= 0], np.int64)
+        if not len(slots):
+            return
+        pos = sp[slots]
+        w, hd, nh = self.w, self.w.head_dim, self.w.n_head_kv
+        x = self.feat(seq, pos)
+        v_exact = x @ self.wv[layer].astype(np.float64).T
+        k_pre = x @ self.wk[layer].astype(np.float64).T
+        # V: the F16 rounding of a float32 accumulation of exact products
+        assert f16_within(v[slots], v_exact, projection_error_bound(x, self.wv[layer])), layer
+        # K: the accumulation error carried through the per-head norm and the rotation:
+        # e = |dk| / rms + |k| |drms| / rms^2 per element with |drms| <= max |dk| of the
+        # head, times max |w|, and a rotation adds two such errors; the float32 norm and
+        # RoPE (cos/sin within 2 float32 units, products and FMAs rounded once each) add
+        # at most 5e-7 (|y1| + |y2|) <= 1.2e-6 max |y| of the head.
+        dk = projection_error_bound(x, self.wk[layer]).reshape(len(pos), nh, hd)
+        kh = k_pre.reshape(len(pos), nh, hd)
+        rms = np.sqrt(np.mean(kh * kh, axis=-1, keepdims=True) + EPS)
+        e = (dk + np.abs(kh) * dk.max(axis=-1, keepdims=True) / rms) / rms
+        y = orc.rms_norm_heads(k_pre, self.kn[layer], EPS, nh, hd)
+        ymax = np.abs(y.reshape(len(pos), nh, hd)).max(axis=-1, keepdims=True)
+        e = 2.0 * e.max(axis=-1, keepdims=True) * np.abs(self.kn[layer]).max() + 1.2e-6 * ymax + 1e-7
+        k_exact = orc.rope_rows(y, pos, nh, hd, w.rope_theta)
+        bound = np.broadcast_to(e, kh.shape).reshape(len(pos), nh * hd)
+        assert f16_within(k[slots], k_exact, bound), layer
+        t = self.g["trash_slot"]
+        assert np.all(k[t] == 0) and np.all(v[t] == 0)
+
+    def attend(self, step, layer, kind):
+        w = self.w
+        qs, ks, vs = [], [], []
+        for s in range(w.n_seq):
+            qs.append(synth.query_block(w.seed, step, s, layer, w.q_len, w.n_head, w.head_dim,
+                                        w.sigma, device=self.dev))
+            kk, vv = synth.noise_rows(w.seed, step, s, layer, w.q_len, w.kv_row, w.sigma,
+                                      device=self.dev)
+            ks.append(kk)
+            vs.append(vv)
+        q, kn, vn = torch.stack(qs), torch.stack(ks), torch.stack(vs)
+        o = torch.empty_like(q)
+        self.ring.attend(layer, kind, q, kn, vn, o)
+        torch.cuda.synchronize()
+        return o.cpu().numpy()
+
+    def expected(self, step, layer, kind, seq, heads=None):
+        w = self.w
+        q = synth.query_block(w.seed, step, seq, layer, w.q_len, w.n_head, w.head_dim, w.sigma)
+        kn, vn = synth.noise_rows(w.seed, step, seq, layer, w.q_len, w.kv_row, w.sigma)
+        return orc.attend_dense(int(self.committed[seq]), w.cap,
+                                lambda pos: self.rows(seq, layer, pos), q.numpy(), kn.numpy(),
+                                vn.numpy(), w.head_dim, w.n_head_kv, w.n_head, w.rope_theta,
+                                kind=kind, swa_window=self.swa, heads=heads)
+
+
+def test_feature_and_weight_generators_bit_identical_on_gpu():
+    dev = torch.device("cuda")
+    a = synth.feature_rows(3, 1, torch.arange(100, 140), 512, 0.5)
+    b = synth.feature_rows(3, 1, torch.arange(100, 140, device=dev), 512, 0.5, device=dev)
+    assert torch.equal(a, b.cpu())
+    for x, y in zip(synth.producer_weights(3, 2, 256, 512, 128),
+                    synth.producer_weights(3, 2, 256, 512, 128, device=dev)):
+        assert torch.equal(x, y.cpu())
+
+
+@pytest.mark.parametrize("hidden", [256, 320])
+def test_small_rings_full_state(hidden):
+    """Two sequences, fold-in and bulk steps (and a jump past the ring), every slot of
+    every layer checked, both masks, attention against the dense window of produced rows.
+    hidden 320 splits unevenly over the cluster (5 stages of 64)."""
+    w = synth.workload(1, n_layer=2, n_seq=2, swa_window=24)
+    run = ProducerRun(w, hidden)
+    try:
+        sched = [[5, 0], [12, 9], [40, 30], [41, 200], [60, 207], [140, 215], [149, 216]]
+        for t, c in enumerate(sched):
+            run.begin_step(c)
+            run.check_state()
+            for s in range(w.n_seq):
+                for layer in range(w.n_layer):
+                    run.check_kv(s, layer)
+            for kind in ("full", "swa"):
+                layer = t % 2
+                o = run.attend(t, layer, kind)
+                for s in range(w.n_seq):
+                    assert_close(o[s], run.expected(t, layer, kind, s), f"step {t} seq {s} {kind}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_steady_decode_full_size():
+    """cap 4096, 5 layers, hidden 4096: an 8192-row prefill (bulk) then decode steps of
+    the acceptance histogram; sampled slots of every layer and sampled heads of the
+    attention output."""
+    w = synth.workload(2)
+    run = ProducerRun(w, 4096)
+    rng = np.random.default_rng(1)
+    try:
+        sched = synth.commit_schedule(w, 4)
+        for t, c in enumerate(sched):
+            run.begin_step(c)
+            run.check_state()
+            lo = int(c[0]) - min(int(c[0]), w.cap)
+            recent = [int(p) % w.cap for p in range(max(lo, int(c[0]) - 9), int(c[0]))]
+            slots = sorted(set(rng.integers(0, w.cap, 24).tolist() + recent))
+            for layer in (0, 4):
+                run.check_kv(0, layer, slots)
+            heads = [0, 13, 31]
+            layer = t % w.n_layer
+            o = run.attend(t, layer, "full")
+            want = run.expected(t, layer, "full", 0, heads=heads)
+            assert_close(o[0][:, heads], want[:, heads], f"step {t}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_producer_errors_and_state_unchanged():
+    w = synth.workload(1, n_layer=2)
+    ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta)
+    dev = torch.device("cuda")
+    try:
+        feat = torch.zeros((4, 256), dtype=torch.float16, device=dev)
+        with pytest.raises(R.RingError) as e:               # no producer yet
+            ring.begin_step_features([4], feat, [0], [0])
+        assert e.value.code == R.RING_ESTATE
+        wk = torch.zeros((2, w.kv_row, 256), dtype=torch.float16, device=dev)
+        kn = torch.ones((2, w.head_dim), dtype=torch.float32, device=dev)
+        with pytest.raises(R.RingError) as e:               # hidden not a multiple of 64
+            ring.set_producer(200, EPS, wk, wk, kn)
+        assert e.value.code == R.RING_EINVAL
+        ring.set_producer(256, EPS, wk, wk, kn)
+        with pytest.raises(R.RingError) as e:               # rows do not cover [start, c)
+            ring.begin_step_features([10], feat, [0], [0])
+        assert e.value.code == R.RING_ERANGE
+        np.testing.assert_array_equal(ring.slot_pos(), np.full(w.cap, -1, np.int32))
+        ring.begin_step_features([4], feat, [0], [0])      # zero weights: K and V rows of 0
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(ring.slot_pos()[:4], [0, 1, 2, 3])
+        k, v = ring.kv(0, 1)
+        assert np.all(k[:4] == 0) and np.all(v[:4] == 0)
+        assert ring.device_error() == 0
+        ring.set_producer(None, 0.0, None, None, None)      # detached again
+        with pytest.raises(R.RingError) as e:
+            ring.begin_step_features([8], feat, [0], [4])
+        assert e.value.code == R.RING_ESTATE
+    finally:
+        ring.close()
