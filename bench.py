@@ -396,6 +396,79 @@ def run_gb300(args):
                    "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                    "steps": n4, "api": "ring_step"}
 
+    # ---- pass 5: the step with the context rows made by the producer from fused
+    # features (ring_begin_step_features + ring_attend per layer), and the producer
+    # kernel's own roofline ----
+    prod_obj = None
+    n_feat_rows = int(sum(int(P.plan[t][3].sum()) for t in range(len(P.plan))))
+    if args.producer_hidden > 0 and n_feat_rows * args.producer_hidden * 2 <= (1 << 30):
+        H = args.producer_hidden
+        ws = [synth.producer_weights(w.seed, l, w.kv_row, H, w.head_dim, device=dev)
+              for l in range(w.n_layer)]
+        wk = torch.stack([x[0] for x in ws]).contiguous()
+        wv = torch.stack([x[1] for x in ws]).contiguous()
+        kn = torch.stack([x[2] for x in ws]).contiguous()
+        del ws
+        feat_all = torch.empty((max(n_feat_rows, 1), H), dtype=torch.float16, device=dev)
+        seq_ids = shard_sequences(rank, world, w.n_seq)
+        for c, row_off, start, counts in P.plan:
+            for s_ in range(w.n_seq):
+                if counts[s_]:
+                    a = int(row_off[s_])
+                    feat_all[a:a + int(counts[s_])] = synth.feature_rows(
+                        w.seed, seq_ids[s_], torch.arange(int(start[s_]), int(c[s_]), device=dev),
+                        H, w.sigma, device=dev)
+
+        def prod_ring():
+            r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
+                       n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
+                       max_cluster=args.max_cluster)
+            r.set_producer(H, 1e-6, wk, wv, kn)
+            c, row_off, start, _ = P.plan[0]
+            r.begin_step_features(c, feat_all, row_off, start, stream)
+            torch.cuda.synchronize()
+            return r
+
+        def step_prod(r, t):
+            c, row_off, start, _ = P.plan[t]
+            r.begin_step_features(c, feat_all, row_off, start, stream)
+            for layer in range(w.n_layer):
+                r.attend(layer, kind, P.q[layer], P.kn[layer], P.vn[layer], P.o[layer], stream)
+
+        n5 = min(K + W, 400)
+        ring = prod_ring()
+        timed_loop(ring, step_prod, 1, min(W, n5))
+        torch.cuda.synchronize()
+        evs = timed_loop(ring, step_prod, 1 + min(W, n5), n5 - min(W, n5))
+        torch.cuda.synchronize()
+        ms_prod = max_over_ranks(ms_of(evs), dist, dev) / max(1, n5 - min(W, n5))
+        assert ring.device_error() == 0
+        ring.close()
+        ring = prod_ring()
+        R.ring_profile_enable(ring.h, True)
+        timed_loop(ring, step_prod, 1, n5)
+        torch.cuda.synchronize()
+        pp = R.ring_profile_read(ring.h)
+        ring.close()
+        pr = pp["produce"]
+        prod_ms = pr["total_ms"] / max(pr["launches"], 1)
+        rows = float(np.mean([int(P.plan[1 + j][3].sum()) for j in range(n5)
+                              if int(P.plan[1 + j][3].sum()) > 0] or [0]))
+        prod_bytes = (2 * w.n_layer * w.kv_row * H * 2 + rows * H * 2
+                      + rows * w.n_layer * 2 * w.kv_row * 2)
+        prod_ach = prod_bytes / (prod_ms * 1e-3) / 1e9
+        prod_obj = {
+            "value": 1000.0 / ms_prod * world, "unit": UNIT, "ms_per_step": ms_prod,
+            "steps": n5 - min(W, n5), "hidden": H,
+            "api": "ring_begin_step_features + ring_attend per layer",
+            "roofline": {"bound": "hbm", "achieved": prod_ach, "peak": peak, "unit": "GB/s",
+                         "frac": prod_ach / peak, "traffic": None, "kernel": "k_produce",
+                         "alg_bytes_per_launch": prod_bytes, "launch_ms": prod_ms,
+                         "rows_per_launch": rows,
+                         "unit_bytes": "W_k and W_v of every layer + feature rows + K/V rows written"},
+        }
+        del feat_all, wk, wv, kn
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, kind, budget_s=args.cpu_seconds)
@@ -414,7 +487,8 @@ def run_gb300(args):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "f16",
-            "data": "synthetic (seeded counter-based generator; no weights involved)",
+            "data": "synthetic (seeded counter-based generator; the with_producer pass uses "
+                    "seeded random-init projection weights)",
             "config": {
                 "workload": w.name, "cap": w.cap, "q_len": w.q_len, "n_seq": w.n_seq,
                 "n_layer": w.n_layer, "head_dim": w.head_dim, "n_head_kv": w.n_head_kv,
@@ -429,6 +503,7 @@ def run_gb300(args):
             "gpu_launches": int(launches),
             "separate_calls": {"value": 1000.0 / ms_calls * world, "ms_per_step": ms_calls,
                                "api": "ring_begin_step + ring_attend per layer"},
+            "with_producer": prod_obj,
             "step_kv_gbs": vis_step / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -558,6 +633,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--producer-hidden", type=int, default=4096,
+                    help="width of the fused features for the producer pass (0: skip it)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

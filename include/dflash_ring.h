@@ -169,8 +169,11 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows,
  *   wk, wv   device F16 [n_layer][kv_row][hidden], row-major, 16-byte aligned.
  *   k_norm   device F32 [n_layer][head_dim].
  *
- * The ring keeps the pointers (the caller owns the memory and keeps it alive and unchanged
- * while steps run); p == NULL detaches the producer.  Errors: EINVAL, ECUDA.
+ * Synchronous: the weights are copied into ring-owned device memory (W_k and W_v
+ * repacked into contiguous 128 x 64 tiles, 2 * n_layer * kv_row * hidden F16 in all; k_norm
+ * as is), so the caller's buffers may be freed or changed afterwards -- call again after
+ * changing them.  Waits for the device to go idle before replacing earlier weights.
+ * p == NULL detaches the producer and frees the copy.  Errors: EINVAL, ENOMEM, ECUDA.
  */
 typedef struct ring_producer {
     int32_t hidden;

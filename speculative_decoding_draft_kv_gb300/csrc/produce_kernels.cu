@@ -9,9 +9,14 @@
 //
 // Shape: a CTA owns 32 feature rows (the step's new positions, packed across sequences)
 // and one 128-wide head of K or of V of one layer.  C = X W^T runs on the F16 tensor cores
-// (m16n8k16, F32 accumulation): W tiles (128 x 64) arrive by TMA, the gathered feature
-// rows (32 x 64) by 16-byte cp.async, both into a 4-stage shared-memory ring guarded by
-// mbarriers.  With few rows the kernel streams weights, so the hidden dimension is split
+// (m16n8k16, F32 accumulation).  The weights are repacked once (ring_set_producer) into
+// contiguous 16 KiB tiles of 128 output rows x 64 hidden columns, so every W tile is one
+// contiguous TMA box -- a row-major W read as 128-row x 128-byte boxes scatters each box
+// over 128 DRAM rows and streamed at well under half of the HBM bandwidth.  W tiles
+// arrive by TMA; the tile's feature rows
+// (32 x 64) by one TMA box when they are consecutive rows of the caller's buffer (one
+// sequence), else by one 128-byte bulk copy per row; both into a 4-stage shared-memory
+// ring guarded by mbarriers.  With few rows the kernel streams weights, so the hidden dimension is split
 // over a thread-block cluster of `ks` CTAs whose partial tiles are summed in the shared
 // memory of the CTA that owns each row (distributed shared memory stores).  The owner then
 // normalises, turns and stores its rows: one warp per row, lane l holding columns
@@ -19,6 +24,8 @@
 #include "ring_internal.h"
 
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 namespace dflash {
 namespace {
@@ -28,8 +35,10 @@ constexpr int kPN = 128;                   // output columns per CTA: one head o
 constexpr int kPK = 64;                    // hidden columns per stage
 constexpr int kPStages = 4;
 constexpr int kPBBytes = kPN * kPK * 2;    // W tile, 16 KiB (TMA box 64 x 128, 128B swizzle)
-constexpr int kPABytes = kPM * kPK * 2;    // feature tile, 4 KiB (same swizzle, by hand)
-constexpr int kPStage = kPBBytes + kPABytes;
+constexpr int kPAPitch = kPK * 2 + 16;     // feature row pitch: 16 bytes of padding keep
+                                           // the row fragments of ldmatrix conflict-free
+constexpr int kPABytes = kPM * kPAPitch;   // feature tile
+constexpr int kPStage = (kPBBytes + kPABytes + 1023) / 1024 * 1024;   // W tiles 1024-aligned
 constexpr int kPConsumers = 128;           // 4 warps, warp w -> columns [32 w, 32 w + 32)
 constexpr int kPThreads = kPConsumers + 32;
 constexpr int kPMaxSplit = 8;
@@ -75,6 +84,19 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// raise the phase's expected transaction bytes without arriving
+__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
                                             uint32_t bar) {
     asm volatile(
@@ -83,16 +105,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-// 16 bytes global -> shared; src_bytes 0 fills the destination with zeros
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-// arrive on `bar` once this thread's earlier cp.async copies have landed (the barrier's
-// expected count includes this arrival)
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+// bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
@@ -143,9 +162,10 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
 // Grid (ks * m_tiles, 2 * n_head_kv, n_layer); clusters of ks CTAs along x when ks > 1.
 // blockIdx.y < n_head_kv: K head y; else V head y - n_head_kv.
 __global__ void __launch_bounds__(kPThreads, 2)
-k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
+k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_feat,
           RingDims d, RingDev m, const uint16_t *__restrict__ feat, int hidden, int ks,
-          int64_t m_total, const float *__restrict__ k_norm, float eps) {
+          int64_t m_total, const float *__restrict__ k_norm, float eps,
+          const __grid_constant__ ProduceSeqs seqs, int pdl) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,7 +174,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
     int64_t *map_pos = reinterpret_cast<int64_t *>(smem + kPOffMap);
     int64_t *map_frow = map_pos + kPM;                    // -1: padding row
     __shared__ int map_seq[kPM];
-    __shared__ int s_fail;
+    __shared__ int s_fail, s_valid, s_contig;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ks > 1 ? cluster_rank() : 0u;
@@ -167,22 +187,40 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
     const int kt0 = min(nkt, (int)rank * per), kt1 = min(nkt, kt0 + per);
     const int rows_per = kPM / ks;
 
-    if (threadIdx.x == 0) {
+    // packed W tile (layer, K head y or V head y - n_head_kv, k-tile kt) is plane
+    // wplane + kt of the packed weights
+    const int wplane = (layer * 2 * d.n_head_kv + yk) * nkt;
+    const int n_pre = min(kPStages, kt1 - kt0);
+    if (threadIdx.x == kPConsumers) {
         for (int k = 0; k < kPStages; ++k) {
-            mbar_init(bar0 + 8 * k, 1 + 32);     // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(bar0 + 8 * k, 1);          // the producer's expect_tx arrival
             mbar_init(bar0 + 8 * (kPStages + k), kPConsumers / 32);
         }
         s_fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the first weight tiles depend on nothing earlier in the stream: start them now
+        // (expected bytes only: the stage's arrival comes with its feature rows)
+        for (int k = 0; k < n_pre; ++k) {
+            mbar_add_tx(bar0 + 8 * k, kPBBytes);
+            tma_load_3d(smem_u32(smem + k * kPStage), &tm_w, 0, 0, wplane + kt0 + k, bar0 + 8 * k);
+        }
     }
+    if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (warp == 0) {
         // row map: packed row index -> (sequence, position, feature row).  Sequence s owns
         // rows [prod_base, prod_base + n_new) of the packed list.
         const int64_t mr = tile * kPM + lane;
         int sq = -1;
         int64_t pos = 0, frow = -1;
-        if (mr < m_total) {
+        if (mr < m_total && seqs.n > 0) {
+            for (int s = 0; s < seqs.n; ++s)
+                if (mr >= seqs.base[s] && mr < seqs.base[s] + seqs.n_new[s]) {
+                    sq = s;
+                    pos = seqs.start[s] + (mr - seqs.base[s]);
+                    frow = seqs.src_row[s] + (mr - seqs.base[s]);
+                }
+        } else if (mr < m_total) {
             int lo = 0, hi = d.n_seq - 1;
             while (lo < hi) {                       // last s with prod_base <= mr
                 const int mid = (lo + hi + 1) >> 1;
@@ -200,14 +238,19 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
         map_seq[lane] = sq;
         map_pos[lane] = pos;
         map_frow[lane] = frow;
+        const int nv = __popc(__ballot_sync(0xffffffffu, frow >= 0));
+        const int64_t f0 = __shfl_sync(0xffffffffu, frow, 0);
+        const bool seq_rows = __all_sync(0xffffffffu, frow < 0 || frow == f0 + lane);
+        if (lane == 0) {
+            s_valid = nv;
+            s_contig = seq_rows ? 1 : 0;
+        }
     }
     __syncthreads();
     if (ks > 1) cluster_arrive_relaxed();
 
     if (warp == kPConsumers / 32) {
         // ---------------- producer warp ----------------
-        const CUtensorMap *tm = is_v ? &tm_wv : &tm_wk;
-        const int wrow = layer * d.kv_row + head * kPN;
         int it = 0;
         for (int kt = kt0; kt < kt1; ++kt, ++it) {
             const int stg = it % kPStages;
@@ -222,21 +265,29 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
             const uint32_t sb = smem_u32(smem + stg * kPStage);
             const uint32_t sa = sb + kPBBytes;
             const uint32_t full = bar0 + 8 * stg;
+            const bool contig = s_contig != 0;
             if (lane == 0) {
-                mbar_expect_tx(full, kPBBytes);
-                tma_load_2d(sb, tm, kt * kPK, wrow, full);
+                // one arrival for the stage, expecting the W tile (unless it went out at
+                // start-up) and the feature rows: one box of 32 rows, or one 128-byte copy
+                // per valid row
+                const uint32_t a_bytes = contig ? (uint32_t)kPM * kPK * 2 : (uint32_t)s_valid * kPK * 2;
+                mbar_expect_tx(full, (it >= n_pre ? kPBBytes : 0) + a_bytes);
+                if (it >= n_pre) tma_load_3d(sb, &tm_w, 0, 0, wplane + kt, full);
+                if (contig) tma_load_2d(sa, &tm_feat, kt * kPK, (int)map_frow[0], full);
             }
-#pragma unroll
-            for (int j = 0; j < (kPM * kPK / 8) / 32; ++j) {
-                const int u = j * 32 + lane;
-                const int r = u >> 3, c = u & 7;
-                const int64_t fr = map_frow[r];
-                const uint16_t *src = fr >= 0 ? feat + fr * hidden + kt * kPK + c * 8 : feat;
-                cp_async16(sa + swz64(r, c * 8), src, fr >= 0 ? 16u : 0u);
-            }
-            cp_async_arrive(full);
+            __syncwarp();
+            const int64_t fr = map_frow[lane];      // row `lane` of the tile
+            if (!contig && fr >= 0)
+                bulk_g2s(sa + lane * kPAPitch, feat + fr * hidden + kt * kPK, kPK * 2, full);
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
+        // no copy may land after the CTA exits: wait (bounded) for the last stages' bytes
+        if (lane == 0)
+            for (int k = max(0, it - kPStages); k < it; ++k)
+                if (!mbar_wait(bar0 + 8 * (k % kPStages), (uint32_t)(k / kPStages) & 1u)) {
+                    atomicOr(m.err, kErrDrain);
+                    break;
+                }
+        __syncwarp();
         if (ks > 1) cluster_wait();
     } else {
         // ---------------- consumer warps: C[32][32 w .. 32 w + 32) ----------------
@@ -245,6 +296,8 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
         for (int a = 0; a < 2; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) acc[a][b][0] = acc[a][b][1] = acc[a][b][2] = acc[a][b][3] = 0.f;
+        const bool two_blocks = m_total - tile * kPM > 16;
+        const bool contig = s_contig != 0;        // feature tile swizzled (TMA) or padded
         int it = 0;
         for (int kt = kt0; kt < kt1; ++kt, ++it) {
             const int stg = it % kPStages;
@@ -258,25 +311,33 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
             }
             const uint32_t sb = smem_u32(smem + stg * kPStage);
             const uint32_t sa = sb + kPBBytes;
+            // MT row blocks of 16: the second only when the tile has more than 16 rows
+            auto mma_stage = [&](auto mtc) {
+                constexpr int MT = decltype(mtc)::value;
 #pragma unroll
-            for (int ks16 = 0; ks16 < kPK / 16; ++ks16) {
-                uint32_t af[2][4];
+                for (int ks16 = 0; ks16 < kPK / 16; ++ks16) {
+                    uint32_t af[MT][4];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
-                    ldsm_x4(sa + swz64(mt * 16 + (lane & 15), ks16 * 16 + ((lane >> 4) << 3)),
-                            af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
+                    for (int mt = 0; mt < MT; ++mt)
+                        ldsm_x4(sa + (contig ? swz64(mt * 16 + (lane & 15), ks16 * 16 + ((lane >> 4) << 3))
+                                             : (uint32_t)((mt * 16 + (lane & 15)) * kPAPitch +
+                                                          (ks16 * 16 + ((lane >> 4) << 3)) * 2)),
+                                af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    const int n = warp * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sb + swz64(n, ks16 * 16 + (((lane >> 3) & 1) << 3)), b0, b1, b2, b3);
+                    for (int np = 0; np < 2; ++np) {
+                        const int n = warp * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(sb + swz64(n, ks16 * 16 + (((lane >> 3) & 1) << 3)), b0, b1, b2, b3);
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        mma16816(acc[mt][np * 2], af[mt], b0, b1);
-                        mma16816(acc[mt][np * 2 + 1], af[mt], b2, b3);
+                        for (int mt = 0; mt < MT; ++mt) {
+                            mma16816(acc[mt][np * 2], af[mt], b0, b1);
+                            mma16816(acc[mt][np * 2 + 1], af[mt], b2, b3);
+                        }
                     }
                 }
-            }
+            };
+            if (two_blocks) mma_stage(std::integral_constant<int, 2>{});
+            else mma_stage(std::integral_constant<int, 1>{});
             __syncwarp();
             if (lane == 0) mbar_arrive(bar0 + 8 * (kPStages + stg));
         }
@@ -354,7 +415,38 @@ k_produce(const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUt
 
 }  // namespace
 
+// Repack W_k and W_v [n_layer][kv_row][hidden] into tiles: tile ((layer * 2 * n_head_kv +
+// y) * nkt + kt), y = K head or n_head_kv + V head, holds rows head*128 .. +128 of that
+// weight, columns kt*64 .. +64, row-major (128 x 64 F16 = 16 KiB).  16 bytes per item.
+__global__ void k_pack_weights(const uint16_t *__restrict__ wk, const uint16_t *__restrict__ wv,
+                               uint16_t *__restrict__ out, int n_layer, int n_head_kv, int hidden) {
+    const int nkt = hidden / kPK;
+    const int64_t total = (int64_t)n_layer * 2 * n_head_kv * nkt * kPN * (kPK / 8);
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(u % (kPK / 8));
+        int64_t t = u / (kPK / 8);
+        const int row = (int)(t % kPN);
+        t /= kPN;
+        const int kt = (int)(t % nkt);
+        t /= nkt;
+        const int yk = (int)(t % (2 * n_head_kv));
+        const int layer = (int)(t / (2 * n_head_kv));
+        const bool is_v = yk >= n_head_kv;
+        const int head = is_v ? yk - n_head_kv : yk;
+        const uint16_t *src = (is_v ? wv : wk) +
+                              ((int64_t)layer * n_head_kv * kPN + head * kPN + row) * hidden + kt * kPK + c8 * 8;
+        *reinterpret_cast<uint4 *>(out + u * 8) = *reinterpret_cast<const uint4 *>(src);
+    }
+}
+
 size_t produce_smem_bytes() { return (size_t)kPSmem; }
+
+cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, uint16_t *out,
+                                int n_layer, int n_head_kv, int hidden, cudaStream_t st) {
+    k_pack_weights<<<1024, 256, 0, st>>>(wk, wv, out, n_layer, n_head_kv, hidden);
+    return cudaGetLastError();
+}
 
 cudaError_t produce_kernels_init() {
     return cudaFuncSetAttribute(k_produce, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
@@ -369,17 +461,17 @@ int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms) {
     return ks;
 }
 
-cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_wk,
-                           const CUtensorMap *tm_wv, const uint16_t *feat, int hidden,
+cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
+                           const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
                            int64_t m_total, int ks, const float *k_norm, float eps,
-                           cudaStream_t st) {
+                           const ProduceSeqs &seqs, bool pdl, cudaStream_t st) {
     const int64_t tiles = (m_total + kPM - 1) / kPM;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * ks), 2 * d.n_head_kv, d.n_layer);
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = kPSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
     if (ks > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -388,10 +480,15 @@ cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMa
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, k_produce, *tm_wk, *tm_wv, d, m, feat, hidden, ks, m_total,
-                              k_norm, eps);
+    return cudaLaunchKernelEx(&cfg, k_produce, *tm_w, *tm_feat, d, m, feat, hidden, ks, m_total,
+                              k_norm, eps, seqs, pdl ? 1 : 0);
 }
 
 }  // namespace dflash

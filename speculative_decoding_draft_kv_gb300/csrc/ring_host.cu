@@ -85,13 +85,13 @@ struct dflash_ring {
     GraphKey graph_key;
     int64_t graph_kernels = 0;
     bool last_was_begin = false;   // the ring's last kernel launch was the begin-step kernel
-    // context-row producer (ring_set_producer); caller-owned device weights
+    // context-row producer (ring_set_producer): weights repacked into ring-owned tiles
     bool has_producer = false;
     int hidden = 0;
     float eps = 0.f;
-    const uint16_t *feat_wk = nullptr, *feat_wv = nullptr;
-    const float *k_norm = nullptr;
-    CUtensorMap tm_wk{}, tm_wv{};
+    uint16_t *w_packed = nullptr;
+    float *k_norm = nullptr;             // ring-owned copy [n_layer][head_dim]
+    CUtensorMap tm_w{};
     int sms = 0;
 };
 
@@ -166,6 +166,8 @@ void release(ring_t *r) {
         cudaEventDestroy(rec.b);
     }
     for (auto e : r->ev_pool) cudaEventDestroy(e);
+    if (r->w_packed) cudaFree(r->w_packed);
+    if (r->k_norm) cudaFree(r->k_norm);
     if (r->graph_exec) cudaGraphExecDestroy(r->graph_exec);
     if (r->cap_stream) cudaStreamDestroy(r->cap_stream);
     delete r;
@@ -186,15 +188,30 @@ bool encode_kv_map(CUtensorMap *tm, void *base, const RingDims &d) {
     return res == CUDA_SUCCESS;
 }
 
-// 2-D TMA map over F16 weights [rows][hidden]: 64 x 128 boxes, 128-byte swizzle.
-bool encode_weight_map(CUtensorMap *tm, const void *base, int hidden, int64_t rows) {
+// 2-D TMA map over F16 rows [rows][hidden]: 64 x box_rows boxes, 128-byte swizzle.
+bool encode_weight_map(CUtensorMap *tm, const void *base, int hidden, int64_t rows,
+                       int box_rows = 128) {
     auto fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// 3-D TMA map over the packed producer weights: planes of 128 rows x 64 columns.
+bool encode_packed_map(CUtensorMap *tm, const void *base, int64_t planes) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, 128, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {128, 128 * 128};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
@@ -620,8 +637,16 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
 
 int ring_set_producer(ring_t *r, const ring_producer *p) {
     if (!r) return RING_EINVAL;
-    if (!p) {
+    auto drop = [&] {
+        if (r->w_packed || r->k_norm) cudaDeviceSynchronize();   // no step may still read them
+        if (r->w_packed) cudaFree(r->w_packed);
+        if (r->k_norm) cudaFree(r->k_norm);
+        r->w_packed = nullptr;
+        r->k_norm = nullptr;
         r->has_producer = false;
+    };
+    if (!p) {
+        drop();
         return RING_OK;
     }
     const RingDims &d = r->d;
@@ -633,15 +658,28 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
     if ((reinterpret_cast<uintptr_t>(p->wk) | reinterpret_cast<uintptr_t>(p->wv)) & 15)
         return fail(r, RING_EINVAL, "ring_set_producer: weights must be 16-byte aligned");
     if (!(p->eps >= 0.f)) return fail(r, RING_EINVAL, "ring_set_producer: eps must be >= 0");
-    const int64_t rows = (int64_t)d.n_layer * d.kv_row;
-    if (!encode_weight_map(&r->tm_wk, p->wk, p->hidden, rows) ||
-        !encode_weight_map(&r->tm_wv, p->wv, p->hidden, rows))
+    drop();
+    const size_t w_elems = (size_t)2 * d.n_layer * d.kv_row * p->hidden;
+    const size_t kn_bytes = sizeof(float) * (size_t)d.n_layer * d.head_dim;
+    cudaError_t e = cudaMalloc(&r->w_packed, w_elems * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&r->k_norm, kn_bytes);
+    if (e == cudaSuccess)
+        e = launch_pack_weights(static_cast<const uint16_t *>(p->wk), static_cast<const uint16_t *>(p->wv),
+                                r->w_packed, d.n_layer, d.n_head_kv, p->hidden, nullptr);
+    if (e == cudaSuccess) e = cudaMemcpy(r->k_norm, p->k_norm, kn_bytes, cudaMemcpyDeviceToDevice);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(r, e, "ring_set_producer: packing the weights");
+        drop();
+        return rc;
+    }
+    const int64_t planes = (int64_t)d.n_layer * 2 * d.n_head_kv * (p->hidden / 64);
+    if (!encode_packed_map(&r->tm_w, r->w_packed, planes)) {
+        drop();
         return fail(r, RING_ECUDA, "ring_set_producer: cuTensorMapEncodeTiled failed");
+    }
     r->hidden = p->hidden;
     r->eps = p->eps;
-    r->feat_wk = static_cast<const uint16_t *>(p->wk);
-    r->feat_wv = static_cast<const uint16_t *>(p->wv);
-    r->k_norm = p->k_norm;
     r->has_producer = true;
     return RING_OK;
 }
@@ -663,16 +701,40 @@ int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *fe
         m_total += x.n_new;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // Few sequences: the row ranges travel as kernel parameters, so the producer goes first
+    // and may overlap the previous kernel (programmatic serialization); the step state is
+    // staged after it.  Otherwise the producer reads the staged step state.
+    ProduceSeqs ps{};
+    if (r->d.n_seq <= kProduceParamSeqs) {
+        ps.n = r->d.n_seq;
+        for (int s = 0; s < r->d.n_seq; ++s) {
+            ps.base[s] = st[s].prod_base;
+            ps.n_new[s] = st[s].n_new;
+            ps.start[s] = st[s].start;
+            ps.src_row[s] = st[s].src_row;
+        }
+    }
+    CUtensorMap tm_feat{};
+    if (m_total > 0 && !encode_weight_map(&tm_feat, feat, r->hidden, n_rows, 32))
+        return fail(r, RING_ECUDA, "ring_begin_step_features: cuTensorMapEncodeTiled failed");
+    auto produce = [&](bool pdl) -> cudaError_t {
+        if (m_total == 0) return cudaSuccess;
+        const int ks = produce_split(m_total, r->d, r->hidden, r->sms);
+        return timed(r, 5, cs, [&] {
+            return launch_produce(r->d, r->m, &r->tm_w, &tm_feat,
+                                  static_cast<const uint16_t *>(feat), r->hidden, m_total, ks,
+                                  r->k_norm, r->eps, ps, pdl, cs);
+        });
+    };
+    cudaError_t e = cudaSuccess;
+    if (ps.n > 0) {
+        e = produce(!r->profiling);
+        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: producer launch");
+    }
     rc = stage_and_bulk(r, "ring_begin_step_features", st, nullptr, nullptr, n_rows, 0, cs);
     if (rc != RING_OK) return rc;
-    cudaError_t e = cudaSuccess;
-    if (m_total > 0) {
-        const int ks = produce_split(m_total, r->d, r->hidden, r->sms);
-        e = timed(r, 5, cs, [&] {
-            return launch_produce(r->d, r->m, &r->tm_wk, &r->tm_wv,
-                                  static_cast<const uint16_t *>(feat), r->hidden, m_total, ks,
-                                  r->k_norm, r->eps, cs);
-        });
+    if (ps.n == 0) {
+        e = produce(false);
         if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: producer launch");
     }
     e = timed(r, 1, cs, [&] {

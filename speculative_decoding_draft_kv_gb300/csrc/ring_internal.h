@@ -110,19 +110,39 @@ cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
                               cudaStream_t st);
 
+// Row ranges of the producer's packed row list, passed by value (no copy to the device
+// before the launch, so the launch can overlap the previous kernel) when n_seq is small.
+constexpr int kProduceParamSeqs = 16;
+struct ProduceSeqs {
+    int n;                                   // sequences described here; 0: use RingDev::steps
+    int64_t base[kProduceParamSeqs];         // first packed row of each sequence
+    int64_t n_new[kProduceParamSeqs];
+    int64_t start[kProduceParamSeqs];        // position of that row
+    int64_t src_row[kProduceParamSeqs];      // its feature row
+};
+
 // ---- launchers (produce_kernels.cu) ----
 cudaError_t produce_kernels_init();   // per device, before the first launch
+// W_k, W_v [n_layer][n_head_kv * 128][hidden] -> tiles of 128 rows x 64 columns, ordered
+// (layer, K heads then V heads, k-tile); out holds 2 * n_layer * n_head_kv * 128 * hidden.
+cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, uint16_t *out,
+                                int n_layer, int n_head_kv, int hidden, cudaStream_t st);
 size_t produce_smem_bytes();
 // split of the hidden dimension over a cluster (1, 2, 4 or 8 CTAs) for m_total rows
 int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms);
 // Context rows of the step's m_total new positions (packed over sequences by
 // SeqStep::prod_base) from F16 features [rows][hidden]: K = RoPE(k_norm(W_k x)), V = W_v x,
-// both rounded to F16 and stored in their ring slots, with slot_pos.  tm_wk / tm_wv: 2-D
-// TMA maps over W [n_layer * kv_row][hidden], 64 x 128 boxes, 128-byte swizzle.
-cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_wk,
-                           const CUtensorMap *tm_wv, const uint16_t *feat, int hidden,
+// both rounded to F16 and stored in their ring slots, with slot_pos.  tm_w: 3-D TMA map
+// over the packed weights (launch_pack_weights): 64 x 128 x 1 boxes, 128-byte swizzle.
+// seqs.n == 0: the row ranges are read from m.steps (staged before the launch).
+// pdl: launch with programmatic stream serialization; the kernel streams its first weight
+// tiles before its grid dependency resolves (weights are constant while steps run) and
+// waits before it reads features or touches ring state.
+// tm_feat: 2-D TMA map over the features [n_rows][hidden], 64 x 32 boxes, 128-byte swizzle.
+cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
+                           const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
                            int64_t m_total, int ks, const float *k_norm, float eps,
-                           cudaStream_t st);
+                           const ProduceSeqs &seqs, bool pdl, cudaStream_t st);
 
 // ---- shared host helpers (ring_host.cu) ----
 // 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],

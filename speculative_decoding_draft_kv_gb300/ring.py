@@ -231,8 +231,8 @@ def ring_begin_step(h, committed, k_rows, v_rows, row_off, first_pos, stream=Non
 
 def ring_set_producer(h, hidden, eps, wk, wv, k_norm):
     """wk, wv: CUDA float16 [n_layer, kv_row, hidden]; k_norm: CUDA float32
-    [n_layer, head_dim].  All None detaches the producer.  The caller keeps the tensors
-    alive while steps run."""
+    [n_layer, head_dim].  The ring copies them (synchronously); all None detaches the
+    producer."""
     import torch
     if wk is None and wv is None and k_norm is None:
         _check(_load().ring_set_producer(h, None), h, "ring_set_producer")
@@ -396,7 +396,6 @@ class Ring:
         ring_begin_step(self.h, committed, k_rows, v_rows, row_off, first_pos, stream)
 
     def set_producer(self, hidden, eps, wk, wv, k_norm):
-        self._producer = (wk, wv, k_norm)          # keep the weights alive
         ring_set_producer(self.h, hidden, eps, wk, wv, k_norm)
 
     def begin_step_features(self, committed, feat, row_off, first_pos, stream=None):

@@ -251,3 +251,25 @@ def test_producer_errors_and_state_unchanged():
         assert e.value.code == R.RING_ESTATE
     finally:
         ring.close()
+
+
+def test_many_sequences_read_the_staged_step_state():
+    """More sequences than travel as kernel parameters: the producer reads the row ranges
+    from the staged step state instead."""
+    w = synth.workload(1, n_layer=1, n_seq=20)
+    run = ProducerRun(w, 128)
+    try:
+        rng = np.random.default_rng(4)
+        c = np.zeros(w.n_seq, np.int64)
+        for t in range(3):
+            c = c + rng.integers(0, 40, w.n_seq)
+            run.begin_step(c)
+            run.check_state()
+            for s in range(w.n_seq):
+                run.check_kv(s, 0)
+            o = run.attend(t, 0, "full")
+            for s in (0, 7, 19):
+                assert_close(o[s], run.expected(t, 0, "full", s), f"step {t} seq {s}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
