@@ -37,15 +37,20 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_130_368, "kernel": "6e70da9100971eb7",
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_129_600, "kernel": "564f47ae5c6c7fe4",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
-    "batched_cap4096_s16_l5": {"bytes": 276_977_920, "kernel": "6e70da9100971eb7",
-                               "source": "profiles/attend_plain_batched_cap4096_s16_l5.md"},
 }
 
 
-def _kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "speculative_decoding_draft_kv_gb300", "csrc", "attn_kernels.cu")
+# the same for the context-row producer kernel (workload: steady decode, hidden 4096)
+PRODUCE_TRAFFIC = {
+    "steady_decode_cap4096_s1_l5": {"bytes": 86_200_000, "kernel": "4ec87acbdf3473a9",
+                                    "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
+}
+
+
+def _kernel_source_hash(name: str = "attn_kernels.cu") -> str:
+    p = os.path.join(ROOT, "speculative_decoding_draft_kv_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -457,12 +462,15 @@ def run_gb300(args):
         prod_bytes = (2 * w.n_layer * w.kv_row * H * 2 + rows * H * 2
                       + rows * w.n_layer * 2 * w.kv_row * 2)
         prod_ach = prod_bytes / (prod_ms * 1e-3) / 1e9
+        ptr = PRODUCE_TRAFFIC.get(w.name)
+        prod_traffic = (ptr["bytes"] if ptr and H == 4096
+                        and ptr.get("kernel") == _kernel_source_hash("produce_kernels.cu") else None)
         prod_obj = {
             "value": 1000.0 / ms_prod * world, "unit": UNIT, "ms_per_step": ms_prod,
             "steps": n5 - min(W, n5), "hidden": H,
             "api": "ring_begin_step_features + ring_attend per layer",
             "roofline": {"bound": "hbm", "achieved": prod_ach, "peak": peak, "unit": "GB/s",
-                         "frac": prod_ach / peak, "traffic": None, "kernel": "k_produce",
+                         "frac": prod_ach / peak, "traffic": prod_traffic, "kernel": "k_produce",
                          "alg_bytes_per_launch": prod_bytes, "launch_ms": prod_ms,
                          "rows_per_launch": rows,
                          "unit_bytes": "W_k and W_v of every layer + feature rows + K/V rows written"},
