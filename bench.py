@@ -475,6 +475,36 @@ def run_gb300(args):
                          "rows_per_launch": rows,
                          "unit_bytes": "W_k and W_v of every layer + feature rows + K/V rows written"},
         }
+        # ---- pass 6: the page's legacy path for comparison -- the whole window produced
+        # again every step (ring_recompute_window + ring_attend per layer); one sequence ----
+        if w.n_seq == 1:
+            start0 = int(P.plan[0][2][0])
+
+            def step_legacy(r, t):
+                c = P.plan[t][0]
+                lo = int(c[0]) - min(int(c[0]), w.cap)
+                r.recompute_window(c, feat_all, [lo - start0], [lo], stream)
+                for layer in range(w.n_layer):
+                    r.attend(layer, kind, P.q[layer], P.kn[layer], P.vn[layer], P.o[layer], stream)
+
+            n6 = min(K + W, 100)
+            ring = prod_ring()
+            timed_loop(ring, step_legacy, 1, min(W, n6))
+            torch.cuda.synchronize()
+            evs = timed_loop(ring, step_legacy, 1 + min(W, n6), n6 - min(W, n6))
+            torch.cuda.synchronize()
+            ms_leg = max_over_ranks(ms_of(evs), dist, dev) / max(1, n6 - min(W, n6))
+            assert ring.device_error() == 0
+            R.ring_profile_enable(ring.h, True)
+            timed_loop(ring, step_legacy, 1 + n6, max(1, min(20, len(P.plan) - 1 - n6)))
+            torch.cuda.synchronize()
+            pl = R.ring_profile_read(ring.h)["produce"]
+            ring.close()
+            prod_obj["legacy_recompute"] = {
+                "value": 1000.0 / ms_leg * world, "unit": UNIT, "ms_per_step": ms_leg,
+                "steps": n6 - min(W, n6), "rows_per_step": min(int(P.plan[1][0][0]), w.cap),
+                "produce_ms": pl["total_ms"] / max(pl["launches"], 1),
+                "api": "ring_recompute_window + ring_attend per layer (page section 1.6 fallback)"}
         del feat_all, wk, wv, kn
 
     cpu = None

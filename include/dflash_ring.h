@@ -204,6 +204,20 @@ int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *fe
                              void *stream);
 
 /*
+ * ring_recompute_window -- the page's legacy path (section 1.6: with the ring disabled
+ * the draft recomputes the whole window every step; section 1.7: the ring gives the
+ * same result): like ring_begin_step_features, but every position of [lo, committed) of
+ * every sequence is produced and written again, not only the new ones, so the rows must
+ * cover [lo, committed) (first_pos[s] <= lo).  The ring state afterwards is that of
+ * ring_begin_step_features up to the rounding order of the projection.  A comparison
+ * workload: it costs a projection of min(committed, cap) rows per sequence and layer.
+ * Errors: as ring_begin_step_features.
+ */
+int ring_recompute_window(ring_t *r, const int64_t *committed, const void *feat,
+                          const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                          void *stream);
+
+/*
  * ring_attend -- one draft layer's masked attention, enqueued on `stream`.
  *
  *   q        device F32 [n_seq][q_len][n_head][head_dim]: pre-RoPE noise-block queries.

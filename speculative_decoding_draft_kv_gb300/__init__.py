@@ -29,6 +29,7 @@ from .ring import (  # noqa: F401
     ring_init_ex,
     ring_last_error,
     ring_launch_count,
+    ring_recompute_window,
     ring_profile_enable,
     ring_profile_read,
     ring_rows_needed,

@@ -492,9 +492,12 @@ namespace {
 
 // Section 1.3 window arithmetic and every argument check of one begin_step; fills the
 // per-sequence step records.  Touches no state.
+// full_window: every position of [lo, c) is appended again (the page's legacy path that
+// recomputes the whole window each step), not only the new ones.
 int validate_step(ring_t *r, const char *who, const int64_t *committed, const void *k_rows,
                   const void *v_rows, const int64_t *row_off, const int64_t *first_pos,
-                  int64_t n_rows, std::vector<SeqStep> &st, int64_t &max_bulk) {
+                  int64_t n_rows, std::vector<SeqStep> &st, int64_t &max_bulk,
+                  bool full_window = false) {
     if (!committed) return fail(r, RING_EINVAL, "%s: committed is NULL", who);
     const RingDims &d = r->d;
     const int64_t pos_limit = (int64_t)INT32_MAX - d.q_len - 1;
@@ -510,7 +513,7 @@ int validate_step(ring_t *r, const char *who, const int64_t *committed, const vo
                         (long long)c, (long long)r->next_pos[s]);
         const int64_t win = std::min<int64_t>(c, d.cap);
         const int64_t lo = c - win;
-        const int64_t start = std::max(r->next_pos[s], lo);
+        const int64_t start = full_window ? lo : std::max(r->next_pos[s], lo);
         const int64_t n_new = c - start;
         SeqStep &x = st[s];
         x.committed = c;
@@ -684,16 +687,19 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
     return RING_OK;
 }
 
-int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *feat,
-                             const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
-                             void *stream) {
+}  // extern "C"
+
+namespace {
+int begin_step_features(ring_t *r, const char *who, const int64_t *committed, const void *feat,
+                        const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                        void *stream, bool full_window) {
     if (!r) return RING_EINVAL;
     if (!r->has_producer)
-        return fail(r, RING_ESTATE, "ring_begin_step_features: no producer set (ring_set_producer)");
+        return fail(r, RING_ESTATE, "%s: no producer set (ring_set_producer)", who);
     std::vector<SeqStep> st;
     int64_t max_bulk = 0;
-    int rc = validate_step(r, "ring_begin_step_features", committed, feat, feat, row_off, first_pos,
-                           n_rows, st, max_bulk);
+    int rc = validate_step(r, who, committed, feat, feat, row_off, first_pos, n_rows, st, max_bulk,
+                           full_window);
     if (rc != RING_OK) return rc;
     int64_t m_total = 0;
     for (auto &x : st) {
@@ -716,7 +722,7 @@ int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *fe
     }
     CUtensorMap tm_feat{};
     if (m_total > 0 && !encode_weight_map(&tm_feat, feat, r->hidden, n_rows, 32))
-        return fail(r, RING_ECUDA, "ring_begin_step_features: cuTensorMapEncodeTiled failed");
+        return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
     auto produce = [&](bool pdl) -> cudaError_t {
         if (m_total == 0) return cudaSuccess;
         const int ks = produce_split(m_total, r->d, r->hidden, r->sms);
@@ -729,21 +735,38 @@ int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *fe
     cudaError_t e = cudaSuccess;
     if (ps.n > 0) {
         e = produce(!r->profiling);
-        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: producer launch");
+        if (e != cudaSuccess) return cuda_fail(r, e, who);
     }
-    rc = stage_and_bulk(r, "ring_begin_step_features", st, nullptr, nullptr, n_rows, 0, cs);
+    rc = stage_and_bulk(r, who, st, nullptr, nullptr, n_rows, 0, cs);
     if (rc != RING_OK) return rc;
     if (ps.n == 0) {
         e = produce(false);
-        if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: producer launch");
+        if (e != cudaSuccess) return cuda_fail(r, e, who);
     }
     e = timed(r, 1, cs, [&] {
         return launch_begin_step(r->d, r->m, nullptr, nullptr, n_rows, !r->profiling, cs);
     });
-    if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step_features: launch");
+    if (e != cudaSuccess) return cuda_fail(r, e, who);
     r->last_was_begin = true;
     commit_host(r, committed);
     return RING_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *feat,
+                             const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                             void *stream) {
+    return begin_step_features(r, "ring_begin_step_features", committed, feat, row_off, first_pos,
+                               n_rows, stream, false);
+}
+
+int ring_recompute_window(ring_t *r, const int64_t *committed, const void *feat,
+                          const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                          void *stream) {
+    return begin_step_features(r, "ring_recompute_window", committed, feat, row_off, first_pos,
+                               n_rows, stream, true);
 }
 
 int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q, const void *k_noise,

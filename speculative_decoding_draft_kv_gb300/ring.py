@@ -33,7 +33,7 @@ EXPORTED = (
     "ring_begin_step", "ring_attend", "ring_step", "ring_get_slot_pos", "ring_get_mask",
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
-    "ring_last_error", "ring_set_producer", "ring_begin_step_features",
+    "ring_last_error", "ring_set_producer", "ring_begin_step_features", "ring_recompute_window",
 )
 
 
@@ -121,6 +121,7 @@ def _load():
         "ring_last_error": ([vp], ctypes.c_char_p),
         "ring_set_producer": ([vp, ctypes.POINTER(RingProducer)], ctypes.c_int),
         "ring_begin_step_features": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
+        "ring_recompute_window": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -242,7 +243,8 @@ def ring_set_producer(h, hidden, eps, wk, wv, k_norm):
     _check(_load().ring_set_producer(h, ctypes.byref(p)), h, "ring_set_producer")
 
 
-def ring_begin_step_features(h, committed, feat, row_off, first_pos, stream=None):
+def ring_begin_step_features(h, committed, feat, row_off, first_pos, stream=None,
+                             _entry="ring_begin_step_features"):
     """``feat``: CUDA float16 [n_rows, hidden] or None (no sequence appends)."""
     import torch
     n_seq = _N_SEQ.get(getattr(h, "value", h)) or ring_get_geometry(h)["n_seq"]
@@ -252,9 +254,15 @@ def ring_begin_step_features(h, committed, feat, row_off, first_pos, stream=None
     n_rows = 0 if feat is None else int(feat.shape[0])
     if feat is not None and feat.dim() != 2:
         raise ValueError("feat must be [n_rows, hidden]")
-    rc = _load().ring_begin_step_features(h, c_ptr, _dev_ptr(feat, torch.float16, "feat"), o_ptr,
-                                          f_ptr, n_rows, _stream(stream))
-    _check(rc, h, "ring_begin_step_features")
+    rc = getattr(_load(), _entry)(h, c_ptr, _dev_ptr(feat, torch.float16, "feat"), o_ptr, f_ptr,
+                                  n_rows, _stream(stream))
+    _check(rc, h, _entry)
+
+
+def ring_recompute_window(h, committed, feat, row_off, first_pos, stream=None):
+    """Every row of [lo, committed) produced again from ``feat`` (rows covering it)."""
+    ring_begin_step_features(h, committed, feat, row_off, first_pos, stream,
+                             _entry="ring_recompute_window")
 
 
 def ring_attend(h, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
@@ -400,6 +408,9 @@ class Ring:
 
     def begin_step_features(self, committed, feat, row_off, first_pos, stream=None):
         ring_begin_step_features(self.h, committed, feat, row_off, first_pos, stream)
+
+    def recompute_window(self, committed, feat, row_off, first_pos, stream=None):
+        ring_recompute_window(self.h, committed, feat, row_off, first_pos, stream)
 
     def attend(self, layer, mask_kind, q, k_noise, v_noise, o, stream=None):
         ring_attend(self.h, layer, mask_kind, q, k_noise, v_noise, o, stream)

@@ -60,12 +60,16 @@ class ProducerRun:
         return orc.produce_rows(self.feat(seq, pos), self.wk[layer], self.wv[layer],
                                 self.kn[layer], EPS, self.w.n_head_kv, self.w.head_dim)
 
-    def begin_step(self, committed):
+    def begin_step(self, committed, recompute=False):
+        """``recompute``: the legacy path -- every row of [lo, c) produced again."""
         w = self.w
         committed = np.asarray(committed, np.int64)
         starts, counts = [], []
         for s in range(w.n_seq):
             st, nn = self.book[s].rows_needed(int(committed[s]))
+            if recompute:
+                c = int(committed[s])
+                st, nn = c - min(c, w.cap), min(c, w.cap)
             starts.append(st)
             counts.append(nn)
         n_rows = int(sum(counts))
@@ -79,12 +83,14 @@ class ProducerRun:
                     feat[a:a + counts[s]] = synth.feature_rows(
                         w.seed, s, torch.arange(starts[s], committed[s], device=self.dev),
                         self.hidden, w.sigma, device=self.dev)
-        self.ring.begin_step_features(committed, feat, row_off, np.asarray(starts, np.int64))
+        step = self.ring.recompute_window if recompute else self.ring.begin_step_features
+        step(committed, feat, row_off, np.asarray(starts, np.int64))
         self._keep = feat
         paths = []
         for s in range(w.n_seq):
-            z = np.zeros((1, counts[s], 2), np.float16)
-            paths.append(self.book[s].begin_step(int(committed[s]), z, z, starts[s]))
+            st, nn = self.book[s].rows_needed(int(committed[s]))
+            z = np.zeros((1, nn, 2), np.float16)
+            paths.append(self.book[s].begin_step(int(committed[s]), z, z, st))
         self.committed = committed.copy()
         return paths
 
@@ -270,6 +276,27 @@ def test_many_sequences_read_the_staged_step_state():
             o = run.attend(t, 0, "full")
             for s in (0, 7, 19):
                 assert_close(o[s], run.expected(t, 0, "full", s), f"step {t} seq {s}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_legacy_window_recompute_equals_the_ring():
+    """The page's legacy path (the whole window produced again every step) leaves the
+    same ring state and gives the same attention as the ring's incremental appends."""
+    w = synth.workload(1, n_layer=2, n_seq=2, swa_window=24)
+    run = ProducerRun(w, 192)
+    try:
+        for t, c in enumerate([[5, 3], [30, 12], [90, 70], [95, 75], [300, 76]]):
+            run.begin_step(c, recompute=True)
+            run.check_state()
+            for s in range(w.n_seq):
+                for layer in range(w.n_layer):
+                    run.check_kv(s, layer)
+            for kind in ("full", "swa"):
+                o = run.attend(t, t % 2, kind)
+                for s in range(w.n_seq):
+                    assert_close(o[s], run.expected(t, t % 2, kind, s), f"step {t} seq {s} {kind}")
         assert run.ring.device_error() == 0
     finally:
         run.close()
