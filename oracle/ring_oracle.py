@@ -42,6 +42,15 @@ features, wk/wv times the features, then k_norm, then RoPE):
   P3  K then takes RoPE at p (R5, R6) and is rounded to F16; V is rounded to F16
       straight from the product.
 
+The whole draft step (the page's one-graph draft forward, section 1.5, with the noise
+block fed in per layer, section 1.6):
+  F1  a layer's noise-block rows come from its input hidden states h (one row per noise
+      position): Q = q_norm(W_q h), K = k_norm(W_k h), V = W_v h, with the same W_k, W_v
+      and k_norm as the context rows and q_norm an RMS norm over each query head with its
+      own weight [head_dim] (P2's form); K and V are handed to the attention as F16
+      pre-RoPE rows, Q as real pre-RoPE values;
+  F2  each layer attends with its own mask kind (full or SWA), a fixed per-layer pattern.
+
 Precision: float64 throughout, except for the F16 storage of K and V that the page
 fixes.  Parity pins for every function here live in tests/test_oracle_*.py.
 """
@@ -175,6 +184,19 @@ def produce_rows(feat, wk, wv, k_norm_w, eps: float, n_head_kv: int, head_dim: i
     k = x @ np.asarray(wk, dtype=np.float64).T
     v = x @ np.asarray(wv, dtype=np.float64).T
     return rms_norm_heads(k, k_norm_w, eps, n_head_kv, head_dim), to_f16(v)
+
+
+def project_noise(h, wq, wk, wv, q_norm_w, k_norm_w, eps: float, n_head: int, n_head_kv: int,
+                  head_dim: int):
+    """Noise-block rows of one layer from its hidden states ``h`` [q_len, hidden] (F1).
+
+    Returns Q (float64 [q_len, n_head, head_dim], pre-RoPE), K and V (F16
+    [q_len, n_head_kv * head_dim], pre-RoPE), as the attention takes them.
+    """
+    x = np.asarray(h, dtype=np.float64)
+    q = rms_norm_heads(x @ np.asarray(wq, dtype=np.float64).T, q_norm_w, eps, n_head, head_dim)
+    k, v = produce_rows(h, wk, wv, k_norm_w, eps, n_head_kv, head_dim)
+    return q.reshape(x.shape[0], n_head, head_dim), to_f16(k), v
 
 
 # ---------------------------------------------------------------------------

@@ -20,6 +20,8 @@ from .gen import (  # noqa: F401
     noise_rows,
     feature_rows,
     producer_weights,
+    query_weights,
+    noise_hidden,
 )
 from .workloads import (  # noqa: F401
     ACCEPT_HISTOGRAM,

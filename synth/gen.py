@@ -34,6 +34,9 @@ KIND_FEATURE = 6        # fused target features, keyed by absolute position
 KIND_W_K = 7            # producer weights, keyed by output row
 KIND_W_V = 8
 KIND_K_NORM = 9
+KIND_W_Q = 10           # the draft step's query projection
+KIND_Q_NORM = 11
+KIND_NOISE_H = 12       # noise-block hidden states, keyed by step * q_len + i
 
 # Standard deviation of a sum of four independent uniform integers on [0, 65535].
 _IRWIN_HALL4_STD = math.sqrt(4.0 * (65536.0 ** 2 - 1.0) / 12.0)
@@ -143,3 +146,20 @@ def producer_weights(seed: int, layer: int, kv_row: int, hidden: int, head_dim: 
     one = torch.zeros(1, dtype=torch.int64, device=device)
     kn = 1.0 + _rows(seed, KIND_K_NORM, 0, layer, one, head_dim, 0.1)[0]
     return wk, wv, kn
+
+
+def query_weights(seed: int, layer: int, q_rows: int, hidden: int, head_dim: int, device=None):
+    """One layer's query projection: W_q float16 ``[q_rows, hidden]`` (standard deviation
+    1/sqrt(hidden)) and the q_norm weight float32 ``[head_dim]`` around 1."""
+    rows = torch.arange(q_rows, dtype=torch.int64, device=device)
+    wq = _rows(seed, KIND_W_Q, 0, layer, rows, hidden, 1.0 / math.sqrt(hidden)).to(torch.float16)
+    one = torch.zeros(1, dtype=torch.int64, device=device)
+    qn = 1.0 + _rows(seed, KIND_Q_NORM, 0, layer, one, head_dim, 0.1)[0]
+    return wq, qn
+
+
+def noise_hidden(seed: int, step: int, seq: int, layer: int, q_len: int, hidden: int,
+                 sigma: float, device=None):
+    """Noise-block hidden states of one layer and step, float16 ``[q_len, hidden]``."""
+    idx = torch.arange(q_len, dtype=torch.int64, device=device) + step * q_len
+    return _rows(seed, KIND_NOISE_H, seq, layer, idx, hidden, sigma).to(torch.float16)

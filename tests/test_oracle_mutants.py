@@ -152,7 +152,32 @@ def _produce_v_normalised(feat, wk, wv, k_norm_w, eps, n_head_kv, head_dim):
             orc.to_f16(orc.rms_norm_heads(v, k_norm_w, eps, n_head_kv, head_dim)))
 
 
+def _noise_q_with_k_weight(h, wq, wk, wv, q_norm_w, k_norm_w, eps, n_head, n_head_kv, head_dim):
+    x = np.asarray(h, np.float64)
+    q = orc.rms_norm_heads(x @ np.asarray(wq, np.float64).T, k_norm_w, eps, n_head, head_dim)
+    k, v = orc.produce_rows(h, wk, wv, k_norm_w, eps, n_head_kv, head_dim)
+    return q.reshape(x.shape[0], n_head, head_dim), orc.to_f16(k), v
+
+
+def _noise_q_not_normalised(h, wq, wk, wv, q_norm_w, k_norm_w, eps, n_head, n_head_kv, head_dim):
+    x = np.asarray(h, np.float64)
+    q = x @ np.asarray(wq, np.float64).T
+    k, v = orc.produce_rows(h, wk, wv, k_norm_w, eps, n_head_kv, head_dim)
+    return q.reshape(x.shape[0], n_head, head_dim), orc.to_f16(k), v
+
+
+def _noise_k_not_normalised(h, wq, wk, wv, q_norm_w, k_norm_w, eps, n_head, n_head_kv, head_dim):
+    x = np.asarray(h, np.float64)
+    q = orc.rms_norm_heads(x @ np.asarray(wq, np.float64).T, q_norm_w, eps, n_head, head_dim)
+    k = x @ np.asarray(wk, np.float64).T
+    v = orc.to_f16(x @ np.asarray(wv, np.float64).T)
+    return q.reshape(x.shape[0], n_head, head_dim), orc.to_f16(k), v
+
+
 MUTANTS = {
+    "noise Q takes the k_norm weight": ("project_noise", _noise_q_with_k_weight),
+    "noise Q not normalised": ("project_noise", _noise_q_not_normalised),
+    "noise K not normalised": ("project_noise", _noise_k_not_normalised),
     "k_norm over the whole row": ("rms_norm_heads", _rms_whole_row),
     "k_norm eps outside the root": ("rms_norm_heads", _rms_eps_outside_root),
     "k_norm weight ignored": ("rms_norm_heads", _rms_weight_ignored),
@@ -198,6 +223,8 @@ PINS = [
     pins.test_k_norm_epsilon_inside_the_root,
     pins.test_producer_brute_force_small_integers,
     pins.test_producer_permutation_weights_pick_features,
+    pins.test_noise_projection_small_integers_and_heads,
+    pins.test_noise_projection_query_weight_per_head,
 ]
 
 

@@ -415,3 +415,47 @@ def test_producer_permutation_weights_pick_features():
     feat = (np.arange(2 * hidden, dtype=np.float64).reshape(2, hidden) - 5.0).astype(np.float16)
     _, v = orc.produce_rows(feat, P, P, np.ones(4), 0.0, 2, 4)
     np.testing.assert_array_equal(v, feat[:, perm])
+
+
+def test_noise_projection_small_integers_and_heads():
+    """F1: with small integers every product is exact: V noise equals the brute-force
+    triple loop, K noise rounds the unit-RMS heads of W_k h to F16, and every query head
+    of Q has mean square 1 (weights 1, eps 0) and points along the brute-force W_q h."""
+    rng = np.random.default_rng(21)
+    q_len, hidden, nh, nkv, d = 3, 10, 4, 2, 4
+    h = rng.integers(-2, 3, (q_len, hidden)).astype(np.float16)
+    wq = rng.integers(-1, 2, (nh * d, hidden)).astype(np.float16)
+    wk = rng.integers(-1, 2, (nkv * d, hidden)).astype(np.float16)
+    wv = rng.integers(-1, 2, (nkv * d, hidden)).astype(np.float16)
+    q, k, v = orc.project_noise(h, wq, wk, wv, np.ones(d), np.ones(d), 0.0, nh, nkv, d)
+    assert q.shape == (q_len, nh, d) and k.dtype == np.float16 and v.dtype == np.float16
+    for r in range(q_len):
+        for o in range(nkv * d):
+            assert float(v[r, o]) == sum(float(h[r, i]) * float(wv[o, i]) for i in range(hidden))
+        qb = np.array([sum(float(h[r, i]) * float(wq[o, i]) for i in range(hidden))
+                       for o in range(nh * d)]).reshape(nh, d)
+        for hh in range(nh):
+            if np.any(qb[hh]):
+                np.testing.assert_allclose(np.mean(q[r, hh] ** 2), 1.0, rtol=1e-13)
+                cosang = q[r, hh] @ qb[hh] / (np.linalg.norm(q[r, hh]) * np.linalg.norm(qb[hh]))
+                np.testing.assert_allclose(cosang, 1.0, rtol=1e-13)
+        kb = np.array([sum(float(h[r, i]) * float(wk[o, i]) for i in range(hidden))
+                       for o in range(nkv * d)]).reshape(nkv, d)
+        for g in range(nkv):
+            if np.any(kb[g]):
+                kk = k[r].reshape(nkv, d)[g].astype(np.float64)
+                np.testing.assert_allclose(np.mean(kk ** 2), 1.0, rtol=2e-3)    # F16 rounding
+
+
+def test_noise_projection_query_weight_per_head():
+    """F1: q_norm scales each query head's slice by its weight, element by element:
+    with W_q a permutation and unit-RMS features the head values are w times the features."""
+    d, nh, hidden = 4, 2, 8
+    perm = np.array([5, 2, 7, 0, 1, 6, 3, 4])
+    P = np.zeros((hidden, hidden), np.float16)
+    P[np.arange(hidden), perm] = 1.0
+    h = np.array([[1.0, -1.0, 1.0, -1.0, 1.0, 1.0, -1.0, -1.0]], np.float16)   # unit RMS
+    wqn = np.array([2.0, 0.5, -1.0, 3.0])
+    q, _, _ = orc.project_noise(h, P, P[:4], P[:4], wqn, np.ones(d), 0.0, nh, 1, d)
+    want = (h[0, perm].astype(np.float64).reshape(nh, d)) * wqn
+    np.testing.assert_allclose(q[0], want, rtol=0, atol=1e-15)
