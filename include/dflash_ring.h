@@ -181,6 +181,10 @@ typedef struct ring_producer {
     const void *wk;
     const void *wv;
     const float *k_norm;
+    const void *wq;          /* optional (with q_norm), for ring_draft_step: device F16
+                                [n_layer][n_head * head_dim][hidden]                        */
+    const float *q_norm;     /* optional: device F32 [n_layer][head_dim], the query heads'
+                                RMS-norm weight                                              */
 } ring_producer;
 int ring_set_producer(ring_t *r, const ring_producer *p);
 
@@ -216,6 +220,29 @@ int ring_begin_step_features(ring_t *r, const int64_t *committed, const void *fe
 int ring_recompute_window(ring_t *r, const int64_t *committed, const void *feat,
                           const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
                           void *stream);
+
+/*
+ * ring_draft_step -- one whole draft step of the page's one-graph draft forward (section
+ * 1.5; the noise block fed in per layer, section 1.6): ring_begin_step_features for the
+ * new context rows, then for every layer l in order
+ *   the noise-block projections of its hidden states h_l:  Q = q_norm(W_q h),
+ *   K = k_norm(W_k h), V = W_v h (the same W_k, W_v, k_norm as the context rows; pre-RoPE),
+ *   and the layer's attention with mask kind mask_kinds[l] (a per-layer full / SWA
+ *   pattern, as the Luce draft's sliding-window layers), output o[l].
+ * Needs ring_set_producer with wq and q_norm.
+ *
+ *   feat, row_off, first_pos, n_rows   as in ring_begin_step_features.
+ *   noise_h     device F16 [n_layer][n_seq][q_len][hidden], 16-byte aligned.
+ *   mask_kinds  host int32[n_layer]: RING_MASK_FULL or RING_MASK_SWA.
+ *   o           host array of n_layer device F32 [n_seq][q_len][n_head][head_dim].
+ *
+ * Launches in stream order with programmatic serialization between them (each kernel
+ * streams its first weight or K/V tiles while its predecessor finishes).
+ * Errors: ESTATE (no producer with W_q, or no step yet), EINVAL, ERANGE, ECUDA.
+ */
+int ring_draft_step(ring_t *r, const int64_t *committed, const void *feat,
+                    const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                    const void *noise_h, const int32_t *mask_kinds, float *const *o, void *stream);
 
 /*
  * ring_attend -- one draft layer's masked attention, enqueued on `stream`.

@@ -20,6 +20,7 @@ from .ring import (  # noqa: F401
     ring_describe,
     ring_destroy,
     ring_device_error,
+    ring_draft_step,
     ring_get_geometry,
     ring_get_kv,
     ring_get_mask,

@@ -159,13 +159,14 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
                  : "memory");
 }
 
-// Grid (ks * m_tiles, 2 * n_head_kv, n_layer); clusters of ks CTAs along x when ks > 1.
-// blockIdx.y < n_head_kv: K head y; else V head y - n_head_kv.
+// Grid (ks * m_tiles, heads, layers); clusters of ks CTAs along x when ks > 1.
+// blockIdx.y: K head y (y < n_head_kv), V head y - n_head_kv (y < 2 n_head_kv), else
+// query head y - 2 n_head_kv (noise rows only).  Layer = job.layer0 + blockIdx.z.
 __global__ void __launch_bounds__(kPThreads, 2)
 k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_feat,
           RingDims d, RingDev m, const uint16_t *__restrict__ feat, int hidden, int ks,
           int64_t m_total, const float *__restrict__ k_norm, float eps,
-          const __grid_constant__ ProduceSeqs seqs, int pdl) {
+          const __grid_constant__ ProduceSeqs seqs, int pdl, ProduceJob job, NoiseOut nout) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -179,9 +180,10 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ks > 1 ? cluster_rank() : 0u;
     const int64_t tile = (int64_t)blockIdx.x / ks;
-    const int yk = blockIdx.y, layer = blockIdx.z;
-    const bool is_v = yk >= d.n_head_kv;
-    const int head = is_v ? yk - d.n_head_kv : yk;
+    const int yk = blockIdx.y, layer = job.layer0 + (int)blockIdx.z;
+    const bool is_q = yk >= 2 * d.n_head_kv;
+    const bool is_v = !is_q && yk >= d.n_head_kv;
+    const int head = is_q ? yk - 2 * d.n_head_kv : (is_v ? yk - d.n_head_kv : yk);
     const int nkt = hidden / kPK;
     const int per = (nkt + ks - 1) / ks;
     const int kt0 = min(nkt, (int)rank * per), kt1 = min(nkt, kt0 + per);
@@ -189,7 +191,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
 
     // packed W tile (layer, K head y or V head y - n_head_kv, k-tile kt) is plane
     // wplane + kt of the packed weights
-    const int wplane = (layer * 2 * d.n_head_kv + yk) * nkt;
+    const int wplane = (layer * job.out_heads + yk) * nkt;
     const int n_pre = min(kPStages, kt1 - kt0);
     if (threadIdx.x == kPConsumers) {
         for (int k = 0; k < kPStages; ++k) {
@@ -213,7 +215,13 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
         const int64_t mr = tile * kPM + lane;
         int sq = -1;
         int64_t pos = 0, frow = -1;
-        if (mr < m_total && seqs.n > 0) {
+        if (job.mode == 1) {                        // noise rows: (sequence, i) of layer
+            if (mr < m_total) {
+                sq = (int)(mr / d.q_len);
+                pos = mr % d.q_len;
+                frow = (int64_t)layer * m_total + mr;
+            }
+        } else if (mr < m_total && seqs.n > 0) {
             for (int s = 0; s < seqs.n; ++s)
                 if (mr >= seqs.base[s] && mr < seqs.base[s] + seqs.n_new[s]) {
                     sq = s;
@@ -383,6 +391,28 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
             for (int src = 0; src < ks; ++src) a += recv[((int64_t)src * rows_per + lr) * kPN + lane + 32 * q4];
             v[q4] = a;
         }
+        if (job.mode == 1) {
+            // noise row i = p of sequence s: V as is, K and Q through their RMS norms
+            const int64_t row = ((int64_t)layer * d.n_seq + s) * d.q_len + p;
+            if (is_v) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    nout.v[row * d.kv_row + head * kHeadDim + lane + 32 * q4] = __half_as_ushort(__float2half_rn(v[q4]));
+                continue;
+            }
+            float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = rsqrtf(ss / (float)kPN + eps);
+            const float *w = (is_q ? nout.q_norm : k_norm) + (int64_t)layer * kPN;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float y = v[q4] * inv * w[lane + 32 * q4];
+                if (is_q) nout.q[(row * d.n_head + head) * kHeadDim + lane + 32 * q4] = y;
+                else nout.k[row * d.kv_row + head * kHeadDim + lane + 32 * q4] = __half_as_ushort(__float2half_rn(y));
+            }
+            continue;
+        }
         const int slot = (int)(p % d.cap);
         const int64_t base = ((((int64_t)s * d.n_layer + layer) * d.n_head_kv + head) * d.kv_total + slot) * kHeadDim;
         if (is_v) {
@@ -415,13 +445,16 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
 
 }  // namespace
 
-// Repack W_k and W_v [n_layer][kv_row][hidden] into tiles: tile ((layer * 2 * n_head_kv +
-// y) * nkt + kt), y = K head or n_head_kv + V head, holds rows head*128 .. +128 of that
-// weight, columns kt*64 .. +64, row-major (128 x 64 F16 = 16 KiB).  16 bytes per item.
+// Repack W_k, W_v [n_layer][kv_row][hidden] (and W_q [n_layer][n_q_heads * 128][hidden])
+// into tiles: tile ((layer * out_heads + y) * nkt + kt), y = K head, n_head_kv + V head or
+// 2 n_head_kv + Q head, holds rows head*128 .. +128 of that weight, columns kt*64 .. +64,
+// row-major (128 x 64 F16 = 16 KiB).  16 bytes per item.
 __global__ void k_pack_weights(const uint16_t *__restrict__ wk, const uint16_t *__restrict__ wv,
-                               uint16_t *__restrict__ out, int n_layer, int n_head_kv, int hidden) {
+                               const uint16_t *__restrict__ wq, uint16_t *__restrict__ out,
+                               int n_layer, int n_head_kv, int n_q_heads, int hidden) {
     const int nkt = hidden / kPK;
-    const int64_t total = (int64_t)n_layer * 2 * n_head_kv * nkt * kPN * (kPK / 8);
+    const int out_heads = 2 * n_head_kv + n_q_heads;
+    const int64_t total = (int64_t)n_layer * out_heads * nkt * kPN * (kPK / 8);
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int c8 = (int)(u % (kPK / 8));
@@ -430,21 +463,24 @@ __global__ void k_pack_weights(const uint16_t *__restrict__ wk, const uint16_t *
         t /= kPN;
         const int kt = (int)(t % nkt);
         t /= nkt;
-        const int yk = (int)(t % (2 * n_head_kv));
-        const int layer = (int)(t / (2 * n_head_kv));
-        const bool is_v = yk >= n_head_kv;
-        const int head = is_v ? yk - n_head_kv : yk;
-        const uint16_t *src = (is_v ? wv : wk) +
-                              ((int64_t)layer * n_head_kv * kPN + head * kPN + row) * hidden + kt * kPK + c8 * 8;
+        const int yk = (int)(t % out_heads);
+        const int layer = (int)(t / out_heads);
+        const bool is_q = yk >= 2 * n_head_kv;
+        const bool is_v = !is_q && yk >= n_head_kv;
+        const int head = is_q ? yk - 2 * n_head_kv : (is_v ? yk - n_head_kv : yk);
+        const int src_heads = is_q ? n_q_heads : n_head_kv;
+        const uint16_t *src = (is_q ? wq : (is_v ? wv : wk)) +
+                              ((int64_t)layer * src_heads * kPN + head * kPN + row) * hidden + kt * kPK + c8 * 8;
         *reinterpret_cast<uint4 *>(out + u * 8) = *reinterpret_cast<const uint4 *>(src);
     }
 }
 
 size_t produce_smem_bytes() { return (size_t)kPSmem; }
 
-cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, uint16_t *out,
-                                int n_layer, int n_head_kv, int hidden, cudaStream_t st) {
-    k_pack_weights<<<1024, 256, 0, st>>>(wk, wv, out, n_layer, n_head_kv, hidden);
+cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, const uint16_t *wq,
+                                uint16_t *out, int n_layer, int n_head_kv, int n_q_heads,
+                                int hidden, cudaStream_t st) {
+    k_pack_weights<<<1024, 256, 0, st>>>(wk, wv, wq, out, n_layer, n_head_kv, n_q_heads, hidden);
     return cudaGetLastError();
 }
 
@@ -452,9 +488,9 @@ cudaError_t produce_kernels_init() {
     return cudaFuncSetAttribute(k_produce, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
 }
 
-int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms) {
+int produce_split(int64_t m_total, int64_t heads_layers, int hidden, int sms) {
     const int64_t tiles = (m_total + kPM - 1) / kPM;
-    const int64_t base = tiles * 2 * d.n_head_kv * d.n_layer;
+    const int64_t base = tiles * heads_layers;
     const int nkt = hidden / kPK;
     int ks = 1;
     while (ks < kPMaxSplit && base * ks * 2 <= 2LL * sms && ks * 2 <= nkt) ks *= 2;
@@ -464,10 +500,12 @@ int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms) {
 cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
                            const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
                            int64_t m_total, int ks, const float *k_norm, float eps,
-                           const ProduceSeqs &seqs, bool pdl, cudaStream_t st) {
+                           const ProduceSeqs &seqs, bool pdl, const ProduceJob &job,
+                           const NoiseOut &nout, cudaStream_t st) {
     const int64_t tiles = (m_total + kPM - 1) / kPM;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(tiles * ks), 2 * d.n_head_kv, d.n_layer);
+    cfg.gridDim = job.mode == 1 ? dim3((unsigned)(tiles * ks), job.out_heads, 1)
+                                : dim3((unsigned)(tiles * ks), 2 * d.n_head_kv, d.n_layer);
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = kPSmem;
     cfg.stream = st;
@@ -488,7 +526,7 @@ cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMa
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, k_produce, *tm_w, *tm_feat, d, m, feat, hidden, ks, m_total,
-                              k_norm, eps, seqs, pdl ? 1 : 0);
+                              k_norm, eps, seqs, pdl ? 1 : 0, job, nout);
 }
 
 }  // namespace dflash

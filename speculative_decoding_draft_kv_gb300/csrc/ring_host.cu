@@ -91,6 +91,10 @@ struct dflash_ring {
     float eps = 0.f;
     uint16_t *w_packed = nullptr;
     float *k_norm = nullptr;             // ring-owned copy [n_layer][head_dim]
+    float *q_norm = nullptr;             // [n_layer][head_dim] when W_q is given
+    int out_heads = 0;                   // heads per layer in the packed weights
+    float *noise_q = nullptr;            // draft-step noise rows, [n_layer][n_seq][q_len][...]
+    uint16_t *noise_k = nullptr, *noise_v = nullptr;
     CUtensorMap tm_w{};
     int sms = 0;
 };
@@ -166,8 +170,9 @@ void release(ring_t *r) {
         cudaEventDestroy(rec.b);
     }
     for (auto e : r->ev_pool) cudaEventDestroy(e);
-    if (r->w_packed) cudaFree(r->w_packed);
-    if (r->k_norm) cudaFree(r->k_norm);
+    for (void *p : {(void *)r->w_packed, (void *)r->k_norm, (void *)r->q_norm, (void *)r->noise_q,
+                    (void *)r->noise_k, (void *)r->noise_v})
+        if (p) cudaFree(p);
     if (r->graph_exec) cudaGraphExecDestroy(r->graph_exec);
     if (r->cap_stream) cudaStreamDestroy(r->cap_stream);
     delete r;
@@ -641,11 +646,13 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
 int ring_set_producer(ring_t *r, const ring_producer *p) {
     if (!r) return RING_EINVAL;
     auto drop = [&] {
-        if (r->w_packed || r->k_norm) cudaDeviceSynchronize();   // no step may still read them
-        if (r->w_packed) cudaFree(r->w_packed);
-        if (r->k_norm) cudaFree(r->k_norm);
+        if (r->w_packed) cudaDeviceSynchronize();   // no step may still read them
+        for (void *q : {(void *)r->w_packed, (void *)r->k_norm, (void *)r->q_norm,
+                        (void *)r->noise_q, (void *)r->noise_k, (void *)r->noise_v})
+            if (q) cudaFree(q);
         r->w_packed = nullptr;
-        r->k_norm = nullptr;
+        r->k_norm = r->q_norm = r->noise_q = nullptr;
+        r->noise_k = r->noise_v = nullptr;
         r->has_producer = false;
     };
     if (!p) {
@@ -658,31 +665,44 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
                     p->hidden);
     if (!p->wk || !p->wv || !p->k_norm)
         return fail(r, RING_EINVAL, "ring_set_producer: weights are NULL");
-    if ((reinterpret_cast<uintptr_t>(p->wk) | reinterpret_cast<uintptr_t>(p->wv)) & 15)
+    if ((reinterpret_cast<uintptr_t>(p->wk) | reinterpret_cast<uintptr_t>(p->wv) |
+         reinterpret_cast<uintptr_t>(p->wq)) & 15)
         return fail(r, RING_EINVAL, "ring_set_producer: weights must be 16-byte aligned");
+    if (!p->wq != !p->q_norm)
+        return fail(r, RING_EINVAL, "ring_set_producer: give both wq and q_norm, or neither");
     if (!(p->eps >= 0.f)) return fail(r, RING_EINVAL, "ring_set_producer: eps must be >= 0");
     drop();
-    const size_t w_elems = (size_t)2 * d.n_layer * d.kv_row * p->hidden;
+    const int n_q = p->wq ? d.n_head : 0;
+    const int out_heads = 2 * d.n_head_kv + n_q;
+    const size_t w_elems = (size_t)out_heads * d.n_layer * d.head_dim * p->hidden;
     const size_t kn_bytes = sizeof(float) * (size_t)d.n_layer * d.head_dim;
+    const size_t noise_rows = (size_t)d.n_layer * d.n_seq * d.q_len;
     cudaError_t e = cudaMalloc(&r->w_packed, w_elems * 2);
     if (e == cudaSuccess) e = cudaMalloc(&r->k_norm, kn_bytes);
+    if (e == cudaSuccess && n_q) e = cudaMalloc(&r->q_norm, kn_bytes);
+    if (e == cudaSuccess && n_q) e = cudaMalloc(&r->noise_q, noise_rows * d.n_head * d.head_dim * 4);
+    if (e == cudaSuccess && n_q) e = cudaMalloc(&r->noise_k, noise_rows * d.kv_row * 2);
+    if (e == cudaSuccess && n_q) e = cudaMalloc(&r->noise_v, noise_rows * d.kv_row * 2);
     if (e == cudaSuccess)
         e = launch_pack_weights(static_cast<const uint16_t *>(p->wk), static_cast<const uint16_t *>(p->wv),
-                                r->w_packed, d.n_layer, d.n_head_kv, p->hidden, nullptr);
+                                static_cast<const uint16_t *>(p->wq), r->w_packed, d.n_layer,
+                                d.n_head_kv, n_q, p->hidden, nullptr);
     if (e == cudaSuccess) e = cudaMemcpy(r->k_norm, p->k_norm, kn_bytes, cudaMemcpyDeviceToDevice);
+    if (e == cudaSuccess && n_q) e = cudaMemcpy(r->q_norm, p->q_norm, kn_bytes, cudaMemcpyDeviceToDevice);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         int rc = cuda_fail(r, e, "ring_set_producer: packing the weights");
         drop();
         return rc;
     }
-    const int64_t planes = (int64_t)d.n_layer * 2 * d.n_head_kv * (p->hidden / 64);
+    const int64_t planes = (int64_t)d.n_layer * out_heads * (p->hidden / 64);
     if (!encode_packed_map(&r->tm_w, r->w_packed, planes)) {
         drop();
         return fail(r, RING_ECUDA, "ring_set_producer: cuTensorMapEncodeTiled failed");
     }
     r->hidden = p->hidden;
     r->eps = p->eps;
+    r->out_heads = out_heads;
     r->has_producer = true;
     return RING_OK;
 }
@@ -725,11 +745,12 @@ int begin_step_features(ring_t *r, const char *who, const int64_t *committed, co
         return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
     auto produce = [&](bool pdl) -> cudaError_t {
         if (m_total == 0) return cudaSuccess;
-        const int ks = produce_split(m_total, r->d, r->hidden, r->sms);
+        const int ks = produce_split(m_total, 2LL * r->d.n_head_kv * r->d.n_layer, r->hidden, r->sms);
+        const ProduceJob job{0, 0, r->out_heads};
         return timed(r, 5, cs, [&] {
             return launch_produce(r->d, r->m, &r->tm_w, &tm_feat,
                                   static_cast<const uint16_t *>(feat), r->hidden, m_total, ks,
-                                  r->k_norm, r->eps, ps, pdl, cs);
+                                  r->k_norm, r->eps, ps, pdl, job, NoiseOut{}, cs);
         });
     };
     cudaError_t e = cudaSuccess;
@@ -767,6 +788,52 @@ int ring_recompute_window(ring_t *r, const int64_t *committed, const void *feat,
                           void *stream) {
     return begin_step_features(r, "ring_recompute_window", committed, feat, row_off, first_pos,
                                n_rows, stream, true);
+}
+
+int ring_draft_step(ring_t *r, const int64_t *committed, const void *feat,
+                    const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
+                    const void *noise_h, const int32_t *mask_kinds, float *const *o, void *stream) {
+    if (!r) return RING_EINVAL;
+    const RingDims &d = r->d;
+    const char *who = "ring_draft_step";
+    if (!r->has_producer || !r->noise_q)
+        return fail(r, RING_ESTATE, "%s: no producer with W_q set (ring_set_producer)", who);
+    if (!noise_h || !mask_kinds || !o) return fail(r, RING_EINVAL, "%s: NULL argument", who);
+    if (reinterpret_cast<uintptr_t>(noise_h) & 15)
+        return fail(r, RING_EINVAL, "%s: noise_h must be 16-byte aligned", who);
+    const int64_t nrow = (int64_t)d.n_seq * d.q_len;
+    for (int l = 0; l < d.n_layer; ++l) {
+        int rc = validate_attend(r, who, l, mask_kinds[l], r->noise_q, r->noise_k, r->noise_v, o[l]);
+        if (rc != RING_OK) return rc;
+    }
+    CUtensorMap tm_h{};
+    if (!encode_weight_map(&tm_h, noise_h, r->hidden, nrow * d.n_layer, 32))
+        return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
+    int rc = begin_step_features(r, who, committed, feat, row_off, first_pos, n_rows, stream, false);
+    if (rc != RING_OK) return rc;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int ks = produce_split(nrow, r->out_heads, r->hidden, r->sms);
+    const NoiseOut nout{r->noise_q, r->noise_k, r->noise_v, r->q_norm};
+    ProduceSeqs ps{};
+    for (int l = 0; l < d.n_layer; ++l) {
+        // this layer's noise rows (Q, K, V from its hidden states), then its attention
+        const ProduceJob job{1, l, r->out_heads};
+        const bool pdl = !r->profiling;
+        cudaError_t e = timed(r, 5, cs, [&] {
+            return launch_produce(d, r->m, &r->tm_w, &tm_h, static_cast<const uint16_t *>(noise_h),
+                                  r->hidden, nrow, ks, r->k_norm, r->eps, ps, pdl, job, nout, cs);
+        });
+        if (e != cudaSuccess) return cuda_fail(r, e, who);
+        const int64_t qoff = (int64_t)l * nrow * d.n_head * d.head_dim;
+        const int64_t koff = (int64_t)l * nrow * d.kv_row;
+        // the projection writes no ring state, so the attention may fill its first stages
+        // early -- except after the begin-step kernel (layer 0), as in ring_step
+        r->last_was_begin = l == 0;
+        e = launch_layer(r, l, mask_kinds[l], r->noise_q + qoff, r->noise_k + koff,
+                         r->noise_v + koff, o[l], pdl, cs);
+        if (e != cudaSuccess) return cuda_fail(r, e, who);
+    }
+    return RING_OK;
 }
 
 int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q, const void *k_noise,

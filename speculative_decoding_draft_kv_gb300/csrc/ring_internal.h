@@ -121,15 +121,38 @@ struct ProduceSeqs {
     int64_t src_row[kProduceParamSeqs];      // its feature row
 };
 
+// Where the noise-block projection (ProduceJob::mode 1) puts a layer's rows: Q F32
+// [n_layer][n_seq][q_len][n_head][128] after q_norm, K and V F16 [n_layer][n_seq][q_len]
+// [kv_row] (K after k_norm), all pre-RoPE, as ring_attend takes them.
+struct NoiseOut {
+    float *q;
+    uint16_t *k, *v;
+    const float *q_norm;      // [n_layer][128]
+};
+
+// One launch of the projection kernel.
+//   mode 0: the step's new context rows (packed over sequences), every layer (grid z),
+//           K and V heads, written into the ring with RoPE at their positions;
+//   mode 1: the noise-block rows of layer `layer0` (n_seq * q_len rows of its hidden
+//           states), Q, K and V heads, written to NoiseOut.
+struct ProduceJob {
+    int mode;
+    int layer0;
+    int out_heads;            // heads in the packed weights per layer: 2 n_head_kv (+ n_head)
+};
+
 // ---- launchers (produce_kernels.cu) ----
 cudaError_t produce_kernels_init();   // per device, before the first launch
-// W_k, W_v [n_layer][n_head_kv * 128][hidden] -> tiles of 128 rows x 64 columns, ordered
-// (layer, K heads then V heads, k-tile); out holds 2 * n_layer * n_head_kv * 128 * hidden.
-cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, uint16_t *out,
-                                int n_layer, int n_head_kv, int hidden, cudaStream_t st);
+// W_k, W_v [n_layer][n_head_kv * 128][hidden] (and W_q [n_layer][n_q_heads * 128][hidden]
+// when n_q_heads > 0) -> tiles of 128 rows x 64 columns, ordered (layer, K heads, V heads,
+// Q heads, k-tile); out holds (2 n_head_kv + n_q_heads) * n_layer * 128 * hidden values.
+cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, const uint16_t *wq,
+                                uint16_t *out, int n_layer, int n_head_kv, int n_q_heads,
+                                int hidden, cudaStream_t st);
 size_t produce_smem_bytes();
-// split of the hidden dimension over a cluster (1, 2, 4 or 8 CTAs) for m_total rows
-int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms);
+// split of the hidden dimension over a cluster (1, 2, 4 or 8 CTAs) for m_total rows and
+// heads_layers (heads x layers) CTAs per row tile
+int produce_split(int64_t m_total, int64_t heads_layers, int hidden, int sms);
 // Context rows of the step's m_total new positions (packed over sequences by
 // SeqStep::prod_base) from F16 features [rows][hidden]: K = RoPE(k_norm(W_k x)), V = W_v x,
 // both rounded to F16 and stored in their ring slots, with slot_pos.  tm_w: 3-D TMA map
@@ -142,7 +165,8 @@ int produce_split(int64_t m_total, const RingDims &d, int hidden, int sms);
 cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
                            const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
                            int64_t m_total, int ks, const float *k_norm, float eps,
-                           const ProduceSeqs &seqs, bool pdl, cudaStream_t st);
+                           const ProduceSeqs &seqs, bool pdl, const ProduceJob &job,
+                           const NoiseOut &nout, cudaStream_t st);
 
 // ---- shared host helpers (ring_host.cu) ----
 // 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],

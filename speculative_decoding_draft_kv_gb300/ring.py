@@ -34,6 +34,7 @@ EXPORTED = (
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
     "ring_last_error", "ring_set_producer", "ring_begin_step_features", "ring_recompute_window",
+    "ring_draft_step",
 )
 
 
@@ -77,7 +78,8 @@ class RingProfile(ctypes.Structure):
 
 class RingProducer(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("eps", ctypes.c_float), ("wk", ctypes.c_void_p),
-                ("wv", ctypes.c_void_p), ("k_norm", ctypes.c_void_p)]
+                ("wv", ctypes.c_void_p), ("k_norm", ctypes.c_void_p), ("wq", ctypes.c_void_p),
+                ("q_norm", ctypes.c_void_p)]
 
 
 PROFILE_CLASSES = ("bulk", "begin", "attend", "combine", "step_graph", "produce")
@@ -122,6 +124,8 @@ def _load():
         "ring_set_producer": ([vp, ctypes.POINTER(RingProducer)], ctypes.c_int),
         "ring_begin_step_features": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
         "ring_recompute_window": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
+        "ring_draft_step": ([vp, p64, vp, p64, p64, i64, vp, ctypes.POINTER(i32),
+                             ctypes.POINTER(vp), vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -230,16 +234,18 @@ def ring_begin_step(h, committed, k_rows, v_rows, row_off, first_pos, stream=Non
     _check(rc, h, "ring_begin_step")
 
 
-def ring_set_producer(h, hidden, eps, wk, wv, k_norm):
+def ring_set_producer(h, hidden, eps, wk, wv, k_norm, wq=None, q_norm=None):
     """wk, wv: CUDA float16 [n_layer, kv_row, hidden]; k_norm: CUDA float32
-    [n_layer, head_dim].  The ring copies them (synchronously); all None detaches the
-    producer."""
+    [n_layer, head_dim]; optional wq (float16 [n_layer, n_head * head_dim, hidden]) and
+    q_norm (float32 [n_layer, head_dim]) for ring_draft_step.  The ring copies them
+    (synchronously); all None detaches the producer."""
     import torch
     if wk is None and wv is None and k_norm is None:
         _check(_load().ring_set_producer(h, None), h, "ring_set_producer")
         return
     p = RingProducer(int(hidden), float(eps), _dev_ptr(wk, torch.float16, "wk"),
-                     _dev_ptr(wv, torch.float16, "wv"), _dev_ptr(k_norm, torch.float32, "k_norm"))
+                     _dev_ptr(wv, torch.float16, "wv"), _dev_ptr(k_norm, torch.float32, "k_norm"),
+                     _dev_ptr(wq, torch.float16, "wq"), _dev_ptr(q_norm, torch.float32, "q_norm"))
     _check(_load().ring_set_producer(h, ctypes.byref(p)), h, "ring_set_producer")
 
 
@@ -257,6 +263,26 @@ def ring_begin_step_features(h, committed, feat, row_off, first_pos, stream=None
     rc = getattr(_load(), _entry)(h, c_ptr, _dev_ptr(feat, torch.float16, "feat"), o_ptr, f_ptr,
                                   n_rows, _stream(stream))
     _check(rc, h, _entry)
+
+
+def ring_draft_step(h, committed, feat, row_off, first_pos, noise_h, mask_kinds, o, stream=None):
+    """``noise_h``: CUDA float16 [n_layer, n_seq, q_len, hidden]; ``mask_kinds``: one
+    "full"/"swa" (or code) per layer; ``o``: n_layer CUDA float32 tensors
+    [n_seq, q_len, n_head, head_dim]."""
+    import torch
+    n_seq = _N_SEQ.get(getattr(h, "value", h)) or ring_get_geometry(h)["n_seq"]
+    c_arr, c_ptr = _i64_array(committed, n_seq, "committed")
+    o_arr, o_ptr = _i64_array(row_off, n_seq, "row_off")
+    f_arr, f_ptr = _i64_array(first_pos, n_seq, "first_pos")
+    n_rows = 0 if feat is None else int(feat.shape[0])
+    kinds = np.ascontiguousarray([MASK_KINDS.get(k, k) for k in mask_kinds], dtype=np.int32)
+    arr = ctypes.c_void_p * len(o)
+    op = arr(*[_dev_ptr(t, torch.float32, "o").value for t in o])
+    rc = _load().ring_draft_step(h, c_ptr, _dev_ptr(feat, torch.float16, "feat"), o_ptr, f_ptr,
+                                 n_rows, _dev_ptr(noise_h, torch.float16, "noise_h"),
+                                 kinds.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), op,
+                                 _stream(stream))
+    _check(rc, h, "ring_draft_step")
 
 
 def ring_recompute_window(h, committed, feat, row_off, first_pos, stream=None):
@@ -403,8 +429,13 @@ class Ring:
     def begin_step(self, committed, k_rows, v_rows, row_off, first_pos, stream=None):
         ring_begin_step(self.h, committed, k_rows, v_rows, row_off, first_pos, stream)
 
-    def set_producer(self, hidden, eps, wk, wv, k_norm):
-        ring_set_producer(self.h, hidden, eps, wk, wv, k_norm)
+    def set_producer(self, hidden, eps, wk, wv, k_norm, wq=None, q_norm=None):
+        ring_set_producer(self.h, hidden, eps, wk, wv, k_norm, wq, q_norm)
+
+    def draft_step(self, committed, feat, row_off, first_pos, noise_h, mask_kinds, o,
+                   stream=None):
+        ring_draft_step(self.h, committed, feat, row_off, first_pos, noise_h, mask_kinds, o,
+                        stream)
 
     def begin_step_features(self, committed, feat, row_off, first_pos, stream=None):
         ring_begin_step_features(self.h, committed, feat, row_off, first_pos, stream)

@@ -300,3 +300,112 @@ def test_legacy_window_recompute_equals_the_ring():
         assert run.ring.device_error() == 0
     finally:
         run.close()
+
+
+class DraftRun(ProducerRun):
+    """ProducerRun plus the query projection, for ring_draft_step."""
+
+    def __init__(self, w, hidden, pattern):
+        super().__init__(w, hidden)
+        self.pattern = pattern
+        qw = [synth.query_weights(w.seed, l, w.n_head * w.head_dim, hidden, w.head_dim)
+              for l in range(w.n_layer)]
+        self.wq = [x[0].numpy() for x in qw]
+        self.qn = [x[1].numpy() for x in qw]
+        gq = [synth.query_weights(w.seed, l, w.n_head * w.head_dim, hidden, w.head_dim,
+                                  device=self.dev) for l in range(w.n_layer)]
+        self.gwq = torch.stack([x[0] for x in gq]).contiguous()
+        self.gqn = torch.stack([x[1] for x in gq]).contiguous()
+        self.ring.set_producer(hidden, EPS, self.gwk, self.gwv, self.gkn, self.gwq, self.gqn)
+
+    def step(self, t, committed):
+        """One ring_draft_step; returns the outputs [n_layer] as numpy arrays."""
+        w = self.w
+        committed = np.asarray(committed, np.int64)
+        starts, counts = [], []
+        for s in range(w.n_seq):
+            st, nn = self.book[s].rows_needed(int(committed[s]))
+            starts.append(st)
+            counts.append(nn)
+        n_rows = int(sum(counts))
+        row_off = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
+        feat = None
+        if n_rows:
+            feat = torch.empty((n_rows, self.hidden), dtype=torch.float16, device=self.dev)
+            for s in range(w.n_seq):
+                if counts[s]:
+                    a = int(row_off[s])
+                    feat[a:a + counts[s]] = synth.feature_rows(
+                        w.seed, s, torch.arange(starts[s], committed[s], device=self.dev),
+                        self.hidden, w.sigma, device=self.dev)
+        h = torch.stack([torch.stack([synth.noise_hidden(w.seed, t, s, l, w.q_len, self.hidden,
+                                                         w.sigma, device=self.dev)
+                                      for s in range(w.n_seq)]) for l in range(w.n_layer)])
+        o = [torch.empty((w.n_seq, w.q_len, w.n_head, w.head_dim), device=self.dev)
+             for _ in range(w.n_layer)]
+        self.ring.draft_step(committed, feat, row_off, np.asarray(starts, np.int64),
+                             h.contiguous(), self.pattern, o)
+        torch.cuda.synchronize()
+        for s in range(w.n_seq):
+            z = np.zeros((1, counts[s], 2), np.float16)
+            self.book[s].begin_step(int(committed[s]), z, z, starts[s])
+        self.committed = committed.copy()
+        return [x.cpu().numpy() for x in o]
+
+    def expected_draft(self, t, layer, seq, heads=None):
+        w = self.w
+        h = synth.noise_hidden(w.seed, t, seq, layer, w.q_len, self.hidden, w.sigma).numpy()
+        q, kn, vn = orc.project_noise(h, self.wq[layer], self.wk[layer], self.wv[layer],
+                                      self.qn[layer], self.kn[layer], EPS, w.n_head,
+                                      w.n_head_kv, w.head_dim)
+        return orc.attend_dense(int(self.committed[seq]), w.cap,
+                                lambda pos: self.rows(seq, layer, pos), q, kn, vn, w.head_dim,
+                                w.n_head_kv, w.n_head, w.rope_theta, kind=self.pattern[layer],
+                                swa_window=self.swa, heads=heads)
+
+
+def test_draft_step_small_rings_mixed_pattern():
+    """ring_draft_step: context rows from features, noise Q/K/V from each layer's hidden
+    states, a full / SWA / full layer pattern; every output against the float64 route."""
+    w = synth.workload(1, n_layer=3, n_seq=2, swa_window=24)
+    run = DraftRun(w, 192, ["full", "swa", "full"])
+    try:
+        for t, c in enumerate([[5, 0], [14, 9], [60, 41], [63, 200], [150, 205]]):
+            outs = run.step(t, c)
+            run.check_state()
+            for layer in range(w.n_layer):
+                for s in range(w.n_seq):
+                    assert_close(outs[layer][s], run.expected_draft(t, layer, s),
+                                 f"step {t} layer {layer} seq {s}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_draft_step_full_size():
+    """cap 4096, 5 layers, hidden 4096: prefill then decode steps, sampled heads."""
+    w = synth.workload(2)
+    run = DraftRun(w, 4096, ["full"] * w.n_layer)
+    try:
+        heads = [0, 17, 31]
+        for t, c in enumerate(synth.commit_schedule(w, 2)):
+            outs = run.step(t, c)
+            for layer in (0, 4):
+                want = run.expected_draft(t, layer, 0, heads=heads)
+                assert_close(outs[layer][0][:, heads], want[:, heads], f"step {t} layer {layer}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_draft_step_needs_query_weights():
+    w = synth.workload(1, n_layer=1)
+    run = ProducerRun(w, 128)
+    try:
+        h = torch.zeros((1, 1, w.q_len, 128), dtype=torch.float16, device=run.dev)
+        o = [torch.empty((1, w.q_len, w.n_head, w.head_dim), device=run.dev)]
+        with pytest.raises(R.RingError) as e:
+            run.ring.draft_step([0], None, [0], [0], h, ["full"], o)
+        assert e.value.code == R.RING_ESTATE
+    finally:
+        run.close()
