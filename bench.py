@@ -505,6 +505,51 @@ def run_gb300(args):
                 "steps": n6 - min(W, n6), "rows_per_step": min(int(P.plan[1][0][0]), w.cap),
                 "produce_ms": pl["total_ms"] / max(pl["launches"], 1),
                 "api": "ring_recompute_window + ring_attend per layer (page section 1.6 fallback)"}
+        # ---- pass 7: the whole draft step (ring_draft_step): the producer, the begin-step
+        # kernel, then per layer the noise-block Q/K/V projections of its hidden states and
+        # its attention (every layer full mask here) ----
+        qws = [synth.query_weights(w.seed, l, w.n_head * w.head_dim, H, w.head_dim, device=dev)
+               for l in range(w.n_layer)]
+        wq = torch.stack([x[0] for x in qws]).contiguous()
+        qn = torch.stack([x[1] for x in qws]).contiguous()
+        del qws
+        noise_h = torch.stack([torch.stack([synth.noise_hidden(w.seed, 0, sid, l, w.q_len, H, w.sigma,
+                                                               device=dev) for sid in seq_ids])
+                               for l in range(w.n_layer)]).contiguous()
+        pattern = [kind] * w.n_layer
+
+        def draft_ring():
+            r = prod_ring()
+            r.set_producer(H, 1e-6, wk, wv, kn, wq, qn)
+            return r
+
+        def step_draft(r, t):
+            c, row_off, start, _ = P.plan[t]
+            r.draft_step(c, feat_all, row_off, start, noise_h, pattern, P.o, stream)
+
+        n7 = min(K + W, 400)
+        ring = draft_ring()
+        timed_loop(ring, step_draft, 1, min(W, n7))
+        torch.cuda.synchronize()
+        evs = timed_loop(ring, step_draft, 1 + min(W, n7), n7 - min(W, n7))
+        torch.cuda.synchronize()
+        ms_draft = max_over_ranks(ms_of(evs), dist, dev) / max(1, n7 - min(W, n7))
+        assert ring.device_error() == 0
+        ring.close()
+        ring = draft_ring()
+        R.ring_profile_enable(ring.h, True)
+        timed_loop(ring, step_draft, 1, min(n7, 100))
+        torch.cuda.synchronize()
+        pd = R.ring_profile_read(ring.h)
+        ring.close()
+        n_prof = min(n7, 100)
+        prod_obj["draft_step"] = {
+            "value": 1000.0 / ms_draft * world, "unit": UNIT, "ms_per_step": ms_draft,
+            "steps": n7 - min(W, n7), "pattern": pattern,
+            "kernel_ms_per_step": {k: v["total_ms"] / n_prof for k, v in pd.items()
+                                   if k in ("produce", "begin", "attend", "combine")},
+            "api": "ring_draft_step (producer + begin + per layer: noise Q/K/V projection, attention)"}
+        del wq, qn, noise_h
         del feat_all, wk, wv, kn
 
     cpu = None
