@@ -41,9 +41,10 @@ constexpr int kPABytes = kPM * kPAPitch;   // feature tile
 constexpr int kPStage = (kPBBytes + kPABytes + 1023) / 1024 * 1024;   // W tiles 1024-aligned
 constexpr int kPConsumers = 128;           // 4 warps, warp w -> columns [32 w, 32 w + 32)
 constexpr int kPThreads = kPConsumers + 32;
-constexpr int kPMaxSplit = 8;
+constexpr int kPMaxSplit = 3;            // wider splits measured slower (merge cost)
+constexpr int kPRecvRows = 40;             // >= ks * ceil(32 / ks) for ks = 1 .. 8
 constexpr int kPOffRecv = kPStages * kPStage;                 // [ks][rows_per][128] f32
-constexpr int kPOffBars = kPOffRecv + kPM * kPN * 4;
+constexpr int kPOffBars = kPOffRecv + kPRecvRows * kPN * 4;
 constexpr int kPOffMap = kPOffBars + 2 * kPStages * 8;
 constexpr int kPSmem = 1024 + kPOffMap + kPM * 16;
 constexpr uint64_t kPWaitNs = 2000000000ull;
@@ -187,7 +188,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     const int nkt = hidden / kPK;
     const int per = (nkt + ks - 1) / ks;
     const int kt0 = min(nkt, (int)rank * per), kt1 = min(nkt, kt0 + per);
-    const int rows_per = kPM / ks;
+    const int rows_per = (kPM + ks - 1) / ks;         // the last rank may own fewer
 
     // packed W tile (layer, K head y or V head y - n_head_kv, k-tile kt) is plane
     // wplane + kt of the packed weights
@@ -381,6 +382,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     const int half = kPN / 2;
     for (int lr = warp; lr < rows_per; lr += kPConsumers / 32) {
         const int r = (int)rank * rows_per + lr;
+        if (r >= kPM) break;
         const int s = map_seq[r];
         if (s < 0) continue;
         const int64_t p = map_pos[r];
@@ -493,7 +495,8 @@ int produce_split(int64_t m_total, int64_t heads_layers, int hidden, int sms) {
     const int64_t base = tiles * heads_layers;
     const int nkt = hidden / kPK;
     int ks = 1;
-    while (ks < kPMaxSplit && base * ks * 2 <= 2LL * sms && ks * 2 <= nkt) ks *= 2;
+    // as many CTAs as two per SM hold (any cluster size up to 8), at least 2 k-tiles each
+    while (ks < kPMaxSplit && base * (ks + 1) <= 2LL * sms && (ks + 1) * 2 <= nkt) ++ks;
     return ks;
 }
 
