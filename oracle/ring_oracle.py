@@ -51,6 +51,15 @@ block fed in per layer, section 1.6):
       pre-RoPE rows, Q as real pre-RoPE values;
   F2  each layer attends with its own mask kind (full or SWA), a fixed per-layer pattern.
 
+The quantised ring (the port's ~48 MiB draft-KV figure, section 1.7, is consistent with a
+q8_0 cache):
+  Q1  q8_0 blocks are 32 consecutive values of one head's row (head_dim / 32 blocks per
+      head); scale d = max|x| / 127 and codes round(x / d), rounding half away from zero,
+      computed in float32 (x * (1/d)); d is stored as F16 and a value reads back as
+      code * d_f16; an all-zero block has d = 0 and codes 0;
+  Q2  K is quantised straight from its rotated value (no F16 rounding first), V from its
+      input value; noise rows like context rows; pad rows are all-zero blocks.
+
 Precision: float64 throughout, except for the F16 storage of K and V that the page
 fixes.  Parity pins for every function here live in tests/test_oracle_*.py.
 """
@@ -126,6 +135,38 @@ def swa_low(committed: int, cap: int, swa_window: int) -> int:
 def to_f16(x) -> np.ndarray:
     """Round float64 values to IEEE binary16, nearest-even (numpy's direct conversion)."""
     return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+Q8_BLOCK = 32
+
+
+def q8_0_quantize(x):
+    """Codes (int8, same shape) and F16 scales (one per 32 values along the last axis) of
+    ``x`` (Q1).  The decisions are taken in float32."""
+    x = np.asarray(x, dtype=np.float64).astype(np.float32)
+    shp = x.shape
+    b = x.reshape(shp[:-1] + (shp[-1] // Q8_BLOCK, Q8_BLOCK))
+    amax = np.max(np.abs(b), axis=-1, keepdims=True)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(d > 0, np.float32(1.0) / np.where(d > 0, d, np.float32(1.0)),
+                       np.float32(0.0)).astype(np.float32)
+    v = (b * inv).astype(np.float32).astype(np.float64)
+    q = np.sign(v) * np.floor(np.abs(v) + 0.5)               # half away from zero
+    codes = np.clip(q, -127, 127).astype(np.int8).reshape(shp)
+    return codes, d[..., 0].astype(np.float16)
+
+
+def q8_0_dequantize(codes, scales) -> np.ndarray:
+    """float64 values of q8_0 ``codes`` with F16 ``scales`` (one per 32 codes)."""
+    c = np.asarray(codes, dtype=np.float64)
+    shp = c.shape
+    b = c.reshape(shp[:-1] + (shp[-1] // Q8_BLOCK, Q8_BLOCK))
+    return (b * np.asarray(scales, dtype=np.float64)[..., None]).reshape(shp)
+
+
+def q8_0_round_trip(x) -> np.ndarray:
+    return q8_0_dequantize(*q8_0_quantize(x))
 
 
 def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
@@ -229,7 +270,7 @@ class RingOracle:
     """One sequence's draft-KV ring: slot_pos, F16 K/V tensors and the masks."""
 
     def __init__(self, cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta,
-                 swa_window=0, bulk_chunk=1024):
+                 swa_window=0, bulk_chunk=1024, kv_format="f16"):
         if n_head % n_head_kv:
             raise ValueError("n_head must be a multiple of n_head_kv")
         g = geometry(cap, q_len, head_dim, n_head_kv, n_layer)
@@ -240,8 +281,19 @@ class RingOracle:
         self.a_step, self.trash_slot = g["a_step"], g["trash_slot"]
         self.kv_total, self.kv_row = g["kv_total"], g["kv_row"]
         # section 1.1: separate F16 tensors, zeroed once; one row of kv_row per slot
-        self.k = np.zeros((n_layer, self.kv_total, self.kv_row), np.float16)
-        self.v = np.zeros((n_layer, self.kv_total, self.kv_row), np.float16)
+        self.kv_format = kv_format
+        if kv_format == "q8_0":
+            # codes and F16 scales (Q1); self.k / self.v hold what the slots read back as
+            nb = self.kv_row // Q8_BLOCK
+            self.kq = np.zeros((n_layer, self.kv_total, self.kv_row), np.int8)
+            self.vq = np.zeros((n_layer, self.kv_total, self.kv_row), np.int8)
+            self.ks = np.zeros((n_layer, self.kv_total, nb), np.float16)
+            self.vs = np.zeros((n_layer, self.kv_total, nb), np.float16)
+            self.k = np.zeros((n_layer, self.kv_total, self.kv_row), np.float64)
+            self.v = np.zeros((n_layer, self.kv_total, self.kv_row), np.float64)
+        else:
+            self.k = np.zeros((n_layer, self.kv_total, self.kv_row), np.float16)
+            self.v = np.zeros((n_layer, self.kv_total, self.kv_row), np.float16)
         self.slot_pos = np.full(cap, -1, np.int64)      # reading R3
         self.next_pos = 0
         self.committed = None
@@ -252,13 +304,23 @@ class RingOracle:
         _, _, start, n_new = step_window(committed, self.next_pos, self.cap)
         return start, n_new
 
+    def _put(self, layer: int, slot: int, k_rot, v_row) -> None:
+        """Store a rotated K row and a V row in one slot: F16, or q8_0 blocks (Q1, Q2)."""
+        if self.kv_format == "q8_0":
+            self.kq[layer, slot], self.ks[layer, slot] = q8_0_quantize(k_rot)
+            self.vq[layer, slot], self.vs[layer, slot] = q8_0_quantize(v_row)
+            self.k[layer, slot] = q8_0_dequantize(self.kq[layer, slot], self.ks[layer, slot])
+            self.v[layer, slot] = q8_0_dequantize(self.vq[layer, slot], self.vs[layer, slot])
+        else:
+            self.k[layer, slot] = to_f16(k_rot)
+            self.v[layer, slot] = v_row
+
     def _store(self, p: int, k_row, v_row) -> None:
         """Section 1.2: the row of absolute position p goes to slot p % cap."""
         slot = slot_of(p, self.cap)
         for layer in range(self.n_layer):
             kr = rope_rows(k_row[layer], p, self.n_head_kv, self.head_dim, self.theta)
-            self.k[layer, slot] = to_f16(kr)
-            self.v[layer, slot] = v_row[layer]
+            self._put(layer, slot, kr, v_row[layer])
         self.slot_pos[slot] = p
 
     def begin_step(self, committed: int, k_rows, v_rows, first_pos: int) -> str:
@@ -291,6 +353,11 @@ class RingOracle:
                 else:
                     self.k[:, self.trash_slot] = 0
                     self.v[:, self.trash_slot] = 0
+                    if self.kv_format == "q8_0":
+                        self.kq[:, self.trash_slot] = 0
+                        self.vq[:, self.trash_slot] = 0
+                        self.ks[:, self.trash_slot] = 0
+                        self.vs[:, self.trash_slot] = 0
             path = "fold"
         self.next_pos = committed
         self.committed = committed
@@ -335,8 +402,7 @@ class RingOracle:
         c = self.committed
         for j in range(self.q_len):
             kr = rope_rows(k_noise[j], c + j, self.n_head_kv, self.head_dim, self.theta)
-            self.k[layer, self.cap + j] = to_f16(kr)
-            self.v[layer, self.cap + j] = v_noise[j]
+            self._put(layer, self.cap + j, kr, v_noise[j])
 
     def attend(self, layer: int, q, k_noise, v_noise, kind: str = "full") -> np.ndarray:
         """O [q_len, n_head, head_dim] float64 of the noise queries over the ring."""
@@ -362,7 +428,7 @@ class RingOracle:
 # ---------------------------------------------------------------------------
 
 def attend_dense(committed, cap, rows_fn, q, k_noise, v_noise, head_dim, n_head_kv, n_head,
-                 rope_theta, kind="full", swa_window=0, heads=None) -> np.ndarray:
+                 rope_theta, kind="full", swa_window=0, heads=None, kv_format="f16") -> np.ndarray:
     """Attention of the q_len noise queries over the positions [lo, committed) plus the
     noise block, computed from the rows themselves.
 
@@ -380,12 +446,15 @@ def attend_dense(committed, cap, rows_fn, q, k_noise, v_noise, head_dim, n_head_
         lo = c - min(swa_window, win)
     pos = np.arange(lo, c, dtype=np.int64)
     kc, vc = rows_fn(pos)
-    kc = to_f16(rope_rows(np.asarray(kc, np.float64), pos, n_head_kv, head_dim, rope_theta))
+    # the stored form of every key and value: F16, or q8_0 blocks read back (Q1, Q2)
+    store = q8_0_round_trip if kv_format == "q8_0" else to_f16
+    kc = store(rope_rows(np.asarray(kc, np.float64), pos, n_head_kv, head_dim, rope_theta))
     jn = np.arange(q_len)
-    kn = to_f16(rope_rows(np.asarray(k_noise, np.float64), c + jn, n_head_kv, head_dim,
-                          rope_theta))
+    kn = store(rope_rows(np.asarray(k_noise, np.float64), c + jn, n_head_kv, head_dim,
+                         rope_theta))
     keys = np.concatenate([kc, kn], axis=0).astype(np.float64)
-    vals = np.concatenate([np.asarray(vc), np.asarray(v_noise)], axis=0).astype(np.float64)
+    vals = np.concatenate([np.asarray(store(vc), np.float64), np.asarray(store(v_noise), np.float64)],
+                          axis=0)
     n_ctx = len(pos)
     mask = np.zeros((q_len, n_ctx + q_len), np.float64)
     if kind == "swa":

@@ -174,7 +174,52 @@ def _noise_k_not_normalised(h, wq, wk, wv, q_norm_w, k_norm_w, eps, n_head, n_he
     return q.reshape(x.shape[0], n_head, head_dim), orc.to_f16(k), v
 
 
+_ORIG_Q8 = orc.q8_0_quantize
+
+
+def _q8_blocks_of_16(x):
+    x = np.asarray(x, np.float64)
+    codes = np.empty(x.shape, np.int8)
+    scales = []
+    for h in range(0, x.shape[-1], 16):
+        c, sc = _ORIG_Q8(np.concatenate([x[..., h:h + 16], np.zeros(x.shape[:-1] + (16,))], -1))
+        codes[..., h:h + 16] = c[..., :16]
+        scales.append(sc[..., 0])
+    sc = np.stack(scales, -1)[..., ::2]
+    return codes, sc
+
+
+def _q8_divide_by_128(x):
+    x = np.asarray(x, np.float64).astype(np.float32)
+    b = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    d = (np.max(np.abs(b), -1, keepdims=True) / np.float32(128)).astype(np.float32)
+    inv = np.where(d > 0, np.float32(1) / np.where(d > 0, d, 1), 0).astype(np.float32)
+    v = (b * inv).astype(np.float64)
+    q = np.sign(v) * np.floor(np.abs(v) + 0.5)
+    return np.clip(q, -127, 127).astype(np.int8).reshape(x.shape), d[..., 0].astype(np.float16)
+
+
+def _q8_round_half_even(x):
+    x = np.asarray(x, np.float64).astype(np.float32)
+    b = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    d = (np.max(np.abs(b), -1, keepdims=True) / np.float32(127)).astype(np.float32)
+    inv = np.where(d > 0, np.float32(1) / np.where(d > 0, d, 1), 0).astype(np.float32)
+    q = np.rint((b * inv).astype(np.float64))
+    return np.clip(q, -127, 127).astype(np.int8).reshape(x.shape), d[..., 0].astype(np.float16)
+
+
+def _q8_dequant_scale_not_rounded(codes, scales):
+    c = np.asarray(codes, np.float64)
+    b = c.reshape(c.shape[:-1] + (c.shape[-1] // 32, 32))
+    s = np.asarray(scales, np.float64) * (1 + 2 ** -9)      # a scale that is not the stored one
+    return (b * s[..., None]).reshape(c.shape)
+
+
 MUTANTS = {
+    "q8_0 blocks of 16": ("q8_0_quantize", _q8_blocks_of_16),
+    "q8_0 scale max/128": ("q8_0_quantize", _q8_divide_by_128),
+    "q8_0 ties to even": ("q8_0_quantize", _q8_round_half_even),
+    "q8_0 read-back scale off": ("q8_0_dequantize", _q8_dequant_scale_not_rounded),
     "noise Q takes the k_norm weight": ("project_noise", _noise_q_with_k_weight),
     "noise Q not normalised": ("project_noise", _noise_q_not_normalised),
     "noise K not normalised": ("project_noise", _noise_k_not_normalised),
@@ -225,6 +270,8 @@ PINS = [
     pins.test_producer_permutation_weights_pick_features,
     pins.test_noise_projection_small_integers_and_heads,
     pins.test_noise_projection_query_weight_per_head,
+    pins.test_q8_0_hand_values,
+    pins.test_q8_0_error_bound_and_brute_force,
 ]
 
 

@@ -459,3 +459,77 @@ def test_noise_projection_query_weight_per_head():
     q, _, _ = orc.project_noise(h, P, P[:4], P[:4], wqn, np.ones(d), 0.0, nh, 1, d)
     want = (h[0, perm].astype(np.float64).reshape(nh, d)) * wqn
     np.testing.assert_allclose(q[0], want, rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# q8_0 blocks (Q1, Q2)
+# ---------------------------------------------------------------------------
+
+def test_q8_0_hand_values():
+    """A block whose largest magnitude is 127 has scale 1: integer values are their own
+    codes; 2.5 and -2.5 round away from zero; an all-zero block has scale 0; every block of
+    32 has its own scale."""
+    x = np.zeros(64)
+    x[0], x[1], x[2], x[3], x[4] = 127.0, -127.0, 2.5, -2.5, 7.0
+    x[32], x[33] = 0.5, -0.25                   # block 1: scale 0.5 / 127
+    codes, scales = orc.q8_0_quantize(x)
+    assert scales.dtype == np.float16 and codes.dtype == np.int8
+    assert float(scales[0]) == 1.0
+    assert list(codes[:5]) == [127, -127, 3, -3, 7] and not codes[5:32].any()
+    assert float(scales[1]) == float(np.float16(np.float32(0.5) / np.float32(127)))
+    assert list(codes[32:34]) == [127, -64] and not codes[34:].any()
+    z_codes, z_scales = orc.q8_0_quantize(np.zeros(32))
+    assert not z_codes.any() and float(z_scales[0]) == 0.0
+    np.testing.assert_array_equal(orc.q8_0_dequantize(codes[:32], scales[:1]),
+                                  [127, -127, 3, -3, 7] + [0] * 27)
+
+
+def test_q8_0_error_bound_and_brute_force():
+    """Round trip within half a step plus the F16 scale rounding, and the codes equal a
+    plain per-element loop in float32."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((5, 128)) * np.array([1e-3, 1.0, 30.0, 0.2, 5.0])[:, None]
+    codes, scales = orc.q8_0_quantize(x)
+    back = orc.q8_0_dequantize(codes, scales)
+    for r in range(5):
+        for b in range(4):
+            blk = x[r, 32 * b:32 * b + 32].astype(np.float32)
+            d = np.float32(np.max(np.abs(blk))) / np.float32(127)
+            inv = np.float32(1) / d
+            for j in range(32):
+                v = float(np.float32(blk[j] * inv))
+                want = int(math.copysign(math.floor(abs(v) + 0.5), v))
+                assert codes[r, 32 * b + j] == want
+            # x' - x = (q d - x) + q (d_f16 - d): half a step plus the scale's rounding
+            err = np.abs(back[r, 32 * b:32 * b + 32] - x[r, 32 * b:32 * b + 32])
+            d16 = float(np.float16(d))
+            bound = 0.5 * float(d) * (1 + 1e-6) + 127 * abs(d16 - float(d)) + 1e-30
+            assert np.all(err <= bound)
+
+
+def test_q8_0_ring_equals_dense():
+    """O1 with q8_0 slots (K quantised after RoPE, V as given, noise rows too) equals O2
+    with the same quantisation of exactly the window."""
+    import synth
+    import torch
+    w = synth.workload(1, n_layer=1, swa_window=24)
+    r = orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
+                       swa_window=w.swa_window, kv_format="q8_0")
+    for t, c in enumerate(synth.commit_schedule(w, 12)[:, 0]):
+        c = int(c)
+        start, _ = r.rows_needed(c)
+        pos = torch.arange(start, c)
+        k, v = synth.context_rows(w.seed, 0, 0, pos, w.kv_row, w.sigma)
+        r.begin_step(c, k.numpy()[None], v.numpy()[None], start)
+        q = synth.query_block(w.seed, t, 0, 0, w.q_len, w.n_head, w.head_dim, w.sigma).numpy()
+        kn, vn = synth.noise_rows(w.seed, t, 0, 0, w.q_len, w.kv_row, w.sigma)
+        for kind in ("full", "swa"):
+            o1 = r.attend(0, q, kn.numpy(), vn.numpy(), kind)
+
+            def rows(p):
+                kk, vv = synth.context_rows(w.seed, 0, 0, torch.as_tensor(p), w.kv_row, w.sigma)
+                return kk.numpy(), vv.numpy()
+            o2 = orc.attend_dense(c, w.cap, rows, q, kn.numpy(), vn.numpy(), w.head_dim,
+                                  w.n_head_kv, w.n_head, w.rope_theta, kind=kind,
+                                  swa_window=w.swa_window, kv_format="q8_0")
+            assert float(np.abs(o1 - o2).max()) < 1e-12
