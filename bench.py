@@ -253,7 +253,7 @@ def run_gb300(args):
     def new_ring():
         r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
                    n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
-                   max_cluster=args.max_cluster)
+                   max_cluster=args.max_cluster, kv_format=args.kv_format)
         c, row_off, start, _ = P.plan[0]             # prefill (bulk path), untimed
         r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
         torch.cuda.synchronize()
@@ -336,13 +336,16 @@ def run_gb300(args):
     attn = prof["attend"]
     attn_ms = attn["total_ms"] / max(attn["launches"], 1)
     vis = float(np.mean([visible_rows(w, P.plan[1 + j][0], kind) for j in range(n2)]))
-    kv_bytes = vis * w.kv_row * 2 * 2
+    q8 = args.kv_format == "q8_0"
+    # bytes a slot row holds: F16 two per value; q8_0 34 per 32 values (codes + F16 scale)
+    row_bytes = w.kv_row * (34 / 32 if q8 else 2)
+    kv_bytes = vis * row_bytes * 2
     q_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
     o_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
     alg_bytes = kv_bytes + q_bytes + o_bytes
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (attn_ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(w.name)
+    tr = NCU_TRAFFIC.get(w.name + ("_q8_0" if q8 else ""))
     traffic = tr["bytes"] if tr and tr.get("kernel") == _kernel_source_hash() else None
     shares = {k: v["total_ms"] for k, v in prof.items() if k != "step_graph"}
     tot = sum(shares.values()) or 1.0
@@ -406,7 +409,8 @@ def run_gb300(args):
     # kernel's own roofline ----
     prod_obj = None
     n_feat_rows = int(sum(int(P.plan[t][3].sum()) for t in range(len(P.plan))))
-    if args.producer_hidden > 0 and n_feat_rows * args.producer_hidden * 2 <= (1 << 30):
+    if (args.producer_hidden > 0 and not q8
+            and n_feat_rows * args.producer_hidden * 2 <= (1 << 30)):
         H = args.producer_hidden
         ws = [synth.producer_weights(w.seed, l, w.kv_row, H, w.head_dim, device=dev)
               for l in range(w.n_layer)]
@@ -554,10 +558,10 @@ def run_gb300(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, kind, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(w, kind, budget_s=args.cpu_seconds, kv_format=args.kv_format)
 
     if rank == 0:
-        vis_step = visible_rows(w, P.plan[1][0], kind) * w.kv_row * 4 * w.n_layer
+        vis_step = visible_rows(w, P.plan[1][0], kind) * row_bytes * 2 * w.n_layer
         line = {
             "metric": METRIC,
             "value": 1000.0 / ms_per_step * world,
@@ -569,13 +573,14 @@ def run_gb300(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16",
+            "dtype": "q8_0 slots, f16 mma, f32 accumulate" if q8 else "f16",
             "data": "synthetic (seeded counter-based generator; the with_producer pass uses "
                     "seeded random-init projection weights)",
             "config": {
                 "workload": w.name, "cap": w.cap, "q_len": w.q_len, "n_seq": w.n_seq,
                 "n_layer": w.n_layer, "head_dim": w.head_dim, "n_head_kv": w.n_head_kv,
-                "n_head": w.n_head, "mask": kind, "kv_total": g["kv_total"],
+                "n_head": w.n_head, "mask": kind, "kv_format": args.kv_format,
+                "kv_total": g["kv_total"],
                 "tiles_per_split": g["tiles_per_split"], "n_splits": g["n_splits"],
                 "cluster": g["cluster"], "groups": g["groups"],
                 "l2": ("flushed between steps (512 MiB write, untimed)" if flush
@@ -609,7 +614,7 @@ def run_gb300(args):
 # CPU oracle legs
 # ----------------------------------------------------------------------------------------
 
-def _oracle_setup(w):
+def _oracle_setup(w, kv_format="f16"):
     import numpy as np
     import torch
 
@@ -619,7 +624,8 @@ def _oracle_setup(w):
     sched = synth.commit_schedule(w, 10000)
     S = w.n_seq
     rings = [orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
-                            w.rope_theta, swa_window=w.swa_window) for _ in range(S)]
+                            w.rope_theta, swa_window=w.swa_window, kv_format=kv_format)
+             for _ in range(S)]
 
     def rows(s, a, b):
         ks, vs = [], []
@@ -640,13 +646,13 @@ def _oracle_setup(w):
     return sched, rings, rows, inputs
 
 
-def cpu_baseline(w, kind, budget_s=15.0, max_steps=None):
+def cpu_baseline(w, kind, budget_s=15.0, max_steps=None, kv_format="f16"):
     """Time the float64 oracle (ring-state route) on the host: untimed prefill, then as many
     full steps (begin_step for every sequence + every layer's attention, inputs drawn
     beforehand) as fit in ``budget_s``."""
     import time as _t
 
-    sched, rings, rows, inputs = _oracle_setup(w)
+    sched, rings, rows, inputs = _oracle_setup(w, kv_format)
     S = w.n_seq
     sample_seqs = min(S, 1)
     for s in range(sample_seqs):
@@ -683,7 +689,8 @@ def run_reference(args):
         return
     w = _workload(args)
     budget = max(5.0, min(150.0, 0.6 * (args.steps + args.warmup)))
-    cpu = cpu_baseline(w, args.mask, budget_s=budget, max_steps=args.steps + args.warmup)
+    cpu = cpu_baseline(w, args.mask, budget_s=budget, max_steps=args.steps + args.warmup,
+                       kv_format=args.kv_format)
     line = {
         "impl": "reference",
         "metric": METRIC, "value": cpu["value"], "unit": UNIT, "n_gpus": world,
@@ -691,7 +698,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": w.name, "cap": w.cap, "q_len": w.q_len, "n_seq": w.n_seq,
-                   "n_layer": w.n_layer, "mask": args.mask},
+                   "n_layer": w.n_layer, "mask": args.mask, "kv_format": args.kv_format},
         "cpu_baseline": cpu,
         "e2e": {"value": cpu["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -716,6 +723,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", choices=["f16", "q8_0"], default="f16",
+                    help="slot format of the ring (q8_0: 32-value blocks, codes + F16 scale)")
     ap.add_argument("--producer-hidden", type=int, default=4096,
                     help="width of the fused features for the producer pass (0: skip it)")
     args = ap.parse_args()

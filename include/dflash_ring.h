@@ -78,7 +78,19 @@ typedef struct ring_params {
                                 SM count and the number of (sequence, kv head) pairs          */
     int32_t max_cluster;     /* upper bound on the attention cluster size (1 = no clusters);
                                 0 = the largest the device can co-schedule, at most 16        */
+    int32_t kv_format;       /* RING_KV_F16 (default) or RING_KV_Q8_0: slots hold q8_0 blocks
+                                of 32 values (int8 codes, one F16 scale d = max|x| / 127,
+                                codes round(x / d) half away from zero, decided in float32);
+                                K is quantised straight from its rotated value, V from its
+                                input; pad rows are all-zero blocks.  (Page
+                                "DFLASH2_RING_PORT.md", section 1.7: the port's draft-KV
+                                size is that of a q8_0 cache.)  A q8_0 ring attends with
+                                independent CTAs (no clusters), dequantising each tile to F16
+                                in shared memory, and takes its context rows through
+                                ring_begin_step / ring_step only (no producer).              */
 } ring_params;
+
+enum { RING_KV_F16 = 0, RING_KV_Q8_0 = 1 };
 
 /* Geometry and sizes of an initialised ring (all counts, no pointers). */
 typedef struct ring_geometry {
@@ -293,8 +305,15 @@ int ring_get_mask(ring_t *r, int32_t seq, int32_t mask_kind, float *out);
 int ring_get_tile_flags(ring_t *r, int32_t seq, int32_t mask_kind, uint8_t *out);
 
 /* ring_get_kv -- host F16 bits [kv_total][kv_row] of K and V of (seq, layer), in the
- * page's row layout (either pointer may be NULL).  Syncs. */
+ * page's row layout (either pointer may be NULL).  F16 rings only (ESTATE otherwise).
+ * Syncs. */
 int ring_get_kv(ring_t *r, int32_t seq, int32_t layer, uint16_t *k, uint16_t *v);
+
+/* ring_get_kv_q8 -- q8_0 rings: host int8 codes [kv_total][kv_row] and F16 scale bits
+ * [kv_total][kv_row / 32] of K and V of (seq, layer), page row layout (any pointer may be
+ * NULL).  ESTATE on an F16 ring.  Syncs. */
+int ring_get_kv_q8(ring_t *r, int32_t seq, int32_t layer, int8_t *k_codes, uint16_t *k_scales,
+                   int8_t *v_codes, uint16_t *v_scales);
 
 /* ring_device_error -- synchronise, read and clear the device-side error word.  Returns
  * RING_OK, or RING_EDEVICE with the word's bits stored in *bits (may be NULL). */

@@ -23,6 +23,7 @@ from .ring import (  # noqa: F401
     ring_draft_step,
     ring_get_geometry,
     ring_get_kv,
+    ring_get_kv_q8,
     ring_get_mask,
     ring_get_slot_pos,
     ring_get_tile_flags,

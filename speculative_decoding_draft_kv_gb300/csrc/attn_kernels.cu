@@ -19,6 +19,9 @@
 //     per SM, so per-tile latency halves); every warp pushes its partial state into the
 //     shared memory of the CTA that owns its rows (distributed shared memory stores),
 //     and after one cluster barrier each CTA finishes 32 / cluster rows locally.
+// q8_0 slots (int8 codes + one F16 scale per 32 values) take the first shape with 17 KiB
+// stages of codes and scales; the consumers turn the codes straight into F16 MMA operands
+// in registers (no second pass through shared memory).
 #include "ring_internal.h"
 
 #include <cuda_fp16.h>
@@ -37,18 +40,22 @@ constexpr uint64_t kWaitNs = 2000000000ull;        // bounded waits give up afte
 // per SM, partial states pushed to the owning CTA of the cluster.  Plain: 4 consumer warps
 // (2 key halves), 3 stages, two CTAs per SM, key halves merged in shared memory and the
 // CTA's partial written straight from registers.
-template <bool CLUSTER>
+template <bool CLUSTER, bool Q8 = false>
 struct Shape {
     static constexpr int CW = CLUSTER ? 8 : 4;      // consumer warps
     static constexpr int kConsumers = CW * 32;
     static constexpr int kThreads = kConsumers + 32;
-    static constexpr int kStages = CLUSTER ? 6 : 3;
+    static constexpr int kStages = CLUSTER ? 6 : (Q8 ? 5 : 3);
     static constexpr int kSlices = CW / 2;          // key slices per tile
     static constexpr int kKeys = kTile / kSlices;   // keys per warp per tile (32 or 16)
     static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
     static constexpr int kKK = kKeys / 16;          // k-steps of P V per warp
     static constexpr int kMinBlocks = CLUSTER ? 1 : 2;
-    static constexpr int kOffQ = kStages * kStageBytes;  // 1024-aligned (swizzled like K)
+    // q8_0 slots: a stage holds a tile's K and V codes (two 128 x 64-byte TMA boxes) and
+    // their scales (2 x 512 bytes); the consumers turn codes into F16 MMA operands in
+    // registers, so a stage costs 17 KiB instead of 32 and five of them fit
+    static constexpr int kStageBytesT = Q8 ? 2 * kTile * 128 + 2 * kTile * 8 : kStageBytes;
+    static constexpr int kOffQ = kStages * kStageBytesT;  // 1024-aligned (swizzled like K)
     static constexpr int kOffBits = kOffQ + kQBytes;
     static constexpr int kOffBars = kOffBits + kStages * kBitsPerStage;
     static constexpr int kOffRecv = kOffBars + 2 * kStages * 8 + 16;
@@ -59,11 +66,13 @@ struct Shape {
     // key-slice pre-merge scratch (in the idle stage buffers): every warp's partial,
     // 64 numerators + 2 maxima + 2 sums per lane
     static constexpr int kXPer = 68 * 32;
-    static_assert(kSlices * 2 * kXPer * 4 <= kStages * kStageBytes, "pre-merge scratch");
+    static_assert(kSlices * 2 * kXPer * 4 <= kStages * kStageBytesT, "pre-merge scratch");
+    static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStages * kStageBytesT,
+                  "key-half merge scratch must fit in the idle stage buffers");
+    static_assert(kStageBytesT % 1024 == 0, "stages keep TMA boxes 1024-aligned");
+    static_assert(!Q8 || (!CLUSTER && kKeys == 32), "q8_0 operands: plain shape, 32 keys a warp");
     static constexpr int kSmem = 1024 + kOffRecv + (CLUSTER ? kRecvBytes : 0);
 };
-static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStageBytes,
-              "key-half merge scratch must fit in stage buffer 0");
 
 // ---------------------------------------------------------------------------------
 // PTX helpers
@@ -212,6 +221,25 @@ __device__ __forceinline__ void bar_arrive(int id, int n) {
     asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Two q8_0 codes as an F16 pair times a pair of scales.  `wx` holds four codes with their
+// sign bits flipped (code + 128 as unsigned bytes); `sel` picks two of those bytes and puts
+// 0x64 above each, which as binary16 reads 1024 + (code + 128); subtracting 1152 leaves
+// the code exactly, and one correctly rounded multiply gives code * scale in F16 -- the
+// same value as rounding the exact float32 product.  Explicit .rn keeps the two apart.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t wx, uint32_t sel, uint32_t s2) {
+    const uint32_t h = prmt(wx, 0x64646464u, sel);
+    uint32_t c, r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(h), "r"(0x64806480u));   // 1152, 1152
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(c), "r"(s2));
+    return r;
+}
+
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
@@ -242,14 +270,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 //              barrier that CTA merges the kSlices * cluster partial states of its rows
 //              and writes O (or a group partial for the combine kernel).
 // ---------------------------------------------------------------------------------
-template <bool CLUSTER>
-__global__ void __launch_bounds__(Shape<CLUSTER>::kThreads, Shape<CLUSTER>::kMinBlocks)
+template <bool CLUSTER, bool Q8>
+__global__ void __launch_bounds__(Shape<CLUSTER, Q8>::kThreads, Shape<CLUSTER, Q8>::kMinBlocks)
 k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          RingDims d, RingDev m, int layer, int kind, float scale_log2,
          const float *__restrict__ q, const uint16_t *__restrict__ k_noise,
          const uint16_t *__restrict__ v_noise, float *__restrict__ o, int preload) {
-    using SH = Shape<CLUSTER>;
+    using SH = Shape<CLUSTER, Q8>;
     constexpr int CW = SH::CW;
+    constexpr int kStageB = SH::kStageBytesT;
     constexpr int kStages = SH::kStages;
     constexpr int kOffQ = SH::kOffQ, kOffBits = SH::kOffBits, kOffBars = SH::kOffBars,
                   kOffRecv = SH::kOffRecv;
@@ -295,6 +324,32 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         // The whole warp walks the tile list (so every barrier it meets is met by all 32
         // lanes together); lane 0 alone waits on the stage barriers and issues the copies.
         const int zrow = (s * d.n_layer + layer) * d.n_head_kv + gk;
+        // lane 0: one stage's copies of tile t (F16: four 64 x 64 boxes; q8_0: two 128 x 64
+        // code boxes and the scales of the tile's rows), plus its visibility bits
+        auto issue = [&](int stg, int t, int flag) {
+            const uint32_t full = bar0 + 8 * stg;
+            const uint32_t dk = smem_u32(smem + stg * kStageB);
+            const uint32_t nbits = flag == 2 ? (uint32_t)qw * 8u : 0u;
+            if constexpr (Q8) {
+                const int rows = min(kTile, d.kv_total - t * kTile);     // 64 or 32
+                mbar_expect_tx(full, 2 * kTile * 128 + 2 * rows * 8 + nbits);
+                tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
+                tma_load_3d(dk + kTile * 128, &tm_v, 0, t * kTile, zrow, full);
+                const int64_t so = ((int64_t)zrow * d.kv_total + (int64_t)t * kTile) * (kHeadDim / 32);
+                bulk_g2s(dk + 2 * kTile * 128, m.ks + so, rows * 8, full);
+                bulk_g2s(dk + 2 * kTile * 128 + kTile * 8, m.vs + so, rows * 8, full);
+            } else {
+                const uint32_t dv = dk + kTileBytes;
+                mbar_expect_tx(full, kStageBytes + nbits);
+                tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
+                tma_load_3d(dk + kHalfBox, &tm_k, 64, t * kTile, zrow, full);
+                tma_load_3d(dv, &tm_v, 0, t * kTile, zrow, full);
+                tma_load_3d(dv + kHalfBox, &tm_v, 64, t * kTile, zrow, full);
+            }
+            if (nbits)
+                bulk_g2s(smem_u32(smem + kOffBits + stg * kBitsPerStage),
+                         m.maskbits + (fbase + t) * qw, nbits, full);
+        };
         bool noise_ready = false;
         int it = 0;
         int t = t0;
@@ -326,20 +381,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 const int flag = flags[t];
                 if (flag == 0) continue;
                 if (t >= tn0 && t <= tn1) break;
-                if (lane == 0) {
-                    const uint32_t full = bar0 + 8 * it;
-                    const uint32_t dk = smem_u32(smem + it * kStageBytes);
-                    const uint32_t dv = dk + kTileBytes;
-                    const uint32_t nbits = flag == 2 ? (uint32_t)qw * 8u : 0u;
-                    mbar_expect_tx(full, kStageBytes + nbits);
-                    tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
-                    tma_load_3d(dk + kHalfBox, &tm_k, 64, t * kTile, zrow, full);
-                    tma_load_3d(dv, &tm_v, 0, t * kTile, zrow, full);
-                    tma_load_3d(dv + kHalfBox, &tm_v, 64, t * kTile, zrow, full);
-                    if (nbits)
-                        bulk_g2s(smem_u32(smem + kOffBits + it * kBitsPerStage),
-                                 m.maskbits + (fbase + t) * qw, nbits, full);
-                }
+                if (lane == 0) issue(it, t, flag);
                 __syncwarp();
                 ++it;
             }
@@ -367,18 +409,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 } else if (s_abort) {
                     ok = 0;
                 } else {
-                    const uint32_t full = bar0 + 8 * stg;
-                    const uint32_t dk = smem_u32(smem + stg * kStageBytes);
-                    const uint32_t dv = dk + kTileBytes;
-                    const uint32_t nbits = flag == 2 ? (uint32_t)qw * 8u : 0u;
-                    mbar_expect_tx(full, kStageBytes + nbits);
-                    tma_load_3d(dk, &tm_k, 0, t * kTile, zrow, full);
-                    tma_load_3d(dk + kHalfBox, &tm_k, 64, t * kTile, zrow, full);
-                    tma_load_3d(dv, &tm_v, 0, t * kTile, zrow, full);
-                    tma_load_3d(dv + kHalfBox, &tm_v, 64, t * kTile, zrow, full);
-                    if (nbits)
-                        bulk_g2s(smem_u32(smem + kOffBits + stg * kBitsPerStage),
-                                 m.maskbits + (fbase + t) * qw, nbits, full);
+                    issue(stg, t, flag);
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -446,7 +477,59 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     *reinterpret_cast<const uint2 *>(hi);
             }
         }
-        if (owns_noise) {
+        if (Q8 && owns_noise) {
+            // q8_0 slots: the same items, quantised per 32-value block by the four lanes
+            // that hold it (every thread runs every round, so the shuffles see full warps)
+            const int64_t head = ((int64_t)s * d.n_layer + layer) * d.n_head_kv + gk;
+            const int n_items = d.q_len * (half / 8);
+            for (int u0 = 0; u0 < n_items; u0 += SH::kConsumers) {
+                const int u = u0 + tid;
+                const bool okn = u < n_items;
+                const int uu = okn ? u : 0;
+                const int i = uu / (half / 8), jc = uu - i * (half / 8);
+                const uint16_t *ks = k_noise + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + jc * 8;
+                const uint16_t *vs = v_noise + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + jc * 8;
+                uint4 a = make_uint4(0, 0, 0, 0), bq = a, va = a, vb = a;
+                if (okn) {
+                    a = *reinterpret_cast<const uint4 *>(ks);
+                    bq = *reinterpret_cast<const uint4 *>(ks + half);
+                    va = *reinterpret_cast<const uint4 *>(vs);
+                    vb = *reinterpret_cast<const uint4 *>(vs + half);
+                }
+                const uint16_t *a16 = reinterpret_cast<const uint16_t *>(&a);
+                const uint16_t *b16 = reinterpret_cast<const uint16_t *>(&bq);
+                const uint16_t *va16 = reinterpret_cast<const uint16_t *>(&va);
+                const uint16_t *vb16 = reinterpret_cast<const uint16_t *>(&vb);
+                float k1[8], k2[8], v1[8], v2[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 rr = rope_rotate(a16[e], b16[e], csq[i * half + jc * 8 + e]);
+                    k1[e] = rr.x;
+                    k2[e] = rr.y;
+                    v1[e] = __half2float(__ushort_as_half(va16[e]));
+                    v2[e] = __half2float(__ushort_as_half(vb16[e]));
+                }
+                float dk1, dk2, dv1, dv2;
+                const uint2 ck1 = q8_quant8(k1, &dk1), ck2 = q8_quant8(k2, &dk2);
+                const uint2 cv1 = q8_quant8(v1, &dv1), cv2 = q8_quant8(v2, &dv2);
+                if (okn) {
+                    const int64_t dst = (head * d.kv_total + d.cap + i) * kHeadDim + jc * 8;
+                    *reinterpret_cast<uint2 *>(m.kq + dst) = ck1;
+                    *reinterpret_cast<uint2 *>(m.kq + dst + half) = ck2;
+                    *reinterpret_cast<uint2 *>(m.vq + dst) = cv1;
+                    *reinterpret_cast<uint2 *>(m.vq + dst + half) = cv2;
+                    if ((jc & 3) == 0) {
+                        const int64_t sb = (head * d.kv_total + d.cap + i) * (kHeadDim / 32);
+                        const int b1 = jc >> 2, b2 = 2 + (jc >> 2);
+                        m.ks[sb + b1] = __half_as_ushort(__float2half_rn(dk1));
+                        m.ks[sb + b2] = __half_as_ushort(__float2half_rn(dk2));
+                        m.vs[sb + b1] = __half_as_ushort(__float2half_rn(dv1));
+                        m.vs[sb + b2] = __half_as_ushort(__float2half_rn(dv2));
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        } else if (owns_noise) {
             // noise block of this head: K turned at committed + i, V copied.  Item u =
             // (noise row, 8 consecutive pairs); loads first, then stores.
             const int64_t head = ((int64_t)s * d.n_layer + layer) * d.n_head_kv + gk;
@@ -492,7 +575,21 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const int g = lane >> 2, c = lane & 3;
         const int r0 = mb * 16 + g, r1 = r0 + 8;
         uint32_t qf[8][4];
-        {
+        if constexpr (Q8) {
+            // q8_0 K operands come four consecutive dimensions to a thread (4c .. 4c+3 of
+            // each 16), which fill the MMA's k slots 2c, 2c+1, 2c+8, 2c+9; the query takes
+            // the same order (a dot product does not care which slot holds which dimension)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int col = ks * 16 + 4 * c;
+                const uint2 a = *reinterpret_cast<const uint2 *>(sq + swz(r0, col & ~7, kRows) + (col & 7) * 2);
+                const uint2 b = *reinterpret_cast<const uint2 *>(sq + swz(r1, col & ~7, kRows) + (col & 7) * 2);
+                qf[ks][0] = a.x;
+                qf[ks][1] = b.x;
+                qf[ks][2] = a.y;
+                qf[ks][3] = b.y;
+            }
+        } else {
             const uint32_t sqa = smem_u32(sq);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
@@ -536,21 +633,48 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             s_abort = 1;
             return false;
         };
-        // S = Q K^T over this warp's keys of stage `stg`, scaled to the log2 domain and
-        // masked by the tile's per-row visibility bits when it is only partly visible
-        auto qk = [&](int stg, int flag, float (&sc)[SH::kNT][4]) {
-            const uint32_t sk = smem_u32(smem + stg * kStageBytes);
+        // S = Q K^T over this warp's keys of stage stg (F16 K tile at sk, or q8_0 codes and
+        // scales), scaled to the log2 domain and masked by the stage's per-row visibility
+        // bits when flag == 2.  nvalid: slots of the tile below kv_total.
+        auto qk = [&](uint32_t sk, int flag, int stg, int nvalid, float (&sc)[SH::kNT][4]) {
 #pragma unroll
             for (int n = 0; n < SH::kNT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            if constexpr (Q8) {
+                // n-tile m holds keys key0 + 8m .. +7; this thread's key in it is key0 + 8m + g
+                const uint2 *ksc = reinterpret_cast<const uint2 *>(smem + stg * kStageB + 2 * kTile * 128);
+                uint2 kw[4];
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+                for (int mt = 0; mt < 4; ++mt) {
+                    const int key = key0 + 8 * mt + g;
+                    kw[mt] = key < nvalid ? ksc[key] : make_uint2(0u, 0u);
+                }
+                // one ldmatrix.x4 per 16 dimensions: lane L addresses key key0 + L
+                const uint32_t rowa = sk + (uint32_t)(key0 + lane) * 128u;
+                const int xr = (key0 + lane) & 7;
 #pragma unroll
-                for (int np = 0; np < SH::kNT / 2; ++np) {
-                    const int key = key0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sk + swz(key, ks * 16 + (((lane >> 3) & 1) << 3), kTile), b0, b1, b2, b3);
-                    mma16816(sc[np * 2], qf[ks], b0, b1);
-                    mma16816(sc[np * 2 + 1], qf[ks], b2, b3);
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t w[4];
+                    ldsm_x4(rowa + ((ks ^ xr) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        // scale of block ks / 2 of this key, in both halves
+                        const uint32_t s2 = prmt((ks >> 2) ? kw[mt].y : kw[mt].x, 0u,
+                                                 ((ks >> 1) & 1) ? 0x3232u : 0x1010u);
+                        const uint32_t wx = w[mt] ^ 0x80808080u;
+                        mma16816(sc[mt], qf[ks], q8_pair(wx, 0x5140u, s2), q8_pair(wx, 0x7362u, s2));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+                    for (int np = 0; np < SH::kNT / 2; ++np) {
+                        const int key = key0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(sk + swz(key, ks * 16 + (((lane >> 3) & 1) << 3), kTile), b0, b1, b2, b3);
+                        mma16816(sc[np * 2], qf[ks], b0, b1);
+                        mma16816(sc[np * 2 + 1], qf[ks], b2, b3);
+                    }
                 }
             }
 #pragma unroll
@@ -558,7 +682,8 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[n][e] *= scale_log2;
             if (flag == 2) {
-                const uint64_t w0 = sbits[stg * kMaxQWords + i0], w1 = sbits[stg * kMaxQWords + i1];
+                const uint64_t w0 = sbits[stg * kMaxQWords + i0];
+                const uint64_t w1 = sbits[stg * kMaxQWords + i1];
 #pragma unroll
                 for (int n = 0; n < SH::kNT; ++n)
 #pragma unroll
@@ -570,8 +695,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
         };
         // online softmax (log2 domain) of rows r0 (j = 0) and r1 (j = 1), then O += P V
-        // over the same keys of stage `stg`, then the stage goes back to the producer
-        auto softmax_pv = [&](int stg, float (&sc)[SH::kNT][4]) {
+        // over the same keys of stage stg (F16 V tile at sv, or q8_0 codes and scales);
+        // then the stage barrier `release` hands the stage back to the producer
+        auto softmax_pv = [&](uint32_t sv, uint32_t release, int stg, int nvalid,
+                              float (&sc)[SH::kNT][4]) {
             float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -605,7 +732,6 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     oacc[n][3] *= alpha[1];
                 }
             }
-            const uint32_t sv = smem_u32(smem + stg * kStageBytes) + kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < SH::kKK; ++kk) {
                 uint32_t pa[4];
@@ -614,24 +740,58 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 pa[2] = pack_half2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
                 pa[3] = pack_half2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
                 const int key = key0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                if constexpr (Q8) {
+                    // keys kb + 2c, +1 (k slots 2c, 2c+1) and kb + 2c + 8, +9: their scales
+                    const int kb = key0 + kk * 16;
+                    const uint2 *vsc = reinterpret_cast<const uint2 *>(smem + stg * kStageB + 2 * kTile * 128 + kTile * 8);
+                    const uint2 zero2 = make_uint2(0u, 0u);
+                    const uint2 s0 = kb + 2 * c < nvalid ? vsc[kb + 2 * c] : zero2;
+                    const uint2 s1 = kb + 2 * c + 1 < nvalid ? vsc[kb + 2 * c + 1] : zero2;
+                    const uint2 s2 = kb + 2 * c + 8 < nvalid ? vsc[kb + 2 * c + 8] : zero2;
+                    const uint2 s3 = kb + 2 * c + 9 < nvalid ? vsc[kb + 2 * c + 9] : zero2;
+                    const uint32_t rowv = sv + (uint32_t)key * 128u;
 #pragma unroll
-                for (int dp = 0; dp < 8; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(sv + swz(key, dp * 16 + ((lane >> 4) << 3), kTile), b0, b1, b2, b3);
-                    mma16816(oacc[dp * 2], pa, b0, b1);
-                    mma16816(oacc[dp * 2 + 1], pa, b2, b3);
+                    for (int qp = 0; qp < 4; ++qp) {
+                        // 16-byte chunks 2qp, 2qp+1 (dimensions 32qp .. 32qp+31, scale block
+                        // qp) of keys kb..kb+15, transposed: a thread holds codes of keys
+                        // (2c, 2c+1) at dimensions (2g, 2g+1) of each chunk
+                        uint32_t r[4];
+                        ldsm_x4_t(rowv + (((2 * qp + (lane >> 4)) ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
+                        const uint32_t hs = (qp & 1) ? 0x7632u : 0x5410u;
+                        const uint32_t sA = prmt((qp >> 1) ? s0.y : s0.x, (qp >> 1) ? s1.y : s1.x, hs);
+                        const uint32_t sB = prmt((qp >> 1) ? s2.y : s2.x, (qp >> 1) ? s3.y : s3.x, hs);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            // chunk q = 2qp + h: n-tile 2q takes its even dimensions, 2q+1
+                            // its odd ones (undone where O is written)
+                            const uint32_t wa = r[2 * h] ^ 0x80808080u, wb = r[2 * h + 1] ^ 0x80808080u;
+                            const int q = 2 * qp + h;
+                            mma16816(oacc[2 * q], pa, q8_pair(wa, 0x6240u, sA), q8_pair(wb, 0x6240u, sB));
+                            mma16816(oacc[2 * q + 1], pa, q8_pair(wa, 0x7351u, sA), q8_pair(wb, 0x7351u, sB));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int dp = 0; dp < 8; ++dp) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(sv + swz(key, dp * 16 + ((lane >> 4) << 3), kTile), b0, b1, b2, b3);
+                        mma16816(oacc[dp * 2], pa, b0, b1);
+                        mma16816(oacc[dp * 2 + 1], pa, b2, b3);
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * (kStages + stg));
+            if (lane == 0) mbar_arrive(release);
         };
-
         int it = 0, t = 0, flag = 0;
         while (next_tile(t, flag)) {
-            if (!wait_full(it)) break;
             float sc[SH::kNT][4];
-            qk(it % kStages, flag, sc);
-            softmax_pv(it % kStages, sc);
+            if (!wait_full(it)) break;
+            const int stg = it % kStages;
+            const uint32_t sk = smem_u32(smem + stg * kStageB);
+            const int nvalid = d.kv_total - t * kTile;      // >= 32: kv_total is a multiple of 32
+            qk(sk, flag, stg, nvalid, sc);
+            softmax_pv(sk + (Q8 ? kTile * 128 : kTileBytes), bar0 + 8 * (kStages + stg), stg, nvalid, sc);
             ++it;
         }
 
@@ -733,22 +893,49 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                             const int h = gk * d.group + hh;
                             const float inv = ll > 0.f ? 1.f / ll : 0.f;
                             float *dst = o + (((int64_t)s * d.q_len + i) * d.n_head + h) * kHeadDim;
+                            if constexpr (Q8) {
+                                // n-tiles 2q / 2q+1: even / odd dimensions of 16q .. 16q+15
 #pragma unroll
-                            for (int n = 0; n < 16; ++n) {
-                                const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
-                                const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
-                                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0 * inv, v1 * inv);
+                                for (int q = 0; q < 8; ++q) {
+                                    float v[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int n = 2 * q + (e & 1), x = 2 * j + (e >> 1);
+                                        v[e] = (oacc[n][x] * a0 + xo[(mb * 64 + n * 4 + x) * 32 + lane] * a1) * inv;
+                                    }
+                                    *reinterpret_cast<float4 *>(dst + 16 * q + 4 * c) = make_float4(v[0], v[1], v[2], v[3]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int n = 0; n < 16; ++n) {
+                                    const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
+                                    const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
+                                    *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0 * inv, v1 * inv);
+                                }
                             }
                         }
                     } else {
                         // one of several independent CTAs: partial for the combine kernel
                         const int64_t base = (((int64_t)s * d.n_head_kv + gk) * d.groups + sp) * kRows + r;
                         float *dst = m.part_acc + base * kHeadDim;
+                        if constexpr (Q8) {
 #pragma unroll
-                        for (int n = 0; n < 16; ++n) {
-                            const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
-                            const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
-                            *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0, v1);
+                            for (int q = 0; q < 8; ++q) {
+                                float v[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int n = 2 * q + (e & 1), x = 2 * j + (e >> 1);
+                                    v[e] = oacc[n][x] * a0 + xo[(mb * 64 + n * 4 + x) * 32 + lane] * a1;
+                                }
+                                *reinterpret_cast<float4 *>(dst + 16 * q + 4 * c) = make_float4(v[0], v[1], v[2], v[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int n = 0; n < 16; ++n) {
+                                const float v0 = oacc[n][2 * j] * a0 + xo[(mb * 64 + n * 4 + 2 * j) * 32 + lane] * a1;
+                                const float v1 = oacc[n][2 * j + 1] * a0 + xo[(mb * 64 + n * 4 + 2 * j + 1) * 32 + lane] * a1;
+                                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * c) = make_float2(v0, v1);
+                            }
                         }
                         if (c == 0) m.part_ml[base] = make_float2(mm, ll);
                     }
@@ -837,13 +1024,16 @@ k_attend_combine(RingDims d, RingDev m, float *o) {
 size_t attend_smem_bytes() { return (size_t)Shape<true>::kSmem; }
 
 cudaError_t attend_kernels_init() {
-    cudaError_t e = cudaFuncSetAttribute(k_attend<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_attend<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Shape<true>::kSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attend<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(k_attend<true, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attend<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(k_attend<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Shape<false>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attend<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Shape<false, true>::kSmem);
     return e;
 }
 
@@ -860,7 +1050,7 @@ int attend_cluster_capacity(int cluster) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_attend<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, k_attend<true, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -875,7 +1065,8 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.n_splits, d.n_head_kv, d.n_seq);
     cfg.blockDim = dim3(clustered ? Shape<true>::kThreads : Shape<false>::kThreads);
-    cfg.dynamicSmemBytes = clustered ? Shape<true>::kSmem : Shape<false>::kSmem;
+    cfg.dynamicSmemBytes = clustered ? Shape<true>::kSmem
+                                     : (d.kv_q8 ? Shape<false, true>::kSmem : Shape<false>::kSmem);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -894,9 +1085,12 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     cfg.attrs = attr;
     cfg.numAttrs = na;
     if (clustered)
-        return cudaLaunchKernelEx(&cfg, k_attend<true>, *tm_k, *tm_v, d, m, layer, kind,
+        return cudaLaunchKernelEx(&cfg, k_attend<true, false>, *tm_k, *tm_v, d, m, layer, kind,
                                   scale_log2, q, k_noise, v_noise, o, (int)(preload && pdl));
-    return cudaLaunchKernelEx(&cfg, k_attend<false>, *tm_k, *tm_v, d, m, layer, kind, scale_log2,
+    if (d.kv_q8)
+        return cudaLaunchKernelEx(&cfg, k_attend<false, true>, *tm_k, *tm_v, d, m, layer, kind,
+                                  scale_log2, q, k_noise, v_noise, o, 0);
+    return cudaLaunchKernelEx(&cfg, k_attend<false, false>, *tm_k, *tm_v, d, m, layer, kind, scale_log2,
                               q, k_noise, v_noise, o, 0);
 }
 

@@ -181,13 +181,16 @@ void release(ring_t *r) {
 bool encode_kv_map(CUtensorMap *tm, void *base, const RingDims &d) {
     auto fn = get_encode_fn();
     if (!fn) return false;
-    // dims (innermost first): head_dim, kv_total slots, (seq, layer, kv head) planes
+    // dims (innermost first): head_dim, kv_total slots, (seq, layer, kv head) planes; F16
+    // slots in 64 x 64 boxes, q8_0 codes (one byte each) in 128 x 64 boxes -- 128 bytes wide
+    const cuuint64_t esz = d.kv_q8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.kv_total,
                           (cuuint64_t)d.n_seq * d.n_layer * d.n_head_kv};
-    cuuint64_t strides[2] = {(cuuint64_t)d.head_dim * 2, (cuuint64_t)d.kv_total * d.head_dim * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)d.head_dim * esz, (cuuint64_t)d.kv_total * d.head_dim * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kTile, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+    CUresult res = fn(tm, d.kv_q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      3, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
@@ -324,6 +327,8 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
                     group * p->q_len, kRows);
     if ((int64_t)p->cap + p->q_len + 32 > (int64_t)INT32_MAX / 2)
         return fail(nullptr, RING_EINVAL, "ring_init: cap too large");
+    if (p->kv_format != RING_KV_F16 && p->kv_format != RING_KV_Q8_0)
+        return fail(nullptr, RING_EINVAL, "ring_init: unknown kv_format %d", p->kv_format);
 
     ring_t *r = new dflash_ring();
     RingDims &d = r->d;
@@ -344,6 +349,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     d.n_tiles = (d.kv_total + kTile - 1) / kTile;
     d.n_kinds = p->swa_window > 0 ? 2 : 1;
     d.bulk_chunk = p->bulk_chunk > 0 ? p->bulk_chunk : 1024;
+    d.kv_q8 = p->kv_format == RING_KV_Q8_0 ? 1 : 0;
     r->rope_theta = p->rope_theta;
     r->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
 
@@ -363,7 +369,8 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         delete r;
         return rc;
     }
-    int max_cluster = p->max_cluster > 0 ? p->max_cluster : 16;
+    // q8_0 slots are dequantised by independent CTAs only (the plain attention shape)
+    int max_cluster = d.kv_q8 ? 1 : (p->max_cluster > 0 ? p->max_cluster : 16);
     choose_split(d, sms, max_cluster, p->tiles_per_split);
     {
         // one wave: every CTA (every cluster) of the attention grid resident at once; only
@@ -388,8 +395,15 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
             return rc;                                                           \
         }                                                                        \
     } while (0)
-    ALLOC(m.k, uint16_t, kv_elems);
-    ALLOC(m.v, uint16_t, kv_elems);
+    if (d.kv_q8) {
+        ALLOC(m.kq, int8_t, kv_elems);
+        ALLOC(m.vq, int8_t, kv_elems);
+        ALLOC(m.ks, uint16_t, kv_elems / 32);
+        ALLOC(m.vs, uint16_t, kv_elems / 32);
+    } else {
+        ALLOC(m.k, uint16_t, kv_elems);
+        ALLOC(m.v, uint16_t, kv_elems);
+    }
     ALLOC(m.slot_pos, int32_t, (size_t)d.n_seq * d.cap);
     ALLOC(m.mask, float, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total);
     ALLOC(m.flags, uint8_t, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
@@ -407,8 +421,15 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     auto zero = [&](void *ptr, int val, size_t bytes) {
         if (z == cudaSuccess) z = cudaMemset(ptr, val, bytes);
     };
-    zero(m.k, 0, kv_elems * 2);
-    zero(m.v, 0, kv_elems * 2);
+    if (d.kv_q8) {
+        zero(m.kq, 0, kv_elems);
+        zero(m.vq, 0, kv_elems);
+        zero(m.ks, 0, kv_elems / 32 * 2);
+        zero(m.vs, 0, kv_elems / 32 * 2);
+    } else {
+        zero(m.k, 0, kv_elems * 2);
+        zero(m.v, 0, kv_elems * 2);
+    }
     zero(m.slot_pos, 0xff, (size_t)d.n_seq * d.cap * 4);
     zero(m.mask, 0, (size_t)d.n_seq * d.n_kinds * d.q_len * d.kv_total * 4);
     zero(m.flags, 0, (size_t)d.n_seq * d.n_kinds * d.n_tiles);
@@ -435,7 +456,9 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         return rc;
     }
     for (auto &ev : r->slot_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-    if (!encode_kv_map(&r->tm_k, m.k, d) || !encode_kv_map(&r->tm_v, m.v, d)) {
+    const bool maps_ok = d.kv_q8 ? encode_kv_map(&r->tm_k, m.kq, d) && encode_kv_map(&r->tm_v, m.vq, d)
+                                 : encode_kv_map(&r->tm_k, m.k, d) && encode_kv_map(&r->tm_v, m.v, d);
+    if (!maps_ok) {
         int rc = fail(nullptr, RING_ECUDA, "ring_init: cuTensorMapEncodeTiled failed");
         release(r);
         return rc;
@@ -473,7 +496,8 @@ int ring_get_geometry(const ring_t *r, ring_geometry *g) {
     g->n_splits = d.n_splits;
     g->cluster = d.cluster;
     g->groups = d.groups;
-    g->cache_bytes = 2LL * d.n_layer * d.kv_row * d.kv_total * 2;
+    g->cache_bytes = d.kv_q8 ? 2LL * d.n_layer * d.kv_total * (d.kv_row + d.kv_row / 32 * 2)
+                             : 2LL * d.n_layer * d.kv_row * d.kv_total * 2;
     g->device_bytes = r->device_bytes;
     return RING_OK;
 }
@@ -660,6 +684,7 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
         return RING_OK;
     }
     const RingDims &d = r->d;
+    if (d.kv_q8) return fail(r, RING_EINVAL, "ring_set_producer: not available on a q8_0 ring");
     if (p->hidden <= 0 || p->hidden % 64)
         return fail(r, RING_EINVAL, "ring_set_producer: hidden %d must be a positive multiple of 64",
                     p->hidden);
@@ -966,6 +991,7 @@ int ring_get_tile_flags(ring_t *r, int32_t seq, int32_t mask_kind, uint8_t *out)
 int ring_get_kv(ring_t *r, int32_t seq, int32_t layer, uint16_t *k, uint16_t *v) {
     if (!check_seq(r, seq) || layer < 0 || layer >= r->d.n_layer) return RING_EINVAL;
     const RingDims &d = r->d;
+    if (d.kv_q8) return fail(r, RING_ESTATE, "ring_get_kv: the ring holds q8_0 slots (ring_get_kv_q8)");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_get_kv");
     // device [kv head][slot][head_dim] -> host [slot][kv head * head_dim]
@@ -986,6 +1012,33 @@ int ring_get_kv(ring_t *r, int32_t seq, int32_t layer, uint16_t *k, uint16_t *v)
     return RING_OK;
 }
 
+int ring_get_kv_q8(ring_t *r, int32_t seq, int32_t layer, int8_t *k_codes, uint16_t *k_scales,
+                   int8_t *v_codes, uint16_t *v_scales) {
+    if (!check_seq(r, seq) || layer < 0 || layer >= r->d.n_layer) return RING_EINVAL;
+    const RingDims &d = r->d;
+    if (!d.kv_q8) return fail(r, RING_ESTATE, "ring_get_kv_q8: the ring holds F16 slots");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_get_kv_q8");
+    // device [kv head][slot][x] -> host [slot][kv head * x], x = 128 codes or 4 scales
+    const size_t plane = (size_t)(seq * d.n_layer + layer) * d.n_head_kv;
+    for (int t = 0; t < 4 && e == cudaSuccess; ++t) {
+        void *dst = t == 0 ? (void *)k_codes : t == 1 ? (void *)k_scales : t == 2 ? (void *)v_codes
+                                                                                  : (void *)v_scales;
+        if (!dst) continue;
+        const bool codes = t % 2 == 0;
+        const size_t width = codes ? (size_t)d.head_dim : (size_t)d.head_dim / 32;   // per head
+        const size_t esz = codes ? 1 : 2;
+        const uint8_t *base = codes ? reinterpret_cast<const uint8_t *>(t == 0 ? r->m.kq : r->m.vq)
+                                    : reinterpret_cast<const uint8_t *>(t == 1 ? r->m.ks : r->m.vs);
+        for (int g = 0; g < d.n_head_kv && e == cudaSuccess; ++g)
+            e = cudaMemcpy2D(static_cast<uint8_t *>(dst) + g * width * esz, width * d.n_head_kv * esz,
+                             base + ((plane + g) * d.kv_total) * width * esz, width * esz,
+                             width * esz, d.kv_total, cudaMemcpyDeviceToHost);
+    }
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_get_kv_q8");
+    return RING_OK;
+}
+
 int ring_device_error(ring_t *r, uint32_t *bits) {
     if (!r) return RING_EINVAL;
     uint32_t w = 0;
@@ -1001,10 +1054,12 @@ int ring_device_error(ring_t *r, uint32_t *bits) {
 int ring_describe(const ring_t *r, char *buf, size_t len) {
     if (!r || !buf || !len) return RING_EINVAL;
     const RingDims &d = r->d;
-    const double mib = 2.0 * d.n_layer * d.kv_row * d.kv_total * 2 / 1048576.0;
+    // F16: 2 bytes a value; q8_0: 34 bytes per 32 values (codes + one F16 scale)
+    const double row_bytes = d.kv_q8 ? d.kv_row + d.kv_row / 32 * 2.0 : d.kv_row * 2.0;
+    const double mib = 2.0 * d.n_layer * row_bytes * d.kv_total / 1048576.0;
     snprintf(buf, len,
-             "[draft-kv] ctx-KV ring active: cap=%d kv_total=%d a_step=%d layers=%d f16 cache %.1f MiB",
-             d.cap, d.kv_total, d.a_step, d.n_layer, mib);
+             "[draft-kv] ctx-KV ring active: cap=%d kv_total=%d a_step=%d layers=%d %s cache %.1f MiB",
+             d.cap, d.kv_total, d.a_step, d.n_layer, d.kv_q8 ? "q8_0" : "f16", mib);
     return RING_OK;
 }
 

@@ -56,11 +56,14 @@ struct RingDims {
     int a_step, trash_slot, kv_total, kv_row, group, rows;
     int n_tiles, tiles_per_split, n_splits, n_kinds, bulk_chunk;
     int cluster, groups;
+    int kv_q8;            // slots hold q8_0 blocks (codes + F16 scales) instead of F16
     int single_wave;      // attention grid fits in one wave (all its CTAs resident at once)
 };
 
 struct RingDev {
-    uint16_t *k, *v;
+    uint16_t *k, *v;          // F16 slots [S][L][Hkv][kv_total][128] (F16 rings)
+    int8_t *kq, *vq;          // q8_0 codes, same layout (q8_0 rings)
+    uint16_t *ks, *vs;        // q8_0 F16 scales [S][L][Hkv][kv_total][4]
     int32_t *slot_pos;
     float *mask;
     uint8_t *flags;
@@ -96,6 +99,30 @@ __device__ __forceinline__ float2 rope_rotate(uint16_t x1b, uint16_t x2b, float2
     const float x1 = __half2float(__ushort_as_half(x1b));
     const float x2 = __half2float(__ushort_as_half(x2b));
     return make_float2(fmaf(x1, cs.x, -x2 * cs.y), fmaf(x1, cs.y, x2 * cs.x));
+}
+
+// q8_0 quantisation of 8 values that are one quarter of a 32-value block, the block's
+// four quarters held by lanes 4k .. 4k+3 of a warp: the block maximum by two butterfly
+// shuffles (every lane of the warp calls this, lanes without data pass zeros), scale
+// d = max|x| / 127, codes roundf(x * (1 / d)) (half away from zero), all in float32.
+// Returns the 8 codes packed little-endian and the scale in *d_out.
+__device__ __forceinline__ uint2 q8_quant8(const float (&x)[8], float *d_out) {
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = amax / 127.f;
+    const float id = d > 0.f ? 1.f / d : 0.f;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        int c = (int)roundf(x[e] * id);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        w[e >> 2] |= ((uint32_t)c & 0xffu) << (8 * (e & 3));
+    }
+    *d_out = d;
+    return make_uint2(w[0], w[1]);
 }
 
 // ---- launchers (ring_kernels.cu) ----

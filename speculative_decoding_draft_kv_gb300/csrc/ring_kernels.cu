@@ -28,10 +28,74 @@ __device__ __forceinline__ void rope_table(float2 *cs, int64_t pos, const double
 // F16), V copied.  Called by a whole block after rope_table() for p.  Work item u is
 // (layer, kv head, 8 consecutive pairs); all of a thread's loads are issued before any of
 // its stores, so a row costs one memory round trip instead of one per item.
+// q8_0 slots: the same items; the four items of one 32-value block sit on four
+// consecutive lanes (item u and thread index agree modulo 8), which quantise it together
+// (q8_quant8).  Every thread runs every round so that the shuffles see full warps.
+__device__ void append_row_q8(const RingDims &d, const RingDev &m, int s, int64_t p,
+                              int64_t row, const uint16_t *__restrict__ k_rows,
+                              const uint16_t *__restrict__ v_rows, int64_t n_rows,
+                              const float2 *cs) {
+    const int slot = (int)(p % d.cap);
+    const int hd = d.head_dim, half = hd / 2;
+    const int chunks = half / 8;
+    const int n_items = d.n_layer * d.n_head_kv * chunks;
+    for (int base = 0; base < n_items; base += (int)blockDim.x) {
+        const int u = base + (int)threadIdx.x;
+        const bool ok = u < n_items;
+        const int uu = ok ? u : 0;
+        const int layer = uu / (d.n_head_kv * chunks);
+        const int g = (uu / chunks) % d.n_head_kv, jc = uu % chunks;
+        const int64_t src = ((int64_t)layer * n_rows + row) * d.kv_row + g * hd + jc * 8;
+        uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, va = xa, vb = xa;
+        if (ok) {
+            xa = *reinterpret_cast<const uint4 *>(k_rows + src);
+            xb = *reinterpret_cast<const uint4 *>(k_rows + src + half);
+            va = *reinterpret_cast<const uint4 *>(v_rows + src);
+            vb = *reinterpret_cast<const uint4 *>(v_rows + src + half);
+        }
+        const uint16_t *a16 = reinterpret_cast<const uint16_t *>(&xa);
+        const uint16_t *b16 = reinterpret_cast<const uint16_t *>(&xb);
+        const uint16_t *va16 = reinterpret_cast<const uint16_t *>(&va);
+        const uint16_t *vb16 = reinterpret_cast<const uint16_t *>(&vb);
+        float k1[8], k2[8], v1[8], v2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 r = rope_rotate(a16[e], b16[e], cs[jc * 8 + e]);
+            k1[e] = r.x;
+            k2[e] = r.y;
+            v1[e] = __half2float(__ushort_as_half(va16[e]));
+            v2[e] = __half2float(__ushort_as_half(vb16[e]));
+        }
+        float dk1, dk2, dv1, dv2;
+        const uint2 ck1 = q8_quant8(k1, &dk1), ck2 = q8_quant8(k2, &dk2);
+        const uint2 cv1 = q8_quant8(v1, &dv1), cv2 = q8_quant8(v2, &dv2);
+        if (!ok) continue;
+        const int64_t head = ((int64_t)s * d.n_layer + layer) * d.n_head_kv + g;
+        const int64_t dst = (head * d.kv_total + slot) * hd + jc * 8;
+        *reinterpret_cast<uint2 *>(m.kq + dst) = ck1;
+        *reinterpret_cast<uint2 *>(m.kq + dst + half) = ck2;
+        *reinterpret_cast<uint2 *>(m.vq + dst) = cv1;
+        *reinterpret_cast<uint2 *>(m.vq + dst + half) = cv2;
+        if ((jc & 3) == 0) {
+            const int64_t sb = (head * d.kv_total + slot) * (hd / 32);
+            const int b1 = jc >> 2, b2 = (half >> 5) + (jc >> 2);
+            m.ks[sb + b1] = __half_as_ushort(__float2half_rn(dk1));
+            m.ks[sb + b2] = __half_as_ushort(__float2half_rn(dk2));
+            m.vs[sb + b1] = __half_as_ushort(__float2half_rn(dv1));
+            m.vs[sb + b2] = __half_as_ushort(__float2half_rn(dv2));
+        }
+    }
+    if (threadIdx.x == 0) m.slot_pos[(int64_t)s * d.cap + slot] = (int32_t)p;
+}
+
 __device__ void append_row(const RingDims &d, const RingDev &m, int s, int64_t p,
                            int64_t row, const uint16_t *__restrict__ k_rows,
                            const uint16_t *__restrict__ v_rows, int64_t n_rows,
                            const float2 *cs) {
+    if (d.kv_q8) {
+        append_row_q8(d, m, s, p, row, k_rows, v_rows, n_rows, cs);
+        return;
+    }
     constexpr int kBatch = 4;
     const int slot = (int)(p % d.cap);
     const int hd = d.head_dim, half = hd / 2;
@@ -86,6 +150,23 @@ __device__ void append_row(const RingDims &d, const RingDev &m, int s, int64_t p
 __device__ void pad_row(const RingDims &d, const RingDev &m, int s) {
     const int vec_per_head = d.head_dim / 8;
     const uint4 zero = make_uint4(0, 0, 0, 0);
+    if (d.kv_q8) {                       // all-zero blocks: codes 0, scales 0
+        for (int layer = 0; layer < d.n_layer; ++layer) {
+            const int64_t head0 = ((int64_t)s * d.n_layer + layer) * d.n_head_kv;
+            for (int idx = threadIdx.x; idx < d.n_head_kv * (d.head_dim / 16); idx += blockDim.x) {
+                const int g = idx / (d.head_dim / 16), c = idx % (d.head_dim / 16);
+                const int64_t off = ((head0 + g) * d.kv_total + d.trash_slot) * d.head_dim;
+                reinterpret_cast<uint4 *>(m.kq + off)[c] = zero;
+                reinterpret_cast<uint4 *>(m.vq + off)[c] = zero;
+                if (c == 0) {
+                    const int64_t so = ((head0 + g) * d.kv_total + d.trash_slot) * (d.head_dim / 32);
+                    *reinterpret_cast<uint2 *>(m.ks + so) = make_uint2(0, 0);
+                    *reinterpret_cast<uint2 *>(m.vs + so) = make_uint2(0, 0);
+                }
+            }
+        }
+        return;
+    }
     for (int layer = 0; layer < d.n_layer; ++layer) {
         const int64_t head0 = ((int64_t)s * d.n_layer + layer) * d.n_head_kv;
         for (int idx = threadIdx.x; idx < d.n_head_kv * vec_per_head; idx += blockDim.x) {

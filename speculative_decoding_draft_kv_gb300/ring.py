@@ -25,6 +25,9 @@ RING_ESTATE = -5
 RING_EDEVICE = -6
 RING_MASK_FULL = 0
 RING_MASK_SWA = 1
+RING_KV_F16 = 0
+RING_KV_Q8_0 = 1
+KV_FORMATS = {"f16": RING_KV_F16, "q8_0": RING_KV_Q8_0}
 MASK_KINDS = {"full": RING_MASK_FULL, "swa": RING_MASK_SWA}
 
 # C symbols the header declares (checked by the test-suite against the shared object).
@@ -34,7 +37,7 @@ EXPORTED = (
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
     "ring_last_error", "ring_set_producer", "ring_begin_step_features", "ring_recompute_window",
-    "ring_draft_step",
+    "ring_draft_step", "ring_get_kv_q8",
 )
 
 
@@ -50,7 +53,8 @@ class RingParams(ctypes.Structure):
                 ("n_head", ctypes.c_int32), ("n_layer", ctypes.c_int32),
                 ("rope_theta", ctypes.c_float), ("n_seq", ctypes.c_int32),
                 ("swa_window", ctypes.c_int32), ("bulk_chunk", ctypes.c_int32),
-                ("tiles_per_split", ctypes.c_int32), ("max_cluster", ctypes.c_int32)]
+                ("tiles_per_split", ctypes.c_int32), ("max_cluster", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 class RingGeometry(ctypes.Structure):
@@ -114,6 +118,7 @@ def _load():
         "ring_get_mask": ([vp, i32, i32, vp], ctypes.c_int),
         "ring_get_tile_flags": ([vp, i32, i32, vp], ctypes.c_int),
         "ring_get_kv": ([vp, i32, i32, vp, vp], ctypes.c_int),
+        "ring_get_kv_q8": ([vp, i32, i32, vp, vp, vp, vp], ctypes.c_int),
         "ring_device_error": ([vp, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
         "ring_describe": ([vp, ctypes.c_char_p, ctypes.c_size_t], ctypes.c_int),
         "ring_profile_enable": ([vp, i32], ctypes.c_int),
@@ -188,9 +193,10 @@ def ring_init(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta):
 
 
 def ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16"):
     p = RingParams(cap, q_len, head_dim, n_head_kv, n_head, n_layer, float(rope_theta), n_seq,
-                   swa_window, bulk_chunk, tiles_per_split, max_cluster)
+                   swa_window, bulk_chunk, tiles_per_split, max_cluster,
+                   KV_FORMATS.get(kv_format, kv_format))
     h = ctypes.c_void_p()
     rc = _load().ring_init_ex(ctypes.byref(h), ctypes.byref(p))
     _check(rc, None, "ring_init_ex")
@@ -364,6 +370,20 @@ def ring_get_kv(h, seq, layer):
     return k.view(np.float16), v.view(np.float16)
 
 
+def ring_get_kv_q8(h, seq, layer):
+    """q8_0 rings: (K codes int8 [kv_total, kv_row], K scales float16 [kv_total, kv_row/32],
+    V codes, V scales) in the page's row layout."""
+    g = ring_get_geometry(h)
+    kc = np.empty((g["kv_total"], g["kv_row"]), np.int8)
+    vc = np.empty_like(kc)
+    ks = np.empty((g["kv_total"], g["kv_row"] // 32), np.uint16)
+    vs = np.empty_like(ks)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(_load().ring_get_kv_q8(h, seq, layer, ptr(kc), ptr(ks), ptr(vc), ptr(vs)), h,
+           "ring_get_kv_q8")
+    return kc, ks.view(np.float16), vc, vs.view(np.float16)
+
+
 def ring_device_error(h) -> int:
     bits = ctypes.c_uint32()
     rc = _load().ring_device_error(h, ctypes.byref(bits))
@@ -418,9 +438,10 @@ class Ring:
     """Owning handle around the C entry points (closes itself)."""
 
     def __init__(self, cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16"):
         self.h = ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta,
-                              n_seq, swa_window, bulk_chunk, tiles_per_split, max_cluster)
+                              n_seq, swa_window, bulk_chunk, tiles_per_split, max_cluster,
+                              kv_format)
         self.geometry = ring_get_geometry(self.h)
 
     def rows_needed(self, seq, committed):
@@ -462,6 +483,9 @@ class Ring:
 
     def kv(self, seq, layer):
         return ring_get_kv(self.h, seq, layer)
+
+    def kv_q8(self, seq, layer):
+        return ring_get_kv_q8(self.h, seq, layer)
 
     def device_error(self):
         return ring_device_error(self.h)

@@ -126,14 +126,15 @@ class GpuRun:
     """One CUDA ring plus bookkeeping oracles (slot_pos and masks only) per sequence."""
 
     def __init__(self, w, swa_window=None, tiles_per_split=0, bulk_chunk=0, device="cuda",
-                 max_cluster=0):
+                 max_cluster=0, kv_format="f16"):
         self.w = w
+        self.kv_format = kv_format
         self.swa = w.swa_window if swa_window is None else swa_window
         self.dev = torch.device(device)
         self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                            w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
                            bulk_chunk=bulk_chunk, tiles_per_split=tiles_per_split,
-                           max_cluster=max_cluster)
+                           max_cluster=max_cluster, kv_format=kv_format)
         self.g = self.ring.geometry
         # head_dim 2, one head, one layer: only slot_pos and masks are read from these
         self.book = [orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta,
@@ -203,7 +204,7 @@ class GpuRun:
         return orc.attend_dense(int(self.committed[seq]), w.cap, self.rows.fn(seq, layer),
                                 q.numpy(), kn.numpy(), vn.numpy(), w.head_dim, w.n_head_kv,
                                 w.n_head, w.rope_theta, kind=kind, swa_window=self.swa,
-                                heads=heads)
+                                heads=heads, kv_format=self.kv_format)
 
     def check_slots_and_masks(self, seqs=None):
         for s in (range(self.w.n_seq) if seqs is None else seqs):
@@ -234,6 +235,42 @@ class GpuRun:
         assert ok and inexact <= 0.01 * want_k.size, inexact
         assert np.all(k[self.g["trash_slot"]] == 0) and np.all(v[self.g["trash_slot"]] == 0)
         return inexact
+
+
+    def check_kv_slots_q8(self, seq, layer, slots):
+        """q8_0 rings: sampled slots' codes and scales against the oracle's quantisation of
+        the rows regenerated by position (V exact; K within q8_k_within)."""
+        w = self.w
+        kc, ks, vc, vs = self.ring.kv_q8(seq, layer)
+        sp = self.book[seq].slot_pos
+        slots = [s for s in slots if sp[s] >= 0]
+        pos = np.array([sp[s] for s in slots], np.int64)
+        t = self.g["trash_slot"]
+        assert not kc[t].any() and not vc[t].any()
+        assert not ks[t].view(np.uint16).any() and not vs[t].view(np.uint16).any()
+        if not len(pos):
+            return 0
+        kr, vr = self.rows.rows(seq, layer, pos)
+        wkc, wks = orc.q8_0_quantize(orc.rope_rows(kr.astype(np.float64), pos, w.n_head_kv,
+                                                   w.head_dim, w.rope_theta))
+        wvc, wvs = orc.q8_0_quantize(vr)
+        np.testing.assert_array_equal(vc[slots], wvc)
+        np.testing.assert_array_equal(vs[slots].view(np.uint16), wvs.view(np.uint16))
+        return q8_k_within(kc[slots], ks[slots], wkc, wks)
+
+
+def q8_k_within(kc, ks, want_kc, want_ks, frac=0.01):
+    """K codes and scales of a q8_0 ring against the oracle's.  The GPU rotates in float32
+    with CUDA's sin/cos and the oracle in float64, so a rotated value can differ in its
+    last float32 bits: a block maximum, and so its scale, may move by one F16 ulp and a
+    code sitting on a rounding boundary by one.  Returns the number of differing codes
+    (at most `frac` of all)."""
+    dc = np.abs(kc.astype(np.int32) - want_kc.astype(np.int32))
+    assert dc.max(initial=0) <= 1, int(dc.max())
+    assert f16_ulp_diff(ks, want_ks).max(initial=0) <= 1
+    n = int((dc != 0).sum())
+    assert n <= frac * kc.size, (n, kc.size)
+    return n
 
 
 def expected_tile_flags(mask, tile):
