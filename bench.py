@@ -37,14 +37,14 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_129_600, "kernel": "564f47ae5c6c7fe4",
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_129_600, "kernel": "9fdbf77a0a1ff409",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
 }
 
 
 # the same for the context-row producer kernel (workload: steady decode, hidden 4096)
 PRODUCE_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 86_200_000, "kernel": "4ec87acbdf3473a9",
+    "steady_decode_cap4096_s1_l5": {"bytes": 86_200_000, "kernel": "ecdda39866f4caf2",
                                     "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
 }
 
@@ -499,8 +499,10 @@ def run_gb300(args):
             torch.cuda.synchronize()
             ms_leg = max_over_ranks(ms_of(evs), dist, dev) / max(1, n6 - min(W, n6))
             assert ring.device_error() == 0
+            ring.close()
+            ring = prod_ring()                 # a fresh ring: committed never goes back
             R.ring_profile_enable(ring.h, True)
-            timed_loop(ring, step_legacy, 1 + n6, max(1, min(20, len(P.plan) - 1 - n6)))
+            timed_loop(ring, step_legacy, 1, min(20, n6))
             torch.cuda.synchronize()
             pl = R.ring_profile_read(ring.h)["produce"]
             ring.close()
