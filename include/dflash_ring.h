@@ -286,8 +286,11 @@ int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q,
  * is captured on the first call and replayed on later ones as long as k_rows, v_rows,
  * n_rows, mask_kind and the layer pointers stay the same (a change re-captures it).  The
  * per-step values (committed counts, row offsets) are staged to the device before the
- * replay; bulk-append chunks, when a sequence needs them, run just before it.  Results
- * equal those of the separate calls.  Errors: as ring_begin_step and ring_attend.
+ * replay; bulk-append chunks, when a sequence needs them, run just before it.  Every
+ * layer's inputs are complete when the call is made, so the layers after the first read
+ * their queries and noise rows while the previous layer is still running: no o[l] may
+ * alias any layer's q, k_noise or v_noise.  Results equal those of the separate calls.
+ * Errors: as ring_begin_step and ring_attend.
  */
 int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
               const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,

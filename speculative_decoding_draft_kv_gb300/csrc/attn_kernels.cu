@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(Shape<CLUSTER, Q8>::kThreads, Shape<CLUSTER, Q
 k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          RingDims d, RingDev m, int layer, int kind, float scale_log2,
          const float *__restrict__ q, const uint16_t *__restrict__ k_noise,
-         const uint16_t *__restrict__ v_noise, float *__restrict__ o, int preload) {
+         const uint16_t *__restrict__ v_noise, float *__restrict__ o, int early) {
     using SH = Shape<CLUSTER, Q8>;
     constexpr int CW = SH::CW;
     constexpr int kStageB = SH::kStageBytesT;
@@ -371,7 +371,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     prefetch_l2(base + ((int64_t)s * d.q_len + i) * d.kv_row + gk * kHeadDim + 64);
                 }
         }
-        if (preload) {
+        if (early & kAttendPreload) {
             // The kernel before this one (an attention kernel of another layer, or one
             // that does not overlap this grid at all) writes none of this layer's context
             // tiles, flags or bits, so the first stages can be filled before the grid
@@ -430,8 +430,13 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         if constexpr (CLUSTER) cluster_wait();
     } else {
         // ---------------- consumers ----------------
-        pdl_wait();   // ring state written by begin_step (and earlier kernels) is visible
-        if (d.single_wave) pdl_trigger();
+        // ring state written by begin_step (and earlier kernels) is visible after the grid
+        // dependency; inputs complete before the previous kernel may be read before it
+        const bool inputs_ready = (early & kAttendInputsReady) != 0;
+        if (!inputs_ready) {
+            pdl_wait();
+            if (d.single_wave) pdl_trigger();
+        }
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
@@ -569,6 +574,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         bar_arrive(2, SH::kThreads);
+        if (inputs_ready) {
+            pdl_wait();
+            if (d.single_wave) pdl_trigger();
+        }
         bar_sync(1, SH::kConsumers);
 
         const int mb = warp & 1, ksl = warp >> 1;
@@ -1060,7 +1069,8 @@ int attend_cluster_capacity(int cluster) {
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
                           const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
-                          float *o, bool pdl, bool preload, cudaStream_t st) {
+                          float *o, bool pdl, int early, cudaStream_t st) {
+    if (!pdl) early = 0;
     const bool clustered = d.cluster > 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.n_splits, d.n_head_kv, d.n_seq);
@@ -1086,7 +1096,7 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     cfg.numAttrs = na;
     if (clustered)
         return cudaLaunchKernelEx(&cfg, k_attend<true, false>, *tm_k, *tm_v, d, m, layer, kind,
-                                  scale_log2, q, k_noise, v_noise, o, (int)(preload && pdl));
+                                  scale_log2, q, k_noise, v_noise, o, early);
     if (d.kv_q8)
         return cudaLaunchKernelEx(&cfg, k_attend<false, true>, *tm_k, *tm_v, d, m, layer, kind,
                                   scale_log2, q, k_noise, v_noise, o, 0);

@@ -85,6 +85,7 @@ struct dflash_ring {
     GraphKey graph_key;
     int64_t graph_kernels = 0;
     bool last_was_begin = false;   // the ring's last kernel launch was the begin-step kernel
+    bool inputs_ready = false;     // layer inputs complete before the step (ring_step capture)
     // context-row producer (ring_set_producer): weights repacked into ring-owned tiles
     bool has_producer = false;
     int hidden = 0;
@@ -628,12 +629,14 @@ cudaError_t launch_layer(ring_t *r, int32_t layer, int32_t mask_kind, const floa
     const auto *kn = static_cast<const uint16_t *>(k_noise);
     const auto *vn = static_cast<const uint16_t *>(v_noise);
     // preloading before the grid dependency is safe unless the ring's previous launch was
-    // the begin-step kernel, which writes context rows, flags and bits
+    // the begin-step kernel, which writes context rows, flags and bits (and the RoPE table
+    // that the query prologue reads)
     const bool preload = !r->last_was_begin;
+    const int early = preload ? (kAttendPreload | (r->inputs_ready ? kAttendInputsReady : 0)) : 0;
     r->last_was_begin = false;
     cudaError_t e = timed(r, 2, cs, [&] {
         return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q, kn, vn,
-                             o, pdl, preload, cs);
+                             o, pdl, early, cs);
     });
     if (e == cudaSuccess && d.groups > 1)
         e = timed(r, 3, cs, [&] { return launch_attend_combine(d, r->m, o, cs); });
@@ -921,8 +924,10 @@ int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const voi
             const auto *vr = static_cast<const uint16_t *>(v_rows);
             cudaError_t le = launch_begin_step(d, r->m, kr, vr, n_rows, true, r->cap_stream);
             r->last_was_begin = true;
+            r->inputs_ready = true;        // every layer's inputs exist before the graph runs
             for (int l = 0; l < d.n_layer && le == cudaSuccess; ++l)
                 le = launch_layer(r, l, mask_kind, q[l], k_noise[l], v_noise[l], o[l], true, r->cap_stream);
+            r->inputs_ready = false;
             cudaGraph_t graph = nullptr;
             e = cudaStreamEndCapture(r->cap_stream, &graph);
             if (le != cudaSuccess) e = le;

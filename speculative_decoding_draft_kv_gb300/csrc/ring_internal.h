@@ -207,14 +207,18 @@ cudaError_t attend_kernels_init();   // per device, before the first launch
 // clusters of `cluster` CTAs that can be resident at once (0 if none)
 int attend_cluster_capacity(int cluster);
 // scale_log2 = log2(e) / sqrt(head_dim): the softmax runs in base 2.
-// preload: the kernel may fill its first pipeline stages before its grid dependency
-// resolves -- only valid when the kernel launched just before it (if it overlaps at all)
-// writes none of this layer's context K/V, flags or visibility bits (so: not right after
-// the begin-step kernel).
+// early (bit mask, with pdl only): kAttendPreload -- the kernel may fill its first
+// pipeline stages before its grid dependency resolves, valid when the kernel launched just
+// before it (if it overlaps at all) writes none of this layer's context K/V, flags or
+// visibility bits (so: not right after the begin-step kernel); kAttendInputsReady -- the
+// queries, the noise rows and the step's RoPE table were complete before the previous
+// kernel started, so the query prologue and the noise-row stores may run before the grid
+// dependency too (the layers after the first inside ring_step).
+constexpr int kAttendPreload = 1, kAttendInputsReady = 2;
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
                           const float *q, const uint16_t *k_noise, const uint16_t *v_noise,
-                          float *o, bool pdl, bool preload, cudaStream_t st);
+                          float *o, bool pdl, int early, cudaStream_t st);
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,
                                   cudaStream_t st);
 size_t attend_smem_bytes();

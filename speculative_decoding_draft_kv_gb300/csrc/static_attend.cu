@@ -226,7 +226,7 @@ extern "C" int ring_attend_static(const ring_attend_static_args *a, void *stream
     if (e == cudaSuccess)
         e = launch_attend(d, m, &tm_k, &tm_v, 0, 0, scale_log2, a->q,
                           static_cast<const uint16_t *>(a->k_noise),
-                          static_cast<const uint16_t *>(a->v_noise), a->o, false, false, st);
+                          static_cast<const uint16_t *>(a->v_noise), a->o, false, 0, st);
     if (e == cudaSuccess && d.groups > 1) e = launch_attend_combine(d, m, a->o, st);
     if (e != cudaSuccess)
         return fail_static(RING_ECUDA, "ring_attend_static: launch: %s", cudaGetErrorString(e));
