@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_129_600, "kernel": "9fdbf77a0a1ff409",
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_130_100, "kernel": "a5715e7f485a39c7",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
 }
 
