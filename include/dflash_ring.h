@@ -85,9 +85,9 @@ typedef struct ring_params {
                                 input; pad rows are all-zero blocks.  (Page
                                 "DFLASH2_RING_PORT.md", section 1.7: the port's draft-KV
                                 size is that of a q8_0 cache.)  A q8_0 ring attends with
-                                independent CTAs (no clusters), dequantising each tile to F16
-                                in shared memory, and takes its context rows through
-                                ring_begin_step / ring_step only (no producer).              */
+                                independent CTAs (no clusters), turning codes into F16 MMA
+                                operands on the fly; the producer quantises the rows it makes
+                                the same way (V after its F16 rounding).                     */
 } ring_params;
 
 enum { RING_KV_F16 = 0, RING_KV_Q8_0 = 1 };

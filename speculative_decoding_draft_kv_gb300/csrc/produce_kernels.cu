@@ -160,6 +160,27 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
                  : "memory");
 }
 
+// One head's row of a q8_0 slot from a warp: lane holds the values at lane + 32 q4, so
+// 32-value block q4 is one value per lane.  Block maximum by a warp reduction, scale
+// d = max|x| / 127, codes roundf(x * (1 / d)) (half away from zero), all in float32; the
+// scale is stored as F16.  base: the slot's first value (codes and scales share it, the
+// scales at base / 32).
+__device__ __forceinline__ void q8_store_head(int8_t *codes, uint16_t *scales, int64_t base,
+                                              const float (&x)[4], int lane) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float amax = fabsf(x[b]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float dq = amax / 127.f;
+        const float id = dq > 0.f ? 1.f / dq : 0.f;
+        int c = (int)roundf(x[b] * id);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        codes[base + lane + 32 * b] = (int8_t)c;
+        if (lane == 0) scales[base / 32 + b] = __half_as_ushort(__float2half_rn(dq));
+    }
+}
+
 // Grid (ks * m_tiles, heads, layers); clusters of ks CTAs along x when ks > 1.
 // blockIdx.y: K head y (y < n_head_kv), V head y - n_head_kv (y < 2 n_head_kv), else
 // query head y - 2 n_head_kv (noise rows only).  Layer = job.layer0 + blockIdx.z.
@@ -379,7 +400,6 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     if (warp >= kPConsumers / 32 || s_fail) return;
 
     // ---------------- epilogue: rows [rank * rows_per, +rows_per) of the tile ----------
-    const int half = kPN / 2;
     for (int lr = warp; lr < rows_per; lr += kPConsumers / 32) {
         const int r = (int)rank * rows_per + lr;
         if (r >= kPM) break;
@@ -418,6 +438,14 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
         const int slot = (int)(p % d.cap);
         const int64_t base = ((((int64_t)s * d.n_layer + layer) * d.n_head_kv + head) * d.kv_total + slot) * kHeadDim;
         if (is_v) {
+            if (d.kv_q8) {
+                // q8_0 slots: V rounded to F16 first (it is an F16 row), then quantised
+                float x[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) x[q4] = __half2float(__float2half_rn(v[q4]));
+                q8_store_head(m.vq, m.vs, base, x, lane);
+                continue;
+            }
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) m.v[base + lane + 32 * q4] = __half_as_ushort(__float2half_rn(v[q4]));
             continue;
@@ -432,13 +460,20 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) y[q4] = v[q4] * inv * w[lane + 32 * q4];
         // RoPE at p: pairs (i, i + 64) for i = lane and lane + 32
+        float kr[4];                      // rotated values at lane + 32 q4
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
             const int i = lane + 32 * q2;
             const float2 cs = rope_angle_cs(p, m.inv_freq[i]);
             const float x1 = y[q2], x2 = y[q2 + 2];
-            m.k[base + i] = __half_as_ushort(__float2half_rn(fmaf(x1, cs.x, -x2 * cs.y)));
-            m.k[base + i + half] = __half_as_ushort(__float2half_rn(fmaf(x1, cs.y, x2 * cs.x)));
+            kr[q2] = fmaf(x1, cs.x, -x2 * cs.y);
+            kr[q2 + 2] = fmaf(x1, cs.y, x2 * cs.x);
+        }
+        if (d.kv_q8) {
+            q8_store_head(m.kq, m.ks, base, kr, lane);   // quantised straight from the rotation
+        } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) m.k[base + lane + 32 * q4] = __half_as_ushort(__float2half_rn(kr[q4]));
         }
         // section 1.2: slot_pos[slot] = p (the begin-step kernel that follows reads it)
         if (layer == 0 && head == 0 && lane == 0) m.slot_pos[(int64_t)s * d.cap + slot] = (int32_t)p;

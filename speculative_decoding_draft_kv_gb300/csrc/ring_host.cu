@@ -687,7 +687,6 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
         return RING_OK;
     }
     const RingDims &d = r->d;
-    if (d.kv_q8) return fail(r, RING_EINVAL, "ring_set_producer: not available on a q8_0 ring");
     if (p->hidden <= 0 || p->hidden % 64)
         return fail(r, RING_EINVAL, "ring_set_producer: hidden %d must be a positive multiple of 64",
                     p->hidden);

@@ -13,8 +13,8 @@ import torch
 import synth
 from oracle import ring_oracle as orc
 from speculative_decoding_draft_kv_gb300 import ring as R
-from tests.ring_harness import (assert_close, expected_tile_flags, f16_within,
-                                projection_error_bound)
+from tests.ring_harness import (ATOL, REL_L2, assert_close, expected_tile_flags, f16_spacing,
+                                f16_within, projection_error_bound, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +24,14 @@ EPS = 1e-6
 class ProducerRun:
     """A CUDA ring fed by the producer, plus per-sequence bookkeeping oracles."""
 
-    def __init__(self, w, hidden, swa_window=None, tiles_per_split=0):
+    def __init__(self, w, hidden, swa_window=None, tiles_per_split=0, kv_format="f16"):
         self.w, self.hidden = w, hidden
+        self.kv_format = kv_format
         self.swa = w.swa_window if swa_window is None else swa_window
         self.dev = torch.device("cuda")
         self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                            w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
-                           tiles_per_split=tiles_per_split)
+                           tiles_per_split=tiles_per_split, kv_format=kv_format)
         self.g = self.ring.geometry
         cpu = [synth.producer_weights(w.seed, l, w.kv_row, hidden, w.head_dim)
                for l in range(w.n_layer)]
@@ -107,19 +108,29 @@ class ProducerRun:
 
     def check_kv(self, seq, layer, slots=None):
         """K and V of (sampled) filled slots against the oracle's produced rows."""
-        k, v = self.ring.kv(seq, layer)
         sp = self.book[seq].slot_pos
         slots = np.flatnonzero(sp >= 0) if slots is None else np.asarray(
             [s for s in slots if sp[s] >= 0], np.int64)
+        if self.kv_format == "q8_0":
+            return self.check_kv_q8(seq, layer, slots)
+        k, v = self.ring.kv(seq, layer)
         if not len(slots):
             return
         pos = sp[slots]
         w, hd, nh = self.w, self.w.head_dim, self.w.n_head_kv
         x = self.feat(seq, pos)
         v_exact = x @ self.wv[layer].astype(np.float64).T
-        k_pre = x @ self.wk[layer].astype(np.float64).T
         # V: the F16 rounding of a float32 accumulation of exact products
         assert f16_within(v[slots], v_exact, projection_error_bound(x, self.wv[layer])), layer
+        k_exact, bound = self.k_exact_and_bound(x, pos, layer)
+        assert f16_within(k[slots], k_exact, bound), layer
+        t = self.g["trash_slot"]
+        assert np.all(k[t] == 0) and np.all(v[t] == 0)
+
+    def k_exact_and_bound(self, x, pos, layer):
+        """Exact rotated K rows of features x and the bound on the GPU's float32 value."""
+        w, hd, nh = self.w, self.w.head_dim, self.w.n_head_kv
+        k_pre = x @ self.wk[layer].astype(np.float64).T
         # K: the accumulation error carried through the per-head norm and the rotation:
         # e = |dk| / rms + |k| |drms| / rms^2 per element with |drms| <= max |dk| of the
         # head, times max |w|, and a rotation adds two such errors; the float32 norm and
@@ -134,9 +145,36 @@ class ProducerRun:
         e = 2.0 * e.max(axis=-1, keepdims=True) * np.abs(self.kn[layer]).max() + 1.2e-6 * ymax + 1e-7
         k_exact = orc.rope_rows(y, pos, nh, hd, w.rope_theta)
         bound = np.broadcast_to(e, kh.shape).reshape(len(pos), nh * hd)
-        assert f16_within(k[slots], k_exact, bound), layer
+        return k_exact, bound
+
+    def check_kv_q8(self, seq, layer, slots):
+        """q8_0 slots: each read-back value code * scale within its quantisation error of
+        the exact row plus the GPU's own error before quantising.  The GPU decides
+        d = max|x| / 127 and codes round(x / d) on its float32 value x (K straight from the
+        rotation, V after its F16 rounding) and stores d as F16, so |code * d16 - exact| <=
+        d / 2 + 127 |d16 - d| + |x - exact|, with d <= d16 + ulp(d16) / 2."""
+        kc, ks, vc, vs = self.ring.kv_q8(seq, layer)
         t = self.g["trash_slot"]
-        assert np.all(k[t] == 0) and np.all(v[t] == 0)
+        assert not kc[t].any() and not vc[t].any()
+        assert not ks[t].view(np.uint16).any() and not vs[t].view(np.uint16).any()
+        if not len(slots):
+            return
+        pos = self.book[seq].slot_pos[slots]
+        x = self.feat(seq, pos)
+
+        def read_back(codes, scales):
+            sc = np.repeat(scales.astype(np.float64), orc.Q8_BLOCK, axis=-1)
+            u = np.repeat(f16_spacing(scales.astype(np.float64)), orc.Q8_BLOCK, axis=-1)
+            return codes.astype(np.float64) * sc, 0.5 * (sc + 0.5 * u) * (1 + 1e-4) + 63.5 * u
+
+        v_exact = x @ self.wv[layer].astype(np.float64).T
+        pv = projection_error_bound(x, self.wv[layer])
+        got, qb = read_back(vc[slots], vs[slots])
+        ev = pv + f16_spacing(np.abs(v_exact) + pv)
+        assert np.all(np.abs(got - v_exact) <= qb + ev + 1e-12), layer
+        k_exact, bound = self.k_exact_and_bound(x, pos, layer)
+        got, qb = read_back(kc[slots], ks[slots])
+        assert np.all(np.abs(got - k_exact) <= qb + bound + 1e-12), layer
 
     def attend(self, step, layer, kind):
         w = self.w
@@ -161,7 +199,37 @@ class ProducerRun:
         return orc.attend_dense(int(self.committed[seq]), w.cap,
                                 lambda pos: self.rows(seq, layer, pos), q.numpy(), kn.numpy(),
                                 vn.numpy(), w.head_dim, w.n_head_kv, w.n_head, w.rope_theta,
-                                kind=kind, swa_window=self.swa, heads=heads)
+                                kind=kind, swa_window=self.swa, heads=heads,
+                                kv_format=self.kv_format)
+
+    def q8_step_allowance(self, seq, layer, q, k_noise, v_noise):
+        """Extra max-abs allowance for attention over q8_0 rows made on the GPU.  The GPU
+        quantises its float32 rows and the oracle its float64 rows; where the two straddle
+        a rounding boundary a code differs by one (the slot checks bound this).  One V code
+        one step away moves an output by at most that step (weights are at most 1); one K
+        code moves a score by scale * |q_j| * d_k and an output by at most that times
+        2 max|v|.  Steps, |q| (after rotation, <= sqrt(2) max|q|) and |v| are the oracle's."""
+        w, c = self.w, int(self.committed[seq])
+        pos = np.arange(c - min(c, w.cap), c)
+        k_pre, v = self.rows(seq, layer, pos)
+        keys = [orc.rope_rows(k_pre, pos, w.n_head_kv, w.head_dim, w.rope_theta),
+                orc.rope_rows(np.asarray(k_noise, np.float64), c + np.arange(w.q_len),
+                              w.n_head_kv, w.head_dim, w.rope_theta)]
+        vals = [np.asarray(v, np.float64), np.asarray(v_noise, np.float64)]
+        dk = max(float(orc.q8_0_quantize(x)[1].astype(np.float64).max()) for x in keys if x.size)
+        dv = max(float(orc.q8_0_quantize(x)[1].astype(np.float64).max()) for x in vals if x.size)
+        vmax = max(float(np.abs(x).max()) for x in vals if x.size)
+        qmax = np.sqrt(2.0) * float(np.abs(q).max())
+        return dv + 2.0 * vmax * qmax * dk / np.sqrt(w.head_dim)
+
+
+def assert_close_q8(got, want, allowance, what=""):
+    """The attention bar (max-abs 2e-3, relative L2 1e-3) with the max-abs bar widened by
+    the one-step allowance of q8_0 rows quantised on two sides; relative L2 unchanged."""
+    err = float(np.abs(got - want).max())
+    rl2 = rel_l2(got, want)
+    assert err <= ATOL + allowance and rl2 <= REL_L2, \
+        f"{what}: max abs {err:.3g} (allowed {ATOL + allowance:.3g}), rel L2 {rl2:.3g}"
 
 
 def test_feature_and_weight_generators_bit_identical_on_gpu():
@@ -305,8 +373,8 @@ def test_legacy_window_recompute_equals_the_ring():
 class DraftRun(ProducerRun):
     """ProducerRun plus the query projection, for ring_draft_step."""
 
-    def __init__(self, w, hidden, pattern):
-        super().__init__(w, hidden)
+    def __init__(self, w, hidden, pattern, kv_format="f16"):
+        super().__init__(w, hidden, kv_format=kv_format)
         self.pattern = pattern
         qw = [synth.query_weights(w.seed, l, w.n_head * w.head_dim, hidden, w.head_dim)
               for l in range(w.n_layer)]
@@ -352,16 +420,24 @@ class DraftRun(ProducerRun):
         self.committed = committed.copy()
         return [x.cpu().numpy() for x in o]
 
-    def expected_draft(self, t, layer, seq, heads=None):
+    def noise_qkv(self, t, layer, seq):
         w = self.w
         h = synth.noise_hidden(w.seed, t, seq, layer, w.q_len, self.hidden, w.sigma).numpy()
-        q, kn, vn = orc.project_noise(h, self.wq[layer], self.wk[layer], self.wv[layer],
-                                      self.qn[layer], self.kn[layer], EPS, w.n_head,
-                                      w.n_head_kv, w.head_dim)
+        return orc.project_noise(h, self.wq[layer], self.wk[layer], self.wv[layer],
+                                 self.qn[layer], self.kn[layer], EPS, w.n_head,
+                                 w.n_head_kv, w.head_dim)
+
+    def draft_allowance(self, t, layer, seq):
+        q, kn, vn = self.noise_qkv(t, layer, seq)
+        return self.q8_step_allowance(seq, layer, q, kn, vn)
+
+    def expected_draft(self, t, layer, seq, heads=None):
+        w = self.w
+        q, kn, vn = self.noise_qkv(t, layer, seq)
         return orc.attend_dense(int(self.committed[seq]), w.cap,
                                 lambda pos: self.rows(seq, layer, pos), q, kn, vn, w.head_dim,
                                 w.n_head_kv, w.n_head, w.rope_theta, kind=self.pattern[layer],
-                                swa_window=self.swa, heads=heads)
+                                swa_window=self.swa, heads=heads, kv_format=self.kv_format)
 
 
 def test_draft_step_small_rings_mixed_pattern():
@@ -407,5 +483,74 @@ def test_draft_step_needs_query_weights():
         with pytest.raises(R.RingError) as e:
             run.ring.draft_step([0], None, [0], [0], h, ["full"], o)
         assert e.value.code == R.RING_ESTATE
+    finally:
+        run.close()
+
+
+def test_q8_small_rings_full_state():
+    """q8_0 rings fed by the producer: two sequences, fold-in, bulk and a jump past the
+    ring; every filled slot of every layer within its derived bound, both masks, and
+    attention against the dense window of the oracle's produced rows, quantised."""
+    w = synth.workload(1, n_layer=2, n_seq=2, swa_window=24)
+    run = ProducerRun(w, 256, kv_format="q8_0")
+    try:
+        sched = [[5, 0], [12, 9], [40, 30], [41, 200], [60, 207], [140, 215], [149, 216]]
+        for t, c in enumerate(sched):
+            run.begin_step(c)
+            run.check_state()
+            for s in range(w.n_seq):
+                for layer in range(w.n_layer):
+                    run.check_kv(s, layer)
+            for kind in ("full", "swa"):
+                layer = t % 2
+                o = run.attend(t, layer, kind)
+                for s in range(w.n_seq):
+                    q = synth.query_block(w.seed, t, s, layer, w.q_len, w.n_head, w.head_dim, w.sigma)
+                    kn, vn = synth.noise_rows(w.seed, t, s, layer, w.q_len, w.kv_row, w.sigma)
+                    allow = run.q8_step_allowance(s, layer, q.numpy(), kn.numpy(), vn.numpy())
+                    assert_close_q8(o[s], run.expected(t, layer, kind, s), allow,
+                                    f"step {t} seq {s} {kind}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_q8_draft_step_small_rings_mixed_pattern():
+    """ring_draft_step on q8_0 rings (context rows quantised by the producer, noise rows by
+    the attention), a full / SWA / full pattern; every output against the float64 route."""
+    w = synth.workload(1, n_layer=3, n_seq=2, swa_window=24)
+    run = DraftRun(w, 192, ["full", "swa", "full"], kv_format="q8_0")
+    try:
+        for t, c in enumerate([[5, 0], [14, 9], [60, 41], [63, 200], [150, 205]]):
+            outs = run.step(t, c)
+            run.check_state()
+            for s in range(w.n_seq):
+                run.check_kv(s, t % w.n_layer)
+            for layer in range(w.n_layer):
+                for s in range(w.n_seq):
+                    assert_close_q8(outs[layer][s], run.expected_draft(t, layer, s),
+                                    run.draft_allowance(t, layer, s),
+                                    f"step {t} layer {layer} seq {s}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
+def test_q8_draft_step_full_size():
+    """q8_0 ring, cap 4096, 5 layers, hidden 4096: prefill then decode steps, sampled heads
+    and slots."""
+    w = synth.workload(2)
+    run = DraftRun(w, 4096, ["full"] * w.n_layer, kv_format="q8_0")
+    try:
+        heads = [0, 17, 31]
+        for t, c in enumerate(synth.commit_schedule(w, 2)):
+            outs = run.step(t, c)
+            for layer in (0, 4):
+                want = run.expected_draft(t, layer, 0, heads=heads)
+                assert_close_q8(outs[layer][0][:, heads], want[:, heads],
+                                run.draft_allowance(t, layer, 0), f"step {t} layer {layer}")
+        rng = np.random.default_rng(1)
+        run.check_kv(0, 3, list(rng.choice(w.cap, 48, replace=False)))
+        assert run.ring.device_error() == 0
     finally:
         run.close()

@@ -220,10 +220,6 @@ def test_q8_host_errors():
             r.kv(0, 0)
         kc, ks, vc, vs = r.kv_q8(0, 0)
         assert not kc.any() and not vc.any()
-        wk = torch.zeros((w.n_layer, w.kv_row, 256), dtype=torch.float16, device="cuda")
-        kn = torch.ones((w.n_layer, w.head_dim), dtype=torch.float32, device="cuda")
-        with pytest.raises(R.RingError):
-            r.set_producer(256, 1e-6, wk, wk, kn)
     with R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta) as r:
         with pytest.raises(R.RingError):
             r.kv_q8(0, 0)
