@@ -409,8 +409,7 @@ def run_gb300(args):
     # kernel's own roofline ----
     prod_obj = None
     n_feat_rows = int(sum(int(P.plan[t][3].sum()) for t in range(len(P.plan))))
-    if (args.producer_hidden > 0 and not q8
-            and n_feat_rows * args.producer_hidden * 2 <= (1 << 30)):
+    if args.producer_hidden > 0 and n_feat_rows * args.producer_hidden * 2 <= (1 << 30):
         H = args.producer_hidden
         ws = [synth.producer_weights(w.seed, l, w.kv_row, H, w.head_dim, device=dev)
               for l in range(w.n_layer)]
@@ -464,9 +463,9 @@ def run_gb300(args):
         rows = float(np.mean([int(P.plan[1 + j][3].sum()) for j in range(n5)
                               if int(P.plan[1 + j][3].sum()) > 0] or [0]))
         prod_bytes = (2 * w.n_layer * w.kv_row * H * 2 + rows * H * 2
-                      + rows * w.n_layer * 2 * w.kv_row * 2)
+                      + rows * w.n_layer * 2 * row_bytes)
         prod_ach = prod_bytes / (prod_ms * 1e-3) / 1e9
-        ptr = PRODUCE_TRAFFIC.get(w.name)
+        ptr = PRODUCE_TRAFFIC.get(w.name + ("_q8_0" if q8 else ""))
         prod_traffic = (ptr["bytes"] if ptr and H == 4096
                         and ptr.get("kernel") == _kernel_source_hash("produce_kernels.cu") else None)
         prod_obj = {

@@ -45,7 +45,7 @@ struct Shape {
     static constexpr int CW = CLUSTER ? 8 : 4;      // consumer warps
     static constexpr int kConsumers = CW * 32;
     static constexpr int kThreads = kConsumers + 32;
-    static constexpr int kStages = CLUSTER ? 6 : (Q8 ? 5 : 3);
+    static constexpr int kStages = CLUSTER ? (Q8 ? 10 : 6) : (Q8 ? 5 : 3);
     static constexpr int kSlices = CW / 2;          // key slices per tile
     static constexpr int kKeys = kTile / kSlices;   // keys per warp per tile (32 or 16)
     static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
@@ -53,7 +53,8 @@ struct Shape {
     static constexpr int kMinBlocks = CLUSTER ? 1 : 2;
     // q8_0 slots: a stage holds a tile's K and V codes (two 128 x 64-byte TMA boxes) and
     // their scales (2 x 512 bytes); the consumers turn codes into F16 MMA operands in
-    // registers, so a stage costs 17 KiB instead of 32 and five of them fit
+    // registers, so a stage costs 17 KiB instead of 32 and five (plain) or ten (cluster)
+    // of them fit
     static constexpr int kStageBytesT = Q8 ? 2 * kTile * 128 + 2 * kTile * 8 : kStageBytes;
     static constexpr int kOffQ = kStages * kStageBytesT;  // 1024-aligned (swizzled like K)
     static constexpr int kOffBits = kOffQ + kQBytes;
@@ -70,8 +71,8 @@ struct Shape {
     static_assert(2 * 64 * 32 * 4 + 2 * 2 * 2 * 32 * 4 <= kStages * kStageBytesT,
                   "key-half merge scratch must fit in the idle stage buffers");
     static_assert(kStageBytesT % 1024 == 0, "stages keep TMA boxes 1024-aligned");
-    static_assert(!Q8 || (!CLUSTER && kKeys == 32), "q8_0 operands: plain shape, 32 keys a warp");
     static constexpr int kSmem = 1024 + kOffRecv + (CLUSTER ? kRecvBytes : 0);
+    static_assert(kSmem <= 227 * 1024, "dynamic shared memory of one CTA");
 };
 
 // ---------------------------------------------------------------------------------
@@ -238,6 +239,11 @@ __device__ __forceinline__ uint32_t q8_pair(uint32_t wx, uint32_t sel, uint32_t 
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(h), "r"(0x64806480u));   // 1152, 1152
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(c), "r"(s2));
     return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
@@ -651,26 +657,51 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             if constexpr (Q8) {
                 // n-tile m holds keys key0 + 8m .. +7; this thread's key in it is key0 + 8m + g
                 const uint2 *ksc = reinterpret_cast<const uint2 *>(smem + stg * kStageB + 2 * kTile * 128);
-                uint2 kw[4];
+                uint2 kw[SH::kNT];
 #pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
+                for (int mt = 0; mt < SH::kNT; ++mt) {
                     const int key = key0 + 8 * mt + g;
                     kw[mt] = key < nvalid ? ksc[key] : make_uint2(0u, 0u);
                 }
-                // one ldmatrix.x4 per 16 dimensions: lane L addresses key key0 + L
-                const uint32_t rowa = sk + (uint32_t)(key0 + lane) * 128u;
-                const int xr = (key0 + lane) & 7;
+                // scale of block b of n-tile mt's key, in both halves
+                auto kscale = [&](int mt, int b) {
+                    return prmt((b >> 1) ? kw[mt].y : kw[mt].x, 0u, (b & 1) ? 0x3232u : 0x1010u);
+                };
+                if constexpr (SH::kNT == 4) {
+                    // one ldmatrix.x4 per 16 dimensions: lane L addresses key key0 + L
+                    const uint32_t rowa = sk + (uint32_t)(key0 + lane) * 128u;
+                    const int xr = (key0 + lane) & 7;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t w[4];
-                    ldsm_x4(rowa + ((ks ^ xr) << 4), w[0], w[1], w[2], w[3]);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint32_t w[4];
+                        ldsm_x4(rowa + ((ks ^ xr) << 4), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) {
-                        // scale of block ks / 2 of this key, in both halves
-                        const uint32_t s2 = prmt((ks >> 2) ? kw[mt].y : kw[mt].x, 0u,
-                                                 ((ks >> 1) & 1) ? 0x3232u : 0x1010u);
-                        const uint32_t wx = w[mt] ^ 0x80808080u;
-                        mma16816(sc[mt], qf[ks], q8_pair(wx, 0x5140u, s2), q8_pair(wx, 0x7362u, s2));
+                        for (int mt = 0; mt < 4; ++mt) {
+                            const uint32_t s2 = kscale(mt, ks >> 1);
+                            const uint32_t wx = w[mt] ^ 0x80808080u;
+                            mma16816(sc[mt], qf[ks], q8_pair(wx, 0x5140u, s2), q8_pair(wx, 0x7362u, s2));
+                        }
+                    }
+                } else {
+                    // 16 keys: one ldmatrix.x4 covers both n-tiles and two k steps (the 32
+                    // dimensions of scale block kp)
+                    const int lkey = key0 + 8 * ((lane >> 3) & 1) + (lane & 7);
+                    const uint32_t rowa = sk + (uint32_t)lkey * 128u;
+                    const int xr = lkey & 7;
+#pragma unroll
+                    for (int kp = 0; kp < 4; ++kp) {
+                        uint32_t w[4];
+                        ldsm_x4(rowa + (((2 * kp + (lane >> 4)) ^ xr) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt) {
+                            const uint32_t s2 = kscale(mt, kp);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t wx = w[2 * h + mt] ^ 0x80808080u;
+                                mma16816(sc[mt], qf[2 * kp + h], q8_pair(wx, 0x5140u, s2),
+                                         q8_pair(wx, 0x7362u, s2));
+                            }
+                        }
                     }
                 }
             } else {
@@ -850,17 +881,34 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 const int owner = r / rows_per, lr = r - owner * rows_per;
                 float *acc_row = recv_acc + ((int64_t)rank * rows_per + lr) * kHeadDim;
                 const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
+                if constexpr (Q8) {
+                    // n-tiles 2q / 2q+1 hold the even / odd dimensions of 16q .. 16q+15
 #pragma unroll
-                for (int nn = 0; nn < 16 / SH::kSlices; ++nn) {
-                    const int n = ksl * (16 / SH::kSlices) + nn;
-                    float v0 = 0.f, v1 = 0.f;
+                    for (int qq = 0; qq < 8 / SH::kSlices; ++qq) {
+                        const int q = ksl * (8 / SH::kSlices) + qq;
+                        float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < SH::kSlices; ++k) {
-                        const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
-                        v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
-                        v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
+                        for (int k = 0; k < SH::kSlices; ++k) {
+                            const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                v[e] += wk[k] * x[((2 * q + (e & 1)) * 4 + 2 * j + (e >> 1)) * 32 + lane];
+                        }
+                        st_cluster_v4(a_row + 4u * (16 * q + 4 * c), v[0], v[1], v[2], v[3]);
                     }
-                    st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
+                } else {
+#pragma unroll
+                    for (int nn = 0; nn < 16 / SH::kSlices; ++nn) {
+                        const int n = ksl * (16 / SH::kSlices) + nn;
+                        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                        for (int k = 0; k < SH::kSlices; ++k) {
+                            const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
+                            v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
+                            v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
+                        }
+                        st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
+                    }
                 }
                 if (ksl == 0 && c == 0)
                     st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rows_per + lr), (uint32_t)owner),
@@ -1043,14 +1091,19 @@ cudaError_t attend_kernels_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attend<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Shape<false, true>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attend<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Shape<true, true>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attend<true, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
-int attend_cluster_capacity(int cluster) {
+int attend_cluster_capacity(int cluster, bool q8) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster, 1, 1);
     cfg.blockDim = dim3(Shape<true>::kThreads);
-    cfg.dynamicSmemBytes = Shape<true>::kSmem;
+    cfg.dynamicSmemBytes = q8 ? Shape<true, true>::kSmem : Shape<true>::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;
@@ -1059,7 +1112,9 @@ int attend_cluster_capacity(int cluster) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_attend<true, false>, &cfg) != cudaSuccess) {
+    const cudaError_t e = q8 ? cudaOccupancyMaxActiveClusters(&n, k_attend<true, true>, &cfg)
+                             : cudaOccupancyMaxActiveClusters(&n, k_attend<true, false>, &cfg);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1075,7 +1130,7 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.n_splits, d.n_head_kv, d.n_seq);
     cfg.blockDim = dim3(clustered ? Shape<true>::kThreads : Shape<false>::kThreads);
-    cfg.dynamicSmemBytes = clustered ? Shape<true>::kSmem
+    cfg.dynamicSmemBytes = clustered ? (d.kv_q8 ? Shape<true, true>::kSmem : Shape<true>::kSmem)
                                      : (d.kv_q8 ? Shape<false, true>::kSmem : Shape<false>::kSmem);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -1094,6 +1149,9 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
+    if (clustered && d.kv_q8)
+        return cudaLaunchKernelEx(&cfg, k_attend<true, true>, *tm_k, *tm_v, d, m, layer, kind,
+                                  scale_log2, q, k_noise, v_noise, o, early);
     if (clustered)
         return cudaLaunchKernelEx(&cfg, k_attend<true, false>, *tm_k, *tm_v, d, m, layer, kind,
                                   scale_log2, q, k_noise, v_noise, o, early);

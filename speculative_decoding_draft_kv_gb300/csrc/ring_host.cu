@@ -251,7 +251,7 @@ void choose_split(RingDims &d, int sms, int max_cluster, int tps_req) {
         const int tps = std::min(tps_req, d.n_tiles);
         const int ns = (d.n_tiles + tps - 1) / tps;
         d.cluster = std::min(cmax, pow2_floor(ns));
-        while (d.cluster > 1 && attend_cluster_capacity(d.cluster) < 1) d.cluster /= 2;
+        while (d.cluster > 1 && attend_cluster_capacity(d.cluster, d.kv_q8 != 0) < 1) d.cluster /= 2;
         d.groups = (ns + d.cluster - 1) / d.cluster;
         d.tiles_per_split = tps;
         d.n_splits = d.cluster * d.groups;
@@ -259,7 +259,7 @@ void choose_split(RingDims &d, int sms, int max_cluster, int tps_req) {
     }
     // widest cluster whose whole grid (pairs clusters) is resident at once
     int c = std::min(cmax, pow2_ceil(d.n_tiles));
-    while (c > 1 && ((int64_t)attend_cluster_capacity(c) < pairs ||
+    while (c > 1 && ((int64_t)attend_cluster_capacity(c, d.kv_q8 != 0) < pairs ||
                      (int64_t)pairs * c > std::max(sms, 1)))
         c /= 2;
     if (c >= 2 && (d.n_tiles + c - 1) / c <= 128) {
@@ -370,8 +370,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         delete r;
         return rc;
     }
-    // q8_0 slots are dequantised by independent CTAs only (the plain attention shape)
-    int max_cluster = d.kv_q8 ? 1 : (p->max_cluster > 0 ? p->max_cluster : 16);
+    int max_cluster = p->max_cluster > 0 ? p->max_cluster : 16;
     choose_split(d, sms, max_cluster, p->tiles_per_split);
     {
         // one wave: every CTA (every cluster) of the attention grid resident at once; only
@@ -379,7 +378,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         // that its own later CTAs wait for)
         const int64_t ctas = (int64_t)d.n_splits * d.n_head_kv * d.n_seq;
         if (d.cluster > 1)
-            d.single_wave = ctas / d.cluster <= (int64_t)attend_cluster_capacity(d.cluster) &&
+            d.single_wave = ctas / d.cluster <= (int64_t)attend_cluster_capacity(d.cluster, d.kv_q8 != 0) &&
                             ctas <= std::max(sms, 1);
         else
             d.single_wave = ctas <= 2LL * std::max(sms, 1) ? 1 : 0;

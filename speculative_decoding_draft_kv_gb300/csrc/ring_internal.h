@@ -205,7 +205,7 @@ void set_global_error(const char *msg);
 // ---- launchers (attn_kernels.cu) ----
 cudaError_t attend_kernels_init();   // per device, before the first launch
 // clusters of `cluster` CTAs that can be resident at once (0 if none)
-int attend_cluster_capacity(int cluster);
+int attend_cluster_capacity(int cluster, bool q8);
 // scale_log2 = log2(e) / sqrt(head_dim): the softmax runs in base 2.
 // early (bit mask, with pdl only): kAttendPreload -- the kernel may fill its first
 // pipeline stages before its grid dependency resolves, valid when the kernel launched just

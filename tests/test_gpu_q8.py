@@ -81,7 +81,7 @@ def test_q8_steady_decode_parity_full_size():
     run = GpuRun(w, kv_format="q8_0")
     try:
         g = run.g
-        assert g["cluster"] == 1
+        assert g["cluster"] > 1          # one sequence: the cluster shape
         assert g["cache_bytes"] == 2 * w.n_layer * g["kv_total"] * (w.kv_row + w.kv_row // 32 * 2)
         sched = synth.commit_schedule(w, 6)
         assert run.begin_step(sched[0]) == ["bulk"]
