@@ -37,14 +37,14 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_130_100, "kernel": "a5715e7f485a39c7",
+    "steady_decode_cap4096_s1_l5": {"bytes": 17_120_300, "kernel": "a684f3ab371e7c90",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
 }
 
 
 # the same for the context-row producer kernel (workload: steady decode, hidden 4096)
 PRODUCE_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 86_200_000, "kernel": "ecdda39866f4caf2",
+    "steady_decode_cap4096_s1_l5": {"bytes": 85_043_500, "kernel": "4be0a7000c1f4369",
                                     "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
 }
 
