@@ -29,7 +29,7 @@
  *   - Layouts are row-major, innermost index last.  A K/V "row" is kv_row = head_dim *
  *     n_head_kv F16 values, head-major (the page's [kv_row, kv_total] ggml tensor,
  *     section 1.1).  F16 values travel as uint16_t bit patterns.
- *   - Fast-path limits of this build: head_dim == 128 and (n_head / n_head_kv) * q_len
+ *   - Shape limits of the kernels: head_dim == 128 and (n_head / n_head_kv) * q_len
  *     <= 32; other shapes are rejected with RING_EINVAL.
  */
 #ifndef DFLASH_RING_H
@@ -66,7 +66,7 @@ enum ring_mask_kind {
 typedef struct ring_params {
     int32_t cap;             /* ring capacity in context slots (section 1.1)                 */
     int32_t q_len;           /* noise-block length = draft block size (section 1.1)          */
-    int32_t head_dim;        /* 128 in this build                                            */
+    int32_t head_dim;        /* 128 (the only head size the kernels take)                    */
     int32_t n_head_kv;       /* K/V heads                                                    */
     int32_t n_head;          /* query heads, a multiple of n_head_kv (GQA)                   */
     int32_t n_layer;         /* draft layers sharing the slot map                            */
