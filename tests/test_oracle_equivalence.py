@@ -49,9 +49,9 @@ def _step_rows(w, seq, start, c, source=_context_rows):
     return np.stack(ks), np.stack(vs)
 
 
-def _run_equivalence(w, n_steps, kinds, source=_context_rows):
+def _run_equivalence(w, n_steps, kinds, source=_context_rows, kv_format="f16"):
     r = orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
-                       w.rope_theta, swa_window=w.swa_window)
+                       w.rope_theta, swa_window=w.swa_window, kv_format=kv_format)
     sched = synth.commit_schedule(w, n_steps)
     worst = 0.0
     for t, c in enumerate(sched[:, 0]):
@@ -66,7 +66,8 @@ def _run_equivalence(w, n_steps, kinds, source=_context_rows):
                 o1 = r.attend(layer, q.numpy(), kn.numpy(), vn.numpy(), kind)
                 o2 = orc.attend_dense(c, w.cap, _rows_fn(w, 0, layer, source), q.numpy(), kn.numpy(),
                                       vn.numpy(), w.head_dim, w.n_head_kv, w.n_head,
-                                      w.rope_theta, kind=kind, swa_window=w.swa_window)
+                                      w.rope_theta, kind=kind, swa_window=w.swa_window,
+                                      kv_format=kv_format)
                 worst = max(worst, float(np.abs(o1 - o2).max()))
     return worst
 
@@ -87,6 +88,15 @@ def test_ring_equals_dense_window_with_produced_rows():
     w = synth.workload(3, cap=48, n_layer=2, head_dim=16, n_head_kv=2, n_head=4,
                        extra={"jump_max": 200, "fold_max": 18, "p_jump": 0.3})
     assert _run_equivalence(w, 20, ("full",), _produced_rows(64, 1e-6)) < 1e-12
+
+
+def test_q8_0_ring_equals_dense_window_with_produced_rows_and_jumps():
+    """q8_0 slots (Q1, Q2) with rows from the producer, bulk jumps past the ring and both
+    masks: the ring's state-by-step route and the dense route quantise the same rows the
+    same way, so they agree to float64 rounding."""
+    w = synth.workload(3, cap=64, n_layer=2, head_dim=32, n_head_kv=2, n_head=4, swa_window=20,
+                       extra={"jump_max": 300, "fold_max": 18, "p_jump": 0.3})
+    assert _run_equivalence(w, 16, ("full", "swa"), _produced_rows(64, 1e-6), "q8_0") < 1e-12
 
 
 def test_naive_roll_differs_once_rows_are_evicted():
