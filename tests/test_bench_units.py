@@ -1,0 +1,29 @@
+"""The unit behind bench.py's roofline: the visible K/V rows of one attention launch must be
+exactly the slots the oracle's masks open (ring slots inside the window plus the noise
+block).  CPU only."""
+
+import numpy as np
+import pytest
+
+import bench
+import synth
+from oracle import ring_oracle as orc
+
+
+@pytest.mark.parametrize("cap,swa", [(64, 24), (48, 100), (200, 40)])
+def test_visible_rows_equal_the_slots_the_masks_open(cap, swa):
+    w = synth.workload(1, cap=cap, swa_window=swa)
+    r = orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta, swa_window=swa)
+    for c in [0, 5, 30, 63, 64, 65, 150, 400]:
+        start, n_new = r.rows_needed(c)
+        z = np.zeros((1, n_new, 2), np.float16)
+        r.begin_step(c, z, z, start)
+        for kind in ("full", "swa"):
+            opened = int((r.mask(kind) == 0).any(axis=0).sum())
+            assert bench.visible_rows(w, [c], kind) == opened, (c, kind)
+
+
+def test_visible_rows_sum_over_sequences():
+    w = synth.workload(1, cap=64, swa_window=24)
+    assert bench.visible_rows(w, [0, 10, 100], "full") == (0 + 8) + (10 + 8) + (64 + 8)
+    assert bench.visible_rows(w, [0, 10, 100], "swa") == (0 + 8) + (10 + 8) + (24 + 8)
