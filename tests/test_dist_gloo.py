@@ -45,3 +45,26 @@ def test_two_ranks_shard_and_take_the_slowest_time():
         assert p.exitcode == 0
     assert res[0][0] == [0, 1, 2] and res[1][0] == [3, 4, 5]
     assert res[0][1] == res[1][1] == 20.0
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under a multi-rank launch the reference arm (the oracle on the host) runs on rank 0
+    alone and prints one line; the other ranks exit 0 without work or output."""
+    import json
+    import subprocess
+    base = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()),
+                WORLD_SIZE="2")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "3"]
+    r1 = subprocess.run(cmd, env=dict(base, RANK="1", LOCAL_RANK="1"), capture_output=True,
+                        text=True, timeout=120)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = subprocess.run(cmd, env=dict(base, RANK="0", LOCAL_RANK="0"), capture_output=True,
+                        text=True, timeout=300)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    lines = [x for x in r0.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
