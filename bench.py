@@ -253,7 +253,8 @@ def run_gb300(args):
     def new_ring():
         r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
                    n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
-                   max_cluster=args.max_cluster, kv_format=args.kv_format)
+                   max_cluster=args.max_cluster, kv_format=args.kv_format,
+                   step_split=args.step_split)
         c, row_off, start, _ = P.plan[0]             # prefill (bulk path), untimed
         r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
         torch.cuda.synchronize()
@@ -721,6 +722,9 @@ def main():
     ap.add_argument("--tiles-per-split", type=int, default=0)
     ap.add_argument("--max-cluster", type=int, default=0)
     ap.add_argument("--n-seq", type=int, default=0, help="override the workload's sequence count")
+    ap.add_argument("--step-split", type=int, default=0,
+                    help="ring_step attention: 0 one launch per layer, -1 the persistent "
+                         "whole-step kernel with the widest cluster, >0 its cluster size")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

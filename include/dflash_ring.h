@@ -88,6 +88,14 @@ typedef struct ring_params {
                                 independent CTAs (no clusters), turning codes into F16 MMA
                                 operands on the fly; the producer quantises the rows it makes
                                 the same way (V after its F16 rounding).                     */
+    int32_t step_split;      /* ring_step's attention: 0 = one launch per layer (default);
+                                > 0 = every layer of the step in one persistent kernel, one
+                                thread-block cluster of this many CTAs per sequence x kv
+                                head pair, one CTA per SM (F16 slots, n_layer <= 16, at most
+                                16 CTAs with c * ceil(32 / c) <= 40; refused with EINVAL
+                                when that is not met or a cluster per pair does not fit on
+                                the GPU at once); -1 = that kernel with the widest such
+                                cluster when the pairs are few (else one launch per layer)  */
 } ring_params;
 
 enum { RING_KV_F16 = 0, RING_KV_Q8_0 = 1 };
@@ -106,6 +114,10 @@ typedef struct ring_geometry {
     int64_t cache_bytes;     /* F16 K+V of one sequence: 2 * n_layer * kv_row * kv_total * 2
                                 (section 1.7)                                                */
     int64_t device_bytes;    /* everything ring_init allocated on the device                 */
+    int32_t step_split;      /* CTAs per (sequence, kv head) -- one cluster -- of ring_step's
+                                persistent attention kernel; 0 = ring_step launches each
+                                layer                                                        */
+    int32_t step_ctas;       /* CTAs of that kernel (step_split * n_seq * n_head_kv)         */
 } ring_geometry;
 
 /* Per-kernel timing collected while profiling is on (CUDA events on the launch stream). */
@@ -284,12 +296,20 @@ int ring_attend(ring_t *r, int32_t layer, int32_t mask_kind, const float *q,
  * o[l], layouts as for ring_attend).  The page builds its step graph once and replays it
  * every step, feeding new inputs through dedicated buffers (section 1.5); here the graph
  * is captured on the first call and replayed on later ones as long as k_rows, v_rows,
- * n_rows, mask_kind and the layer pointers stay the same (a change re-captures it).  The
- * per-step values (committed counts, row offsets) are staged to the device before the
- * replay; bulk-append chunks, when a sequence needs them, run just before it.  Every
- * layer's inputs are complete when the call is made, so the layers after the first read
- * their queries and noise rows while the previous layer is still running: no o[l] may
- * alias any layer's q, k_noise or v_noise.  Results equal those of the separate calls.
+ * n_rows, mask_kind, the layer pointers and the kernel clock setting stay the same (a
+ * change re-captures it).  The per-step values (committed counts, row offsets) are staged
+ * to the device before the replay; bulk-append chunks, when a sequence needs them, run
+ * just before it.
+ *
+ * The layers run in order: layer l reads its queries and noise rows only after every
+ * output of layer l-1 is written, so o[l] may serve as a later layer's q.  With few
+ * (sequence, kv head) pairs (ring_geometry.step_split > 0) the attention of all layers is
+ * one persistent kernel (one CTA per SM, launched cooperatively): its CTAs stream every
+ * layer's context K/V tiles ahead while the layers run, and hand over from layer to layer
+ * through counters in device memory with bounded waits (a wait that runs out sets
+ * ring_device_error's bits).  Otherwise each layer is its own launch.  The ring state
+ * afterwards equals that of the separate calls bit for bit; the outputs equal them up to
+ * the order of the softmax merges (the persistent kernel splits the slots differently).
  * Errors: as ring_begin_step and ring_attend.
  */
 int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const void *v_rows,
@@ -319,7 +339,12 @@ int ring_get_kv_q8(ring_t *r, int32_t seq, int32_t layer, int8_t *k_codes, uint1
                    int8_t *v_codes, uint16_t *v_scales);
 
 /* ring_device_error -- synchronise, read and clear the device-side error word.  Returns
- * RING_OK, or RING_EDEVICE with the word's bits stored in *bits (may be NULL). */
+ * RING_OK, or RING_EDEVICE with the word's bits stored in *bits (may be NULL).  Bits: 1 a
+ * consumer's wait for a stage's K/V load ran out, 2 the copy warp's wait for a free stage,
+ * 4 draining the copies in flight, 8 the wait for a layer's noise rows, 16 a wait on other
+ * CTAs of the persistent whole-step kernel.  Every such wait gives up after 2 s; the
+ * kernel then stops its CTA (and, in the whole-step kernel, every other CTA) and returns,
+ * and the outputs of that launch are not valid. */
 int ring_device_error(ring_t *r, uint32_t *bits);
 
 /* ring_describe -- the geometry line the Luce server logs (section 11, Test 4), e.g.
@@ -337,6 +362,36 @@ int ring_profile_read(ring_t *r, ring_profile *out);
 
 /* ring_launch_count -- kernels this ring has launched since ring_init. */
 int64_t ring_launch_count(const ring_t *r);
+
+/*
+ * Kernel clock -- the duration of the ring's attention kernels measured on the device,
+ * inside CUDA graphs too: each launch of the attention kernel (one per layer, or the
+ * persistent whole-step kernel) records, with the GPU's global nanosecond timer, the
+ * earliest moment any of its CTAs passed its grid dependency and the latest moment any
+ * CTA exited; the last CTA out adds the difference to a running sum.  (No counterpart on
+ * the page: it is how the throughput of the kernel inside a replayed step is measured.)
+ *
+ * ring_clock_enable -- on != 0 starts recording with the next launch (ring_step re-captures
+ *   its graph); 0 stops.  Errors: EINVAL.
+ * ring_clock_read -- synchronise, return the summed milliseconds and the number of
+ *   launches recorded since the last read, and reset both.  Either pointer may be NULL.
+ *   Errors: EINVAL, ECUDA.
+ */
+int ring_clock_enable(ring_t *r, int32_t on);
+int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches);
+
+/*
+ * ring_check_bounded_wait -- self-test of the kernels' bounded waits (no counterpart on the
+ * page; the page's code has no device waits).  Launches one small kernel that waits on
+ * something nothing will ever complete -- which = 0: an mbarrier phase no thread arrives
+ * at (the wait the attention kernels use for their TMA stages); which = 1: a device
+ * counter no CTA raises (the wait the persistent whole-step kernel uses between layers)
+ * -- giving up after limit_us microseconds (1 .. 2,000,000).  The kernel then sets the
+ * device error word's bit (1 = a stage load timed out, 16 = a wait on other CTAs timed
+ * out) and returns; read it with ring_device_error.  Enqueued on `stream`.
+ * Errors: EINVAL, ECUDA.
+ */
+int ring_check_bounded_wait(ring_t *r, int32_t which, int32_t limit_us, void *stream);
 
 /*
  * ring_attend_static -- the attention of ring_attend for callers that cannot allocate
@@ -358,7 +413,13 @@ int64_t ring_launch_count(const ring_t *r);
  * that device current); make that first call before any stream capture.  Every call on a
  * device shares the array, so calls that overlap on the GPU race: issue them on one
  * stream.  Shapes whose scratch exceeds 16 MiB, or n_seq above 256, fail with
- * RING_ERANGE.  Errors: EINVAL, ERANGE, ECUDA (message in ring_last_error(NULL)).
+ * RING_ERANGE: the scratch holds 4 bytes of error word, the RoPE table (n_seq * q_len *
+ * head_dim * 4 bytes), one flag byte and q_len (rounded up to even) 8-byte visibility
+ * words per 64-slot tile and sequence, and -- only when the call splits a (sequence, kv
+ * head) over several CTAs, which it does when there are few pairs and halves until the
+ * rest fits -- n_seq * n_head_kv * splits * 16.25 KiB of partial states.  A wait that runs
+ * out inside the kernel is reported by ring_attend_static_device_error.
+ * Errors: EINVAL, ERANGE, ECUDA (message in ring_last_error(NULL)).
  */
 typedef struct ring_attend_static_args {
     int32_t cap, q_len, head_dim, n_head_kv, n_head, n_seq;
@@ -372,6 +433,17 @@ typedef struct ring_attend_static_args {
 } ring_attend_static_args;
 
 int ring_attend_static(const ring_attend_static_args *args, void *stream);
+
+/*
+ * ring_attend_static_device_error -- the device error word of ring_attend_static on the
+ * current device (no counterpart on the page).  The attention kernel gives up a wait that
+ * runs out (2 s) and sets a bit instead of hanging; without a ring handle, this is where a
+ * caller of ring_attend_static learns of it.  Synchronises the device, reads the word --
+ * the bits every call since the last read has set (the same bits as ring_device_error) --
+ * and clears it.  Returns RING_OK, or RING_EDEVICE with the bits in *bits (may be NULL);
+ * ECUDA if the device could not be read.  Allocates nothing.
+ */
+int ring_attend_static_device_error(uint32_t *bits);
 
 /* ring_last_error -- message of the last failing call on r (or of the last failed
  * ring_init or ring_attend_static when r is NULL).  Never NULL. */

@@ -23,6 +23,7 @@
 // stages of codes and scales; the consumers turn the codes straight into F16 MMA operands
 // in registers (no second pass through shared memory).
 #include "ring_internal.h"
+#include "ptx.h"
 
 #include <cuda_fp16.h>
 
@@ -34,7 +35,6 @@ constexpr int kHalfBox = kTileBytes / 2;           // TMA box: 64 slots x 64 col
 constexpr int kStageBytes = 2 * kTileBytes;        // K + V
 constexpr int kQBytes = kRows * kHeadDim * 2;
 constexpr int kBitsPerStage = kMaxQWords * 8;      // visibility words of one tile
-constexpr uint64_t kWaitNs = 2000000000ull;        // bounded waits give up after 2 s
 
 // Two shapes of one kernel.  CLUSTER: 8 consumer warps (4 key slices), 6 stages, one CTA
 // per SM, partial states pushed to the owning CTA of the cluster.  Plain: 4 consumer warps
@@ -75,190 +75,6 @@ struct Shape {
     static_assert(kSmem <= 227 * 1024, "dynamic shared memory of one CTA");
 };
 
-// ---------------------------------------------------------------------------------
-// PTX helpers
-// ---------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of `parity` to complete; false once kWaitNs have passed (or after a
-// hard iteration cap), never an unbounded spin.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitNs) return false;
-    }
-    return false;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// D += A(16x16, row) * B(16x8, col), F16 inputs, F32 accumulation.
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// Byte offset of the 16-byte chunk holding (row r, columns dcol..dcol+7) in a
-// [rows][128] F16 tile kept as two halves (columns 0-63 and 64-127) of `rows_half` rows
-// of 128 bytes each, in the TMA 128-byte swizzle (chunk index xor row mod 8).  The
-// tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint32_t swz(int r, int dcol, int rows_half) {
-    return (uint32_t)((dcol >> 6) * rows_half * 128 + r * 128 +
-                      ((((dcol & 63) >> 3) ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// A CTA may write into a peer's shared memory only once the peer runs: every thread
-// arrives here right after start-up and waits before its first remote store.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-
-
-// Named barriers: 1 = the consumer warps; 2 = the noise rows are in global memory (the
-// consumer warps arrive, the producer warp waits before fetching a tile holding noise
-// slots).  Both are always executed by whole, converged warps.
-__device__ __forceinline__ void bar_sync(int id, int n) {
-    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(int id, int n) {
-    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
-// Two q8_0 codes as an F16 pair times a pair of scales.  `wx` holds four codes with their
-// sign bits flipped (code + 128 as unsigned bytes); `sel` picks two of those bytes and puts
-// 0x64 above each, which as binary16 reads 1024 + (code + 128); subtracting 1152 leaves
-// the code exactly, and one correctly rounded multiply gives code * scale in F16 -- the
-// same value as rounding the exact float32 product.  Explicit .rn keeps the two apart.
-__device__ __forceinline__ uint32_t q8_pair(uint32_t wx, uint32_t sel, uint32_t s2) {
-    const uint32_t h = prmt(wx, 0x64646464u, sel);
-    uint32_t c, r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(h), "r"(0x64806480u));   // 1152, 1152
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(c), "r"(s2));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
-}
 
 // ---------------------------------------------------------------------------------
 // Split-KV attention of one layer.  Grid (n_splits, n_head_kv, n_seq) in clusters of
@@ -437,12 +253,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     } else {
         // ---------------- consumers ----------------
         // ring state written by begin_step (and earlier kernels) is visible after the grid
-        // dependency; inputs complete before the previous kernel may be read before it
-        const bool inputs_ready = (early & kAttendInputsReady) != 0;
-        if (!inputs_ready) {
-            pdl_wait();
-            if (d.single_wave) pdl_trigger();
-        }
+        // dependency
+        pdl_wait();
+        if (d.single_wave) pdl_trigger();
+        if (threadIdx.x == 0 && m.clock) clock_start(m.clock);
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
@@ -580,10 +394,6 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         bar_arrive(2, SH::kThreads);
-        if (inputs_ready) {
-            pdl_wait();
-            if (d.single_wave) pdl_trigger();
-        }
         bar_sync(1, SH::kConsumers);
 
         const int mb = warp & 1, ksl = warp >> 1;
@@ -1000,7 +810,13 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
         }
     }
-    if constexpr (!CLUSTER) return;
+    if constexpr (!CLUSTER) {
+        if (m.clock) {
+            __syncthreads();
+            if (threadIdx.x == 0) clock_stop(m.clock, gridDim.x * gridDim.y * gridDim.z);
+        }
+        return;
+    }
 
     // ---------------- cluster merge: this CTA finishes rows [rank * rows_per, +rows_per) ----
     cluster_sync();     // every partial of this CTA's rows is in its receive buffer
@@ -1038,6 +854,10 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             *reinterpret_cast<float4 *>(m.part_acc + base * kHeadDim + c4) = acc;
             if (c4 == 0) m.part_ml[base] = make_float2(mm, l);
         }
+    }
+    if (m.clock) {
+        __syncthreads();
+        if (threadIdx.x == 0) clock_stop(m.clock, gridDim.x * gridDim.y * gridDim.z);
     }
 }
 

@@ -37,9 +37,10 @@ struct GraphKey {
     int64_t n_rows = -1;
     int kind = -1;
     std::vector<const void *> ptrs;
+    bool clock = false;
     bool operator==(const GraphKey &o) const {
         return k_rows == o.k_rows && v_rows == o.v_rows && n_rows == o.n_rows && kind == o.kind &&
-               ptrs == o.ptrs;
+               ptrs == o.ptrs && clock == o.clock;
     }
 };
 
@@ -81,11 +82,17 @@ struct dflash_ring {
     std::string err = "no error";
     std::vector<void *> allocs;
     cudaStream_t cap_stream = nullptr;
-    cudaGraphExec_t graph_exec = nullptr;
+    // one replayable step graph per staging slot: its begin-step kernel reads that slot
+    cudaGraphExec_t graph_exec[kStagingSlots] = {};
     GraphKey graph_key;
     int64_t graph_kernels = 0;
     bool last_was_begin = false;   // the ring's last kernel launch was the begin-step kernel
-    bool inputs_ready = false;     // layer inputs complete before the step (ring_step capture)
+    // whole-step attention kernel inside ring_step: CTAs per (sequence, kv head), 0 = the
+    // layers are launched one by one; step_pdl: it may overlap the begin-step kernel
+    int step_split = 0;
+    bool step_pdl = true;
+    unsigned long long *clock_buf = nullptr;   // kernel clock words (ring_clock_enable)
+    bool clock_on = false;
     // context-row producer (ring_set_producer): weights repacked into ring-owned tiles
     bool has_producer = false;
     int hidden = 0;
@@ -174,7 +181,8 @@ void release(ring_t *r) {
     for (void *p : {(void *)r->w_packed, (void *)r->k_norm, (void *)r->q_norm, (void *)r->noise_q,
                     (void *)r->noise_k, (void *)r->noise_v})
         if (p) cudaFree(p);
-    if (r->graph_exec) cudaGraphExecDestroy(r->graph_exec);
+    for (auto &ge : r->graph_exec)
+        if (ge) cudaGraphExecDestroy(ge);
     if (r->cap_stream) cudaStreamDestroy(r->cap_stream);
     delete r;
 }
@@ -313,7 +321,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     const int n_seq = p->n_seq > 0 ? p->n_seq : 1;
     if (p->cap <= 0 || p->q_len <= 0 || p->head_dim <= 0 || p->n_head_kv <= 0 ||
         p->n_head <= 0 || p->n_layer <= 0 || p->swa_window < 0 || p->bulk_chunk < 0 ||
-        p->tiles_per_split < 0 || p->max_cluster < 0 || !(p->rope_theta > 0.f))
+        p->tiles_per_split < 0 || p->max_cluster < 0 || p->step_split < -1 || !(p->rope_theta > 0.f))
         return fail(nullptr, RING_EINVAL, "ring_init: every dimension must be positive");
     if (p->n_head % p->n_head_kv)
         return fail(nullptr, RING_EINVAL, "ring_init: n_head %d not a multiple of n_head_kv %d",
@@ -383,6 +391,41 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
         else
             d.single_wave = ctas <= 2LL * std::max(sms, 1) ? 1 : 0;
     }
+    // Whole-step attention (ring_step), on request: every layer runs in one persistent
+    // kernel, one cluster of c CTAs per (sequence, kv head) (one CTA per SM); c given, or
+    // (step_split = -1, with few pairs -- the case the clusters above serve) the widest
+    // cluster of which one per pair is resident at once.  F16 slots, up to
+    // kMaxStepLayers layers.  By default ring_step launches each layer: measured faster
+    // at cap 4096 with one sequence.
+    {
+        const int pairs = d.n_seq * d.n_head_kv;
+        const bool able = p->step_split != 0 && !d.kv_q8 && d.n_layer <= kMaxStepLayers &&
+                          d.n_tiles <= kMaxStepTiles && attend_step_init() == cudaSuccess;
+        auto fits = [&](int c) {
+            return c >= 1 && c <= kMaxStepCluster && c * ((kRows + c - 1) / c) <= kMaxRecvSlots &&
+                   attend_step_capacity(c) >= pairs;
+        };
+        int split = 0;
+        if (able && p->step_split > 0) {
+            if (fits(p->step_split)) split = p->step_split;
+        } else if (able && p->step_split == -1 && d.cluster > 1) {
+            for (int c = std::min(kMaxStepCluster, d.n_tiles); c >= 2 && !split; --c)
+                if (fits(c)) split = c;
+        }
+        if (split > 0) {
+            r->step_split = split;
+            d.step_sync_words = d.n_layer + 1;
+        } else if (p->step_split > 0) {
+            int rc = fail(nullptr, RING_EINVAL,
+                          "ring_init: step_split %d: the whole-step kernel needs F16 slots, at most "
+                          "%d layers and %d tiles, clusters of at most %d CTAs with c * ceil(32 / c) "
+                          "<= %d, and a cluster for each of the %d pairs resident at once",
+                          p->step_split, kMaxStepLayers, kMaxStepTiles, kMaxStepCluster,
+                          kMaxRecvSlots, pairs);
+            delete r;
+            return rc;
+        }
+    }
 
     const size_t kv_elems = (size_t)d.n_seq * d.n_layer * d.n_head_kv * d.kv_total * d.head_dim;
     RingDev &m = r->m;
@@ -414,6 +457,9 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows);
     ALLOC(m.err, uint32_t, 1);
     ALLOC(m.inv_freq, double, d.head_dim / 2);
+    ALLOC(r->clock_buf, unsigned long long, 5);
+    ALLOC(m.probe, uint32_t, 2);
+    if (r->step_split > 0) ALLOC(m.step_sync, uint32_t, d.step_sync_words);
 #undef ALLOC
 
     // zeroed once (section 1.1); slot_pos = -1; masks start fully masked
@@ -437,6 +483,10 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     zero(m.steps, 0, sizeof(SeqStep) * d.n_seq);
     zero(m.rope32, 0, (size_t)d.n_seq * d.q_len * d.head_dim / 2 * sizeof(float2));
     zero(m.err, 0, 4);
+    zero(m.probe, 0, 8);
+    zero(r->clock_buf, 0, 5 * 8);
+    zero(r->clock_buf, 0xff, 8);                 // earliest start: none yet
+    if (m.step_sync) zero(m.step_sync, 0, (size_t)d.step_sync_words * 4);
     std::vector<double> inv(d.head_dim / 2);
     for (int i = 0; i < d.head_dim / 2; ++i)
         inv[i] = std::pow((double)p->rope_theta, -2.0 * i / d.head_dim);
@@ -499,6 +549,8 @@ int ring_get_geometry(const ring_t *r, ring_geometry *g) {
     g->cache_bytes = d.kv_q8 ? 2LL * d.n_layer * d.kv_total * (d.kv_row + d.kv_row / 32 * 2)
                              : 2LL * d.n_layer * d.kv_row * d.kv_total * 2;
     g->device_bytes = r->device_bytes;
+    g->step_split = r->step_split;
+    g->step_ctas = r->step_split * d.n_seq * d.n_head_kv;
     return RING_OK;
 }
 
@@ -573,29 +625,43 @@ int validate_step(ring_t *r, const char *who, const int64_t *committed, const vo
     return RING_OK;
 }
 
-// The step records go to the device through a rotating pinned slot; then the bulk chunks
-// (slot_pos of those slots is read by the begin kernel, which runs after them).
+// The step records go to a rotating pinned host slot (*slot), which the begin-step kernel
+// reads directly -- no copy ahead of its launch; a device copy is made as well when other
+// kernels read the records (bulk chunks, the producer).  Then the bulk chunks (slot_pos of
+// those slots is read by the begin kernel, which runs after them).  The caller marks the
+// slot busy (mark_slot) after the last launch that reads it.
 int stage_and_bulk(ring_t *r, const char *who, const std::vector<SeqStep> &st, const void *k_rows,
-                   const void *v_rows, int64_t n_rows, int64_t max_bulk, cudaStream_t cs) {
+                   const void *v_rows, int64_t n_rows, int64_t max_bulk, cudaStream_t cs, int *slot_out,
+                   bool device_copy = false) {
     const RingDims &d = r->d;
     const int slot = r->slot_next;
     r->slot_next = (slot + 1) % kStagingSlots;
     if (r->slot_used[slot]) {
         cudaError_t e = cudaEventSynchronize(r->slot_ev[slot]);
         if (e != cudaSuccess) return cuda_fail(r, e, who);
+        r->slot_used[slot] = false;
     }
+    *slot_out = slot;
     SeqStep *h = r->h_steps + (size_t)slot * d.n_seq;
     std::memcpy(h, st.data(), sizeof(SeqStep) * d.n_seq);
-    cudaError_t e = cudaMemcpyAsync(r->m.steps, h, sizeof(SeqStep) * d.n_seq, cudaMemcpyHostToDevice, cs);
+    cudaError_t e = cudaSuccess;
+    if (device_copy || max_bulk > 0)
+        e = cudaMemcpyAsync(r->m.steps, h, sizeof(SeqStep) * d.n_seq, cudaMemcpyHostToDevice, cs);
     if (e != cudaSuccess) return cuda_fail(r, e, who);
-    cudaEventRecord(r->slot_ev[slot], cs);
-    r->slot_used[slot] = true;
     const auto *kr = static_cast<const uint16_t *>(k_rows);
     const auto *vr = static_cast<const uint16_t *>(v_rows);
     const int n_chunks = (int)((max_bulk + d.bulk_chunk - 1) / d.bulk_chunk);
     for (int c = 0; c < n_chunks && e == cudaSuccess; ++c)
         e = timed(r, 0, cs, [&] { return launch_bulk_append(d, r->m, kr, vr, n_rows, c, cs); });
     return e == cudaSuccess ? RING_OK : cuda_fail(r, e, who);
+}
+
+const SeqStep *slot_steps(const ring_t *r, int slot) { return r->h_steps + (size_t)slot * r->d.n_seq; }
+
+// The staging slot may be rewritten once everything enqueued so far on cs has run.
+void mark_slot(ring_t *r, int slot, cudaStream_t cs) {
+    cudaEventRecord(r->slot_ev[slot], cs);
+    r->slot_used[slot] = true;
 }
 
 void commit_host(ring_t *r, const int64_t *committed) {
@@ -631,7 +697,7 @@ cudaError_t launch_layer(ring_t *r, int32_t layer, int32_t mask_kind, const floa
     // the begin-step kernel, which writes context rows, flags and bits (and the RoPE table
     // that the query prologue reads)
     const bool preload = !r->last_was_begin;
-    const int early = preload ? (kAttendPreload | (r->inputs_ready ? kAttendInputsReady : 0)) : 0;
+    const int early = preload ? kAttendPreload : 0;
     r->last_was_begin = false;
     cudaError_t e = timed(r, 2, cs, [&] {
         return launch_attend(d, r->m, &r->tm_k, &r->tm_v, layer, mask_kind, r->scale_log2, q, kn, vn,
@@ -656,13 +722,15 @@ int ring_begin_step(ring_t *r, const int64_t *committed, const void *k_rows, con
                            n_rows, st, max_bulk);
     if (rc != RING_OK) return rc;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    rc = stage_and_bulk(r, "ring_begin_step", st, k_rows, v_rows, n_rows, max_bulk, cs);
+    int slot = 0;
+    rc = stage_and_bulk(r, "ring_begin_step", st, k_rows, v_rows, n_rows, max_bulk, cs, &slot);
     if (rc != RING_OK) return rc;
     const auto *kr = static_cast<const uint16_t *>(k_rows);
     const auto *vr = static_cast<const uint16_t *>(v_rows);
     cudaError_t e = timed(r, 1, cs, [&] {
-        return launch_begin_step(r->d, r->m, kr, vr, n_rows, !r->profiling, cs);
+        return launch_begin_step(r->d, r->m, kr, vr, n_rows, !r->profiling, slot_steps(r, slot), cs);
     });
+    mark_slot(r, slot, cs);
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_begin_step: launch");
     r->last_was_begin = true;
     commit_host(r, committed);
@@ -784,15 +852,20 @@ int begin_step_features(ring_t *r, const char *who, const int64_t *committed, co
         e = produce(!r->profiling);
         if (e != cudaSuccess) return cuda_fail(r, e, who);
     }
-    rc = stage_and_bulk(r, who, st, nullptr, nullptr, n_rows, 0, cs);
+    // the producer reads the records from the device only when they are not its
+    // parameters (more sequences than fit there)
+    int slot = 0;
+    rc = stage_and_bulk(r, who, st, nullptr, nullptr, n_rows, 0, cs, &slot, ps.n == 0);
     if (rc != RING_OK) return rc;
     if (ps.n == 0) {
         e = produce(false);
         if (e != cudaSuccess) return cuda_fail(r, e, who);
     }
     e = timed(r, 1, cs, [&] {
-        return launch_begin_step(r->d, r->m, nullptr, nullptr, n_rows, !r->profiling, cs);
+        return launch_begin_step(r->d, r->m, nullptr, nullptr, n_rows, !r->profiling,
+                                 slot_steps(r, slot), cs);
     });
+    mark_slot(r, slot, cs);
     if (e != cudaSuccess) return cuda_fail(r, e, who);
     r->last_was_begin = true;
     commit_host(r, committed);
@@ -892,11 +965,12 @@ int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const voi
                            st, max_bulk);
     if (rc != RING_OK) return rc;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    rc = stage_and_bulk(r, "ring_step", st, k_rows, v_rows, n_rows, max_bulk, cs);
+    int slot = 0;
+    rc = stage_and_bulk(r, "ring_step", st, k_rows, v_rows, n_rows, max_bulk, cs, &slot);
     if (rc != RING_OK) return rc;
 
-    // the fixed-topology step graph: captured once, re-captured only when a pointer the
-    // kernels take as a parameter changes
+    // the fixed-topology step graph: captured once per staging slot, re-captured only when
+    // a pointer the kernels take as a parameter changes
     GraphKey key;
     key.k_rows = k_rows;
     key.v_rows = v_rows;
@@ -908,51 +982,77 @@ int ring_step(ring_t *r, const int64_t *committed, const void *k_rows, const voi
         key.ptrs.push_back(v_noise[l]);
         key.ptrs.push_back(o[l]);
     }
+    key.clock = r->clock_on;
     cudaError_t e = cudaSuccess;
-    if (!r->graph_exec || !(key == r->graph_key)) {
+    if (!(key == r->graph_key)) {
+        for (auto &ge : r->graph_exec)
+            if (ge) cudaGraphExecDestroy(ge);
+        for (auto &ge : r->graph_exec) ge = nullptr;
+        r->graph_key = key;
+    }
+    cudaGraphExec_t &gexec = r->graph_exec[slot];
+    if (!gexec) {
         if (!r->cap_stream) {
             e = cudaStreamCreateWithFlags(&r->cap_stream, cudaStreamNonBlocking);
             if (e != cudaSuccess) return cuda_fail(r, e, "ring_step: capture stream");
         }
         const bool prof = r->profiling;
         r->profiling = false;              // no events inside the graph
-        e = cudaStreamBeginCapture(r->cap_stream, cudaStreamCaptureModeThreadLocal);
-        if (e == cudaSuccess) {
+        // capture: the begin-step kernel, then either the whole-step attention kernel or one
+        // attention launch (+ combine) per layer
+        auto capture = [&]() -> cudaError_t {
+            cudaError_t ce = cudaStreamBeginCapture(r->cap_stream, cudaStreamCaptureModeThreadLocal);
+            if (ce != cudaSuccess) return ce;
             const auto *kr = static_cast<const uint16_t *>(k_rows);
             const auto *vr = static_cast<const uint16_t *>(v_rows);
-            cudaError_t le = launch_begin_step(d, r->m, kr, vr, n_rows, true, r->cap_stream);
+            cudaError_t le = launch_begin_step(d, r->m, kr, vr, n_rows, true, slot_steps(r, slot),
+                                               r->cap_stream);
             r->last_was_begin = true;
-            r->inputs_ready = true;        // every layer's inputs exist before the graph runs
-            for (int l = 0; l < d.n_layer && le == cudaSuccess; ++l)
-                le = launch_layer(r, l, mask_kind, q[l], k_noise[l], v_noise[l], o[l], true, r->cap_stream);
-            r->inputs_ready = false;
-            cudaGraph_t graph = nullptr;
-            e = cudaStreamEndCapture(r->cap_stream, &graph);
-            if (le != cudaSuccess) e = le;
-            if (e == cudaSuccess) {
-                bool updated = false;
-                if (r->graph_exec) {
-                    cudaGraphExecUpdateResultInfo info;
-                    updated = cudaGraphExecUpdate(r->graph_exec, graph, &info) == cudaSuccess;
-                    if (!updated) {
-                        cudaGetLastError();
-                        cudaGraphExecDestroy(r->graph_exec);
-                        r->graph_exec = nullptr;
-                    }
+            if (r->step_split > 0) {
+                StepIO io{};
+                for (int l = 0; l < d.n_layer; ++l) {
+                    io.q[l] = q[l];
+                    io.k_noise[l] = static_cast<const uint16_t *>(k_noise[l]);
+                    io.v_noise[l] = static_cast<const uint16_t *>(v_noise[l]);
+                    io.o[l] = o[l];
                 }
-                if (!updated) e = cudaGraphInstantiate(&r->graph_exec, graph, 0);
+                if (le == cudaSuccess)
+                    le = timed(r, 2, r->cap_stream, [&] {
+                        return launch_attend_step(d, r->m, &r->tm_k, &r->tm_v, mask_kind, r->scale_log2,
+                                                  io, r->step_split, r->step_pdl, r->cap_stream);
+                    });
+                r->last_was_begin = false;
+            } else {
+                for (int l = 0; l < d.n_layer && le == cudaSuccess; ++l)
+                    le = launch_layer(r, l, mask_kind, q[l], k_noise[l], v_noise[l], o[l], true,
+                                      r->cap_stream);
             }
+            cudaGraph_t graph = nullptr;
+            ce = cudaStreamEndCapture(r->cap_stream, &graph);
+            if (le != cudaSuccess) ce = le;
+            if (ce == cudaSuccess) ce = cudaGraphInstantiate(&gexec, graph, 0);
             if (graph) cudaGraphDestroy(graph);
+            return ce;
+        };
+        e = capture();
+        if (e != cudaSuccess && r->step_split > 0 && r->step_pdl) {
+            // a cooperative launch that may not overlap its predecessor: capture it plainly
+            cudaGetLastError();
+            if (gexec) cudaGraphExecDestroy(gexec);
+            gexec = nullptr;
+            r->step_pdl = false;
+            e = capture();
         }
         r->profiling = prof;
         if (e != cudaSuccess) {
-            r->graph_exec = nullptr;
+            if (gexec) cudaGraphExecDestroy(gexec);
+            gexec = nullptr;
             return cuda_fail(r, e, "ring_step: graph capture");
         }
-        r->graph_key = key;
-        r->graph_kernels = 1 + d.n_layer * (d.groups > 1 ? 2 : 1);
+        r->graph_kernels = r->step_split > 0 ? 2 : 1 + d.n_layer * (d.groups > 1 ? 2 : 1);
     }
-    e = timed(r, 4, cs, [&] { return cudaGraphLaunch(r->graph_exec, cs); });
+    e = timed(r, 4, cs, [&] { return cudaGraphLaunch(gexec, cs); });
+    mark_slot(r, slot, cs);
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_step: graph launch");
     r->launches += r->graph_kernels - 1;   // timed() counted the launch itself once
     commit_host(r, committed);
@@ -1091,6 +1191,38 @@ int ring_profile_read(ring_t *r, ring_profile *out) {
 }
 
 int64_t ring_launch_count(const ring_t *r) { return r ? r->launches : 0; }
+
+int ring_clock_enable(ring_t *r, int32_t on) {
+    if (!r) return RING_EINVAL;
+    r->clock_on = on != 0;
+    r->m.clock = r->clock_on ? r->clock_buf : nullptr;
+    return RING_OK;
+}
+
+int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches) {
+    if (!r) return RING_EINVAL;
+    unsigned long long w[5] = {};
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(w, r->clock_buf, sizeof w, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(r->clock_buf + 2, 0, 2 * sizeof(unsigned long long));
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_clock_read");
+    if (total_ms) *total_ms = (double)w[2] * 1e-6;
+    if (launches) *launches = (int64_t)w[3];
+    return RING_OK;
+}
+
+int ring_check_bounded_wait(ring_t *r, int32_t which, int32_t limit_us, void *stream) {
+    if (!r) return RING_EINVAL;
+    if (which != 0 && which != 1)
+        return fail(r, RING_EINVAL, "ring_check_bounded_wait: which must be 0 or 1, got %d", which);
+    if (limit_us < 1 || limit_us > 2000000)
+        return fail(r, RING_EINVAL, "ring_check_bounded_wait: limit %d us outside [1, 2e6]", limit_us);
+    cudaError_t e = launch_wait_probe(r->m, which, (unsigned long long)limit_us * 1000ull,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(r, e, "ring_check_bounded_wait: launch");
+    ++r->launches;
+    return RING_OK;
+}
 
 const char *ring_last_error(const ring_t *r) {
     return r ? r->err.c_str() : g_init_error.c_str();

@@ -15,6 +15,9 @@
 //   part_acc  F32  [n_seq][n_head_kv][groups][32][head_dim]  cluster-group partial numerators
 //   part_ml   F32x2[n_seq][n_head_kv][groups][32]            their (max, sum), log2 units
 //   err       U32  device error word (bounded waits that ran out)
+//   step_sync U32  [n_layer] + 1: the whole-step attention kernel's layer counters and
+//             abort word (few sequences, ring_step), zeroed by every begin_step
+//   clock     U64[5] kernel clock (earliest start, latest end, summed ns, launches, CTAs out)
 //
 // Attention work split: n_splits = cluster * groups CTAs per (sequence, kv head), each
 // streaming tiles_per_split consecutive 64-slot tiles.  The `cluster` CTAs of a group are
@@ -39,6 +42,24 @@ constexpr int kMaxQWords = 32;    // visibility words per tile (q_len <= 32, rou
 constexpr uint32_t kErrWaitFull = 1u;     // consumer timed out on a stage's load
 constexpr uint32_t kErrWaitEmpty = 2u;    // producer timed out on a free stage
 constexpr uint32_t kErrDrain = 4u;        // producer timed out draining loads on abort
+constexpr uint32_t kErrWaitNoise = 8u;    // producer timed out on the layer's noise rows
+constexpr uint32_t kErrWaitPeer = 16u;    // a CTA timed out waiting on other CTAs
+
+// Whole-step attention kernel (every layer in one launch, few sequences).
+constexpr int kMaxStepLayers = 16;   // layers one launch takes
+constexpr int kMaxStepTiles = 2048;  // slot tiles per (sequence, kv head): flags staged in smem
+// Each of the c CTAs of a pair's cluster owns ceil(32 / c) or fewer query rows and receives
+// one state per row from every CTA of the cluster: c * ceil(32 / c) receive slots.
+constexpr int kMaxRecvSlots = 40;
+constexpr int kMaxStepCluster = 16;
+
+// Per-layer inputs and outputs of one step (layouts as for ring_attend).
+struct StepIO {
+    const float *q[kMaxStepLayers];
+    const uint16_t *k_noise[kMaxStepLayers];
+    const uint16_t *v_noise[kMaxStepLayers];
+    float *o[kMaxStepLayers];
+};
 
 struct SeqStep {
     int64_t committed;   // c
@@ -58,6 +79,7 @@ struct RingDims {
     int cluster, groups;
     int kv_q8;            // slots hold q8_0 blocks (codes + F16 scales) instead of F16
     int single_wave;      // attention grid fits in one wave (all its CTAs resident at once)
+    int step_sync_words;  // words of RingDev::step_sync that begin_step zeroes (0: none)
 };
 
 struct RingDev {
@@ -74,6 +96,9 @@ struct RingDev {
     float2 *part_ml;
     uint32_t *err;
     double *inv_freq;     // [head_dim / 2] theta^(-2i/head_dim), computed on the host
+    uint32_t *step_sync;  // whole-step kernel: layer counters + abort word
+    unsigned long long *clock;   // kernel clock while enabled (else NULL)
+    uint32_t *probe;      // two words nothing ever writes (bounded-wait self-test)
 };
 
 // RoPE angle of position p for the pair with inverse frequency f (= theta^(-2i/d)):
@@ -132,10 +157,11 @@ cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16
                                cudaStream_t st);
 // Fold-in append + slot_pos + masks + tile flags + the step's RoPE table, one kernel.
 // pdl: launch with programmatic stream serialization (the kernel waits on its
-// predecessor before touching ring state).
+// predecessor before touching ring state).  host_steps: the step records in pinned host
+// memory, read by the kernel directly (NULL: read m.steps, copied to the device before).
 cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
-                              cudaStream_t st);
+                              const SeqStep *host_steps, cudaStream_t st);
 
 // Row ranges of the producer's packed row list, passed by value (no copy to the device
 // before the launch, so the launch can overlap the previous kernel) when n_seq is small.
@@ -213,7 +239,7 @@ int attend_cluster_capacity(int cluster, bool q8);
 // visibility bits (so: not right after the begin-step kernel); kAttendInputsReady -- the
 // queries, the noise rows and the step's RoPE table were complete before the previous
 // kernel started, so the query prologue and the noise-row stores may run before the grid
-// dependency too (the layers after the first inside ring_step).
+// dependency too.
 constexpr int kAttendPreload = 1, kAttendInputsReady = 2;
 cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
                           const CUtensorMap *tm_v, int layer, int kind, float scale_log2,
@@ -222,5 +248,21 @@ cudaError_t launch_attend(const RingDims &d, const RingDev &m, const CUtensorMap
 cudaError_t launch_attend_combine(const RingDims &d, const RingDev &m, float *o,
                                   cudaStream_t st);
 size_t attend_smem_bytes();
+
+// ---- launchers (step_kernels.cu) ----
+cudaError_t attend_step_init();      // per device, before the first launch
+// clusters of `cluster` CTAs of the whole-step kernel resident at once (0 if none)
+int attend_step_capacity(int cluster);
+size_t attend_step_smem_bytes();
+// Every layer's attention of one step: one cluster of `cluster` CTAs per (sequence, kv
+// head), launched cooperatively (CTAs wait on each other, boundedly).  pdl: programmatic
+// serialization after the begin-step kernel.
+cudaError_t launch_attend_step(const RingDims &d, const RingDev &m, const CUtensorMap *tm_k,
+                               const CUtensorMap *tm_v, int kind, float scale_log2,
+                               const StepIO &io, int cluster, bool pdl, cudaStream_t st);
+// which 0: an mbarrier wait, 1: a wait on another CTA's counter, each given limit_ns and
+// bound to run out; the kernel sets kErrWaitFull / kErrWaitPeer and returns.
+cudaError_t launch_wait_probe(const RingDev &m, int which, unsigned long long limit_ns,
+                              cudaStream_t st);
 
 }  // namespace dflash

@@ -236,14 +236,16 @@ __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, 
 //   block  a_step + n_tiles            cos/sin of the noise positions committed + i
 __global__ void __launch_bounds__(kBeginThreads)
 k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
-             const uint16_t *__restrict__ v_rows, int64_t n_rows) {
+             const uint16_t *__restrict__ v_rows, int64_t n_rows, const SeqStep *host_steps) {
     __shared__ float2 cs[kHeadDim / 2];
     pdl_wait();   // the previous step's attention must be done with the ring state
     // one small wave: the first attention kernel may settle its CTAs right away (it waits
     // for this grid to finish before reading anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.x, s = blockIdx.y;
-    const SeqStep st = m.steps[s];
+    // the step's records: straight from the host's pinned staging slot when given (no
+    // copy ahead of the launch), else from the device copy
+    const SeqStep st = host_steps ? host_steps[s] : m.steps[s];
     if (b < d.a_step) {
         if (b < st.fold_rows) {
             if (!k_rows) return;        // the producer kernel already wrote the row and slot_pos
@@ -265,6 +267,10 @@ k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
         const int i = idx / half, j = idx - i * half;
         m.rope32[((int64_t)s * d.q_len + i) * half + j] = rope_angle_cs(st.committed + i, m.inv_freq[j]);
     }
+    // the whole-step attention kernel's counters start every step at zero (the previous
+    // step's kernel has finished: this grid waited for it above)
+    if (s == 0)
+        for (int idx = threadIdx.x; idx < d.step_sync_words; idx += blockDim.x) m.step_sync[idx] = 0u;
 }
 
 // Bulk append, one chunk of bulk_chunk rows: grid (bulk_chunk, n_seq).  Only sequences
@@ -296,7 +302,7 @@ cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16
 
 cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
-                              cudaStream_t st) {
+                              const SeqStep *host_steps, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.a_step + d.n_tiles + 1, d.n_seq);
     cfg.blockDim = dim3(kBeginThreads);
@@ -306,7 +312,7 @@ cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_begin_step, d, m, k_rows, v_rows, n_rows);
+    return cudaLaunchKernelEx(&cfg, k_begin_step, d, m, k_rows, v_rows, n_rows, host_steps);
 }
 
 }  // namespace dflash

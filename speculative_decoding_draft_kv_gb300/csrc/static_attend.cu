@@ -93,9 +93,15 @@ bool carve(unsigned char *base, const RingDims &d, RingDev &m) {
     m.rope32 = reinterpret_cast<float2 *>(take(sizeof(float2) * d.n_seq * d.q_len * (d.head_dim / 2)));
     m.flags = take((size_t)d.n_seq * d.n_tiles);
     m.maskbits = reinterpret_cast<uint64_t *>(take(sizeof(uint64_t) * d.n_seq * d.n_tiles * qw));
-    m.part_acc = reinterpret_cast<float *>(
-        take(sizeof(float) * d.n_seq * d.n_head_kv * d.groups * kRows * kHeadDim));
-    m.part_ml = reinterpret_cast<float2 *>(take(sizeof(float2) * d.n_seq * d.n_head_kv * d.groups * kRows));
+    // split partials only when several CTAs share a (sequence, kv head): with one group the
+    // attention kernel writes O itself
+    m.part_acc = nullptr;
+    m.part_ml = nullptr;
+    if (d.groups > 1) {
+        m.part_acc = reinterpret_cast<float *>(
+            take(sizeof(float) * d.n_seq * d.n_head_kv * d.groups * kRows * kHeadDim));
+        m.part_ml = reinterpret_cast<float2 *>(take(sizeof(float2) * d.n_seq * d.n_head_kv * d.groups * kRows));
+    }
     return off <= kStaticScratchBytes;
 }
 
@@ -107,6 +113,30 @@ int fail_static(int code, const char *fmt, ...) {
     va_end(ap);
     set_global_error(buf);
     return code;
+}
+
+// Set-up, once per device (with that device current): the device address of the scratch
+// array -- in host code its name is only a host-side stand-in -- and the attention
+// kernels' attributes.
+int scratch_base(const char *who, unsigned char **base, int *dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail_static(RING_ECUDA, "%s: cudaGetDevice failed", who);
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess)
+            return fail_static(RING_ECUDA, "%s: cudaGetSymbolAddress: %s", who, cudaGetErrorString(e));
+        e = attend_kernels_init();
+        if (e != cudaSuccess)
+            return fail_static(RING_ECUDA, "%s: kernel attributes: %s", who, cudaGetErrorString(e));
+        g_scratch_addr[dev] = ptr;
+    }
+    *base = static_cast<unsigned char *>(g_scratch_addr[dev]);
+    *dev_out = dev;
+    return RING_OK;
 }
 
 }  // namespace
@@ -146,28 +176,11 @@ extern "C" int ring_attend_static(const ring_attend_static_args *a, void *stream
     for (int j = 0; j < kHeadDim / 2; ++j)
         prm.inv_freq[j] = std::pow((double)a->rope_theta, -2.0 * j / kHeadDim);
 
-    // set-up, once per device: the device address of the scratch array
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return fail_static(RING_ECUDA, "ring_attend_static: cudaGetDevice failed");
     unsigned char *base = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_setup_mu);
-        if (!g_scratch_addr[dev]) {
-            void *ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-            if (e != cudaSuccess)
-                return fail_static(RING_ECUDA, "ring_attend_static: cudaGetSymbolAddress: %s",
-                                   cudaGetErrorString(e));
-            e = attend_kernels_init();
-            if (e != cudaSuccess)
-                return fail_static(RING_ECUDA, "ring_attend_static: kernel attributes: %s",
-                                   cudaGetErrorString(e));
-            g_scratch_addr[dev] = ptr;
-        }
-        base = static_cast<unsigned char *>(g_scratch_addr[dev]);
-    }
+    int dev = 0;
+    int rc = scratch_base("ring_attend_static", &base, &dev);
+    if (rc != RING_OK) return rc;
+    cudaError_t e = cudaSuccess;
 
     RingDims d{};
     d.cap = a->cap;
@@ -217,11 +230,10 @@ extern "C" int ring_attend_static(const ring_attend_static_args *a, void *stream
         return fail_static(RING_ECUDA, "ring_attend_static: cuTensorMapEncodeTiled failed");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    e = cudaMemsetAsync(m.err, 0, 4, st);
-    if (e == cudaSuccess) {
-        k_static_prepare<<<dim3(d.n_tiles + 1, d.n_seq), 128, 0, st>>>(d, m, a->mask, prm);
-        e = cudaGetLastError();
-    }
+    // the error word (first word of the scratch) keeps its bits until
+    // ring_attend_static_device_error reads and clears it
+    k_static_prepare<<<dim3(d.n_tiles + 1, d.n_seq), 128, 0, st>>>(d, m, a->mask, prm);
+    e = cudaGetLastError();
     const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->head_dim));
     if (e == cudaSuccess)
         e = launch_attend(d, m, &tm_k, &tm_v, 0, 0, scale_log2, a->q,
@@ -230,5 +242,22 @@ extern "C" int ring_attend_static(const ring_attend_static_args *a, void *stream
     if (e == cudaSuccess && d.groups > 1) e = launch_attend_combine(d, m, a->o, st);
     if (e != cudaSuccess)
         return fail_static(RING_ECUDA, "ring_attend_static: launch: %s", cudaGetErrorString(e));
+    return RING_OK;
+}
+
+extern "C" int ring_attend_static_device_error(uint32_t *bits) {
+    unsigned char *base = nullptr;
+    int dev = 0;
+    int rc = scratch_base("ring_attend_static_device_error", &base, &dev);
+    if (rc != RING_OK) return rc;
+    // the error word is the first word of the scratch (see carve)
+    uint32_t w = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&w, base, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && w) e = cudaMemset(base, 0, 4);
+    if (e != cudaSuccess)
+        return fail_static(RING_ECUDA, "ring_attend_static_device_error: %s", cudaGetErrorString(e));
+    if (bits) *bits = w;
+    if (w) return fail_static(RING_EDEVICE, "ring_attend_static: device error word 0x%x", w);
     return RING_OK;
 }

@@ -37,7 +37,8 @@ EXPORTED = (
     "ring_get_tile_flags", "ring_get_kv", "ring_device_error", "ring_describe",
     "ring_profile_enable", "ring_profile_read", "ring_launch_count", "ring_attend_static",
     "ring_last_error", "ring_set_producer", "ring_begin_step_features", "ring_recompute_window",
-    "ring_draft_step", "ring_get_kv_q8",
+    "ring_draft_step", "ring_get_kv_q8", "ring_clock_enable", "ring_clock_read",
+    "ring_check_bounded_wait", "ring_attend_static_device_error",
 )
 
 
@@ -54,7 +55,7 @@ class RingParams(ctypes.Structure):
                 ("rope_theta", ctypes.c_float), ("n_seq", ctypes.c_int32),
                 ("swa_window", ctypes.c_int32), ("bulk_chunk", ctypes.c_int32),
                 ("tiles_per_split", ctypes.c_int32), ("max_cluster", ctypes.c_int32),
-                ("kv_format", ctypes.c_int32)]
+                ("kv_format", ctypes.c_int32), ("step_split", ctypes.c_int32)]
 
 
 class RingGeometry(ctypes.Structure):
@@ -62,7 +63,9 @@ class RingGeometry(ctypes.Structure):
         "cap", "q_len", "a_step", "trash_slot", "kv_total", "kv_row", "head_dim", "n_head_kv",
         "n_head", "n_layer", "n_seq", "swa_window", "bulk_chunk", "tile_slots", "n_tiles",
         "tiles_per_split", "n_splits", "cluster", "groups")] + [("cache_bytes", ctypes.c_int64),
-                                           ("device_bytes", ctypes.c_int64)]
+                                           ("device_bytes", ctypes.c_int64),
+                                           ("step_split", ctypes.c_int32),
+                                           ("step_ctas", ctypes.c_int32)]
 
 
 class RingAttendStaticArgs(ctypes.Structure):
@@ -131,6 +134,10 @@ def _load():
         "ring_recompute_window": ([vp, p64, vp, p64, p64, i64, vp], ctypes.c_int),
         "ring_draft_step": ([vp, p64, vp, p64, p64, i64, vp, ctypes.POINTER(i32),
                              ctypes.POINTER(vp), vp], ctypes.c_int),
+        "ring_clock_enable": ([vp, i32], ctypes.c_int),
+        "ring_clock_read": ([vp, ctypes.POINTER(ctypes.c_double), p64], ctypes.c_int),
+        "ring_check_bounded_wait": ([vp, i32, i32, vp], ctypes.c_int),
+        "ring_attend_static_device_error": ([ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -193,10 +200,11 @@ def ring_init(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta):
 
 
 def ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16"):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16",
+                 step_split=0):
     p = RingParams(cap, q_len, head_dim, n_head_kv, n_head, n_layer, float(rope_theta), n_seq,
                    swa_window, bulk_chunk, tiles_per_split, max_cluster,
-                   KV_FORMATS.get(kv_format, kv_format))
+                   KV_FORMATS.get(kv_format, kv_format), step_split)
     h = ctypes.c_void_p()
     rc = _load().ring_init_ex(ctypes.byref(h), ctypes.byref(p))
     _check(rc, None, "ring_init_ex")
@@ -413,6 +421,33 @@ def ring_launch_count(h) -> int:
     return int(_load().ring_launch_count(h))
 
 
+def ring_clock_enable(h, on=True):
+    _check(_load().ring_clock_enable(h, 1 if on else 0), h, "ring_clock_enable")
+
+
+def ring_clock_read(h):
+    """(summed milliseconds, launches) of the attention kernel since the last read."""
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(_load().ring_clock_read(h, ctypes.byref(ms), ctypes.byref(n)), h, "ring_clock_read")
+    return ms.value, n.value
+
+
+def ring_check_bounded_wait(h, which, limit_us, stream=None):
+    """Launch the bounded-wait self-test kernel (0: mbarrier, 1: cross-CTA counter)."""
+    _check(_load().ring_check_bounded_wait(h, int(which), int(limit_us), _stream(stream)), h,
+           "ring_check_bounded_wait")
+
+
+def ring_attend_static_device_error() -> int:
+    """Read and clear ring_attend_static's device error word on the current device."""
+    bits = ctypes.c_uint32()
+    rc = _load().ring_attend_static_device_error(ctypes.byref(bits))
+    if rc not in (RING_OK, RING_EDEVICE):
+        _check(rc, None, "ring_attend_static_device_error")
+    return bits.value
+
+
 def ring_attend_static(cap, q_len, n_head_kv, n_head, rope_theta, committed, k, v, mask, q,
                        k_noise, v_noise, o, head_dim=128, stream=None):
     """One layer's attention over caller-owned buffers, allocating nothing.
@@ -438,10 +473,11 @@ class Ring:
     """Owning handle around the C entry points (closes itself)."""
 
     def __init__(self, cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta, n_seq=1,
-                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16"):
+                 swa_window=0, bulk_chunk=0, tiles_per_split=0, max_cluster=0, kv_format="f16",
+                 step_split=0):
         self.h = ring_init_ex(cap, q_len, head_dim, n_head_kv, n_head, n_layer, rope_theta,
                               n_seq, swa_window, bulk_chunk, tiles_per_split, max_cluster,
-                              kv_format)
+                              kv_format, step_split)
         self.geometry = ring_get_geometry(self.h)
 
     def rows_needed(self, seq, committed):
@@ -495,6 +531,15 @@ class Ring:
 
     def launch_count(self):
         return ring_launch_count(self.h)
+
+    def clock_enable(self, on=True):
+        ring_clock_enable(self.h, on)
+
+    def clock_read(self):
+        return ring_clock_read(self.h)
+
+    def check_bounded_wait(self, which, limit_us, stream=None):
+        ring_check_bounded_wait(self.h, which, limit_us, stream)
 
     def close(self):
         if self.h:

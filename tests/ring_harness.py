@@ -126,7 +126,7 @@ class GpuRun:
     """One CUDA ring plus bookkeeping oracles (slot_pos and masks only) per sequence."""
 
     def __init__(self, w, swa_window=None, tiles_per_split=0, bulk_chunk=0, device="cuda",
-                 max_cluster=0, kv_format="f16"):
+                 max_cluster=0, kv_format="f16", step_split=0):
         self.w = w
         self.kv_format = kv_format
         self.swa = w.swa_window if swa_window is None else swa_window
@@ -134,7 +134,7 @@ class GpuRun:
         self.ring = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
                            w.rope_theta, n_seq=w.n_seq, swa_window=self.swa,
                            bulk_chunk=bulk_chunk, tiles_per_split=tiles_per_split,
-                           max_cluster=max_cluster, kv_format=kv_format)
+                           max_cluster=max_cluster, kv_format=kv_format, step_split=step_split)
         self.g = self.ring.geometry
         # head_dim 2, one head, one layer: only slot_pos and masks are read from these
         self.book = [orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta,
@@ -146,7 +146,9 @@ class GpuRun:
     def close(self):
         self.ring.close()
 
-    def begin_step(self, committed):
+    def step_rows(self, committed):
+        """The new context rows of a step (generated on the device by position), with the
+        per-sequence first positions and row offsets the ring takes."""
         w = self.w
         committed = np.asarray(committed, np.int64)
         starts, counts = [], []
@@ -170,14 +172,29 @@ class GpuRun:
                     k, v = synth.context_rows(w.seed, s, layer, pos, w.kv_row, w.sigma, device=self.dev)
                     k_rows[layer, a:b] = k
                     v_rows[layer, a:b] = v
-        self.ring.begin_step(committed, k_rows, v_rows, row_off, np.asarray(starts, np.int64))
-        self._keep = (k_rows, v_rows)
+        return committed, np.asarray(starts, np.int64), counts, row_off, k_rows, v_rows
+
+    def _advance_book(self, committed, starts, counts):
         paths = []
-        for s in range(w.n_seq):
+        for s in range(self.w.n_seq):
             z = np.zeros((1, counts[s], 2), np.float16)
-            paths.append(self.book[s].begin_step(int(committed[s]), z, z, starts[s]))
-        self.committed = committed.copy()
+            paths.append(self.book[s].begin_step(int(committed[s]), z, z, int(starts[s])))
+        self.committed = np.asarray(committed, np.int64).copy()
         return paths
+
+    def begin_step(self, committed):
+        committed, starts, counts, row_off, k_rows, v_rows = self.step_rows(committed)
+        self.ring.begin_step(committed, k_rows, v_rows, row_off, starts)
+        self._keep = (k_rows, v_rows)
+        return self._advance_book(committed, starts, counts)
+
+    def step(self, committed, kind, q, k_noise, v_noise, o):
+        """One whole step through ring_step (begin-step + every layer's attention as one
+        replayed CUDA graph); q, k_noise, v_noise, o: per-layer device tensors."""
+        committed, starts, counts, row_off, k_rows, v_rows = self.step_rows(committed)
+        self.ring.step(committed, k_rows, v_rows, row_off, starts, kind, q, k_noise, v_noise, o)
+        self._keep = (k_rows, v_rows)
+        return self._advance_book(committed, starts, counts)
 
     def inputs(self, step, layer, device):
         w = self.w
