@@ -6,7 +6,11 @@ this path).  Default workload: one sequence, five layers, cap 4096, q_len 8, pre
 to 8192 committed tokens and then advanced by the page's acceptance histogram.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload 2|3|4|5] [--mask full|swa]
+                  [--workload 2|3|4|5] [--mask full|swa] [--step-split S]
+
+The line also carries, under "configs", the method's other roofline workloads measured
+the same way (cap 32768 x 16 sequences; cap 4096 x 64 sequences with mask_full and with
+mask_swa, window 2048), each with its own roofline, oracle baseline and state check.
 
 Under torchrun every rank runs its own independent rings (weak scaling, no collective on
 the data path); rank 0 prints the line with the max-over-ranks time.
@@ -228,6 +232,140 @@ def _workload(args):
     return w
 
 
+class StepBench:
+    """One workload on the GPU: its prepared inputs, the ring factory and the timed loop.
+    The L2 is flushed between steps (an untimed 512 MiB write) when the ring would fit in
+    it; larger rings are read from HBM anyway."""
+
+    def __init__(self, w, kind, args, dev, rank, n_steps):
+        import torch
+        self.w, self.kind, self.args, self.dev = w, kind, args, dev
+        self.stream = torch.cuda.current_stream()
+        self.P = prepare(w, n_steps, rank, dev)
+        r = self.new_ring()
+        self.g = r.geometry
+        r.close()
+        self.flush = self.g["cache_bytes"] * w.n_seq < 2 * L2_BYTES
+        self.flush_buf = (torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+                          if self.flush else None)
+
+    def new_ring(self, prefill=True):
+        import torch
+        from speculative_decoding_draft_kv_gb300 import ring as R
+        w, a, P = self.w, self.args, self.P
+        r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
+                   n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=a.tiles_per_split,
+                   max_cluster=a.max_cluster, kv_format=a.kv_format, step_split=a.step_split)
+        if prefill:
+            c, row_off, start, _ = P.plan[0]             # prefill (bulk path), untimed
+            r.begin_step(c, P.k_all, P.v_all, row_off, start, self.stream)
+            torch.cuda.synchronize()
+        return r
+
+    def step_graph(self, r, t):
+        P = self.P
+        c, row_off, start, _ = P.plan[t]
+        r.step(c, P.k_all, P.v_all, row_off, start, self.kind, P.q, P.kn, P.vn, P.o, self.stream)
+
+    def step_calls(self, r, t):
+        P = self.P
+        c, row_off, start, _ = P.plan[t]
+        r.begin_step(c, P.k_all, P.v_all, row_off, start, self.stream)
+        for layer in range(self.w.n_layer):
+            r.attend(layer, self.kind, P.q[layer], P.kn[layer], P.vn[layer], P.o[layer], self.stream)
+
+    def timed_loop(self, r, step, t0, n):
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        # an untimed ~1 ms spin first lets the host queue steps ahead of the device, so a
+        # host hiccup never leaves the device idle inside a timed step
+        torch.cuda._sleep(2_000_000)
+        for j in range(n):
+            a, b = evs[j]
+            a.record(self.stream)
+            step(r, t0 + j)
+            b.record(self.stream)
+            if self.flush:
+                self.flush_buf.fill_(j & 0xFF)
+        return evs
+
+    @staticmethod
+    def ms_of(evs):
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    def row_bytes(self):
+        # bytes a slot row holds: F16 two per value; q8_0 34 per 32 values (codes + scale)
+        return self.w.kv_row * (34 / 32 if self.args.kv_format == "q8_0" else 2)
+
+    def attend_bytes(self, committed):
+        """Algorithmic bytes of one layer's attention launch: every visible K/V slot row
+        once, the queries and the outputs (F32)."""
+        w = self.w
+        qo = 2 * w.n_seq * w.n_head * w.q_len * w.head_dim * 4
+        return visible_rows(w, committed, self.kind) * self.row_bytes() * 2 + qo
+
+    def measure(self, K, W, dist, sampler=None, keep_ring=False):
+        """W warm-up steps, then exactly K timed ring_step calls with CUDA events around each,
+        the attention kernel's device clock on.  Returns the figures and, when asked, the
+        ring (state after the last timed step)."""
+        import numpy as np
+        import torch
+        r = self.new_ring()
+        r.clock_enable(True)
+        self.timed_loop(r, self.step_graph, 1, W)
+        torch.cuda.synchronize()
+        r.clock_read()                                  # forget the warm-up launches
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        launches0 = r.launch_count()
+        evs = self.timed_loop(r, self.step_graph, 1 + W, K)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        clock_ms, clock_n = r.clock_read()
+        out = {
+            "ms_per_step": max_over_ranks(self.ms_of(evs), dist, self.dev) / K,
+            "launches": r.launch_count() - launches0,
+            "clocks": clocks,
+            "clock_ms": clock_ms, "clock_launches": clock_n,
+            "last_step": W + K,
+        }
+        assert r.device_error() == 0
+        persistent = self.g["step_split"] > 0
+        per_layer = [self.attend_bytes(self.P.plan[1 + W + j][0]) for j in range(K)]
+        out["alg_bytes_per_launch"] = float(np.mean(per_layer)) * (self.w.n_layer if persistent else 1)
+        out["kernel"] = "k_attend_step" if persistent else "k_attend"
+        out["launches_per_step"] = 1 if persistent else self.w.n_layer
+        out["step_kv_bytes"] = float(np.mean([visible_rows(self.w, self.P.plan[1 + W + j][0], self.kind)
+                                              for j in range(K)])) * self.row_bytes() * 2 * self.w.n_layer
+        if keep_ring:
+            out["ring"] = r
+        else:
+            r.close()
+        return out
+
+    def roofline(self, m, peak, peak_kind, traffic=None):
+        launch_ms = m["clock_ms"] / max(m["clock_launches"], 1)
+        achieved = m["alg_bytes_per_launch"] / (launch_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": m["kernel"],
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "alg_bytes_per_launch": m["alg_bytes_per_launch"], "launch_ms": launch_ms,
+                "launches_per_step": m["launches_per_step"],
+                "timing": "device clock of every launch inside the timed graph replays "
+                          "(globaltimer: earliest CTA past its grid dependency to the last CTA's "
+                          "exit), averaged over the timed steps"}
+
+
+EXTRA_CONFIGS = [(5, "full"), (4, "full"), (4, "swa")]
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -246,111 +384,44 @@ def run_gb300(args):
     B.build()
     w = _workload(args)
     K, W = args.steps, args.warmup
-    P = prepare(w, K + W, rank, dev)
-    stream = torch.cuda.current_stream()
     kind = args.mask
-
-    def new_ring():
-        r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
-                   n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
-                   max_cluster=args.max_cluster, kv_format=args.kv_format,
-                   step_split=args.step_split)
-        c, row_off, start, _ = P.plan[0]             # prefill (bulk path), untimed
-        r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
-        torch.cuda.synchronize()
-        return r
-
-    ring = new_ring()
-    g = ring.geometry
-    flush = g["cache_bytes"] * w.n_seq < 2 * L2_BYTES
-    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
-
-    def step_graph(r, t):
-        c, row_off, start, _ = P.plan[t]
-        r.step(c, P.k_all, P.v_all, row_off, start, kind, P.q, P.kn, P.vn, P.o, stream)
-
-    def step_calls(r, t):
-        c, row_off, start, _ = P.plan[t]
-        r.begin_step(c, P.k_all, P.v_all, row_off, start, stream)
-        for layer in range(w.n_layer):
-            r.attend(layer, kind, P.q[layer], P.kn[layer], P.vn[layer], P.o[layer], stream)
-
-    def timed_loop(r, step, t0, n, pre=None, post=None):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        # an untimed ~1 ms spin first lets the host queue steps ahead of the device, so a
-        # host hiccup never leaves the device idle inside a timed step
-        torch.cuda._sleep(2_000_000)
-        for j in range(n):
-            a, b = evs[j]
-            a.record(stream)
-            if pre:
-                pre(t0 + j)
-            step(r, t0 + j)
-            if post:
-                post(t0 + j)
-            b.record(stream)
-            if flush:
-                flush_buf.fill_(j & 0xFF)
-        return evs
-
-    def ms_of(evs):
-        return sum(a.elapsed_time(b) for a, b in evs)
+    sb = StepBench(w, kind, args, dev, rank, K + W)
+    P, g = sb.P, sb.g
+    stream = sb.stream
+    peak, peak_kind = _peaks()
+    q8 = args.kv_format == "q8_0"
 
     # ---- pass 1: the step graph; warm-up, then exactly K timed steps ----
-    timed_loop(ring, step_graph, 1, W)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}" if rank == 0 else None)
-    if rank == 0:
-        sampler.start()
-    launches0 = ring.launch_count()
-    evs = timed_loop(ring, step_graph, 1 + W, K)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches = ring.launch_count() - launches0
-    clocks = sampler.stop() if rank == 0 else None
-    ms_per_step = max_over_ranks(ms_of(evs), dist, dev) / K
-    assert ring.device_error() == 0
-    ring.close()
+    sampler = ClockSampler(f"GPU-{torch.cuda.get_device_properties(dev).uuid}") if rank == 0 else None
+    head = sb.measure(K, W, dist, sampler, keep_ring=True)
+    head_ring = head.pop("ring")
+    ms_per_step = head["ms_per_step"]
+    tr = NCU_TRAFFIC.get(w.name + ("_q8_0" if q8 else "") + ("_step" if g["step_split"] > 0 else ""))
+    src = "step_kernels.cu" if g["step_split"] > 0 else "attn_kernels.cu"
+    traffic = tr["bytes"] if tr and tr.get("kernel") == _kernel_source_hash(src) else None
+    roof = sb.roofline(head, peak, peak_kind, traffic)
 
     # ---- pass 2: the same steps as separate calls (begin_step + attend per layer) ----
     n2 = min(K + W, 400)
-    ring = new_ring()
-    evs = timed_loop(ring, step_calls, 1, n2)
+    ring = sb.new_ring()
+    evs = sb.timed_loop(ring, sb.step_calls, 1, n2)
     torch.cuda.synchronize()
-    ms_calls = max_over_ranks(ms_of(evs), dist, dev) / n2
+    ms_calls = max_over_ranks(sb.ms_of(evs), dist, dev) / n2
     ring.close()
 
-    # ---- pass 3: separate calls with events around every kernel launch ----
-    ring = new_ring()
+    # ---- pass 3: separate calls with events around every kernel launch (kernel shares) ----
+    ring = sb.new_ring()
     R.ring_profile_enable(ring.h, True)
-    timed_loop(ring, step_calls, 1, n2)
+    sb.timed_loop(ring, sb.step_calls, 1, n2)
     torch.cuda.synchronize()
     prof = R.ring_profile_read(ring.h)
     R.ring_profile_enable(ring.h, False)
     ring.close()
-    attn = prof["attend"]
-    attn_ms = attn["total_ms"] / max(attn["launches"], 1)
-    vis = float(np.mean([visible_rows(w, P.plan[1 + j][0], kind) for j in range(n2)]))
-    q8 = args.kv_format == "q8_0"
-    # bytes a slot row holds: F16 two per value; q8_0 34 per 32 values (codes + F16 scale)
-    row_bytes = w.kv_row * (34 / 32 if q8 else 2)
-    kv_bytes = vis * row_bytes * 2
-    q_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
-    o_bytes = w.n_seq * w.n_head * w.q_len * w.head_dim * 4
-    alg_bytes = kv_bytes + q_bytes + o_bytes
-    peak, peak_kind = _peaks()
-    achieved = alg_bytes / (attn_ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(w.name + ("_q8_0" if q8 else ""))
-    traffic = tr["bytes"] if tr and tr.get("kernel") == _kernel_source_hash() else None
     shares = {k: v["total_ms"] for k, v in prof.items() if k != "step_graph"}
     tot = sum(shares.values()) or 1.0
     shares = {k: round(v / tot, 4) for k, v in shares.items()}
+    roof["kernel_time_share_separate_calls"] = shares
+    row_bytes = sb.row_bytes()
 
     # ---- pass 4: end to end through ring_step with host buffers: every step copies its
     # new rows, queries and noise rows from pinned host memory and reads every layer's
@@ -392,19 +463,18 @@ def run_gb300(args):
             for o, ho in zip(P.o, host_out):
                 ho.copy_(o, non_blocking=True)
 
-        ring = new_ring()
-        timed_loop(ring, step_e2e, 1, min(W, n4))        # warm-up (captures the graph)
+        ring = sb.new_ring()
+        sb.timed_loop(ring, step_e2e, 1, min(W, n4))        # warm-up (captures the graphs)
         torch.cuda.synchronize()
         ring.close()
-        ring = new_ring()
-        evs = timed_loop(ring, step_e2e, 1, n4)
+        ring = sb.new_ring()
+        evs = sb.timed_loop(ring, step_e2e, 1, n4)
         torch.cuda.synchronize()
         ring.close()
-        e2e_ms = max_over_ranks(ms_of(evs), dist, dev) / n4
+        e2e_ms = max_over_ranks(sb.ms_of(evs), dist, dev) / n4
         e2e_obj = {"value": 1000.0 / e2e_ms * world, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                    "steps": n4, "api": "ring_step"}
-
     # ---- pass 5: the step with the context rows made by the producer from fused
     # features (ring_begin_step_features + ring_attend per layer), and the producer
     # kernel's own roofline ----
@@ -431,7 +501,7 @@ def run_gb300(args):
         def prod_ring():
             r = R.Ring(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer, w.rope_theta,
                        n_seq=w.n_seq, swa_window=w.swa_window, tiles_per_split=args.tiles_per_split,
-                       max_cluster=args.max_cluster)
+                       max_cluster=args.max_cluster, kv_format=args.kv_format)
             r.set_producer(H, 1e-6, wk, wv, kn)
             c, row_off, start, _ = P.plan[0]
             r.begin_step_features(c, feat_all, row_off, start, stream)
@@ -446,16 +516,16 @@ def run_gb300(args):
 
         n5 = min(K + W, 400)
         ring = prod_ring()
-        timed_loop(ring, step_prod, 1, min(W, n5))
+        sb.timed_loop(ring, step_prod, 1, min(W, n5))
         torch.cuda.synchronize()
-        evs = timed_loop(ring, step_prod, 1 + min(W, n5), n5 - min(W, n5))
+        evs = sb.timed_loop(ring, step_prod, 1 + min(W, n5), n5 - min(W, n5))
         torch.cuda.synchronize()
-        ms_prod = max_over_ranks(ms_of(evs), dist, dev) / max(1, n5 - min(W, n5))
+        ms_prod = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n5 - min(W, n5))
         assert ring.device_error() == 0
         ring.close()
         ring = prod_ring()
         R.ring_profile_enable(ring.h, True)
-        timed_loop(ring, step_prod, 1, n5)
+        sb.timed_loop(ring, step_prod, 1, n5)
         torch.cuda.synchronize()
         pp = R.ring_profile_read(ring.h)
         ring.close()
@@ -493,16 +563,16 @@ def run_gb300(args):
 
             n6 = min(K + W, 100)
             ring = prod_ring()
-            timed_loop(ring, step_legacy, 1, min(W, n6))
+            sb.timed_loop(ring, step_legacy, 1, min(W, n6))
             torch.cuda.synchronize()
-            evs = timed_loop(ring, step_legacy, 1 + min(W, n6), n6 - min(W, n6))
+            evs = sb.timed_loop(ring, step_legacy, 1 + min(W, n6), n6 - min(W, n6))
             torch.cuda.synchronize()
-            ms_leg = max_over_ranks(ms_of(evs), dist, dev) / max(1, n6 - min(W, n6))
+            ms_leg = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n6 - min(W, n6))
             assert ring.device_error() == 0
             ring.close()
             ring = prod_ring()                 # a fresh ring: committed never goes back
             R.ring_profile_enable(ring.h, True)
-            timed_loop(ring, step_legacy, 1, min(20, n6))
+            sb.timed_loop(ring, step_legacy, 1, min(20, n6))
             torch.cuda.synchronize()
             pl = R.ring_profile_read(ring.h)["produce"]
             ring.close()
@@ -535,16 +605,16 @@ def run_gb300(args):
 
         n7 = min(K + W, 400)
         ring = draft_ring()
-        timed_loop(ring, step_draft, 1, min(W, n7))
+        sb.timed_loop(ring, step_draft, 1, min(W, n7))
         torch.cuda.synchronize()
-        evs = timed_loop(ring, step_draft, 1 + min(W, n7), n7 - min(W, n7))
+        evs = sb.timed_loop(ring, step_draft, 1 + min(W, n7), n7 - min(W, n7))
         torch.cuda.synchronize()
-        ms_draft = max_over_ranks(ms_of(evs), dist, dev) / max(1, n7 - min(W, n7))
+        ms_draft = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n7 - min(W, n7))
         assert ring.device_error() == 0
         ring.close()
         ring = draft_ring()
         R.ring_profile_enable(ring.h, True)
-        timed_loop(ring, step_draft, 1, min(n7, 100))
+        sb.timed_loop(ring, step_draft, 1, min(n7, 100))
         torch.cuda.synchronize()
         pd = R.ring_profile_read(ring.h)
         ring.close()
@@ -558,12 +628,51 @@ def run_gb300(args):
         del wq, qn, noise_h
         del feat_all, wk, wv, kn
 
+
+    # ---- the roofline workloads of the method (cap 32768 x 16 sequences; cap 4096 x 64
+    # sequences with mask_full and with mask_swa, window 2048): the same measurement ----
+    extras = []
+    if world == 1 and not args.no_extra_configs:
+        del sb
+        torch.cuda.empty_cache()
+        for wid, xkind in EXTRA_CONFIGS:
+            xw = synth.workload(wid)
+            Kx, Wx = min(K, args.extra_steps), 3
+            xsb = StepBench(xw, xkind, args, dev, rank, Kx + Wx)
+            xm = xsb.measure(Kx, Wx, None, keep_ring=True)
+            xring = xm.pop("ring")
+            xroof = xsb.roofline(xm, peak, peak_kind)
+            extras.append({"workload": xw.name, "mask": xkind, "value": 1000.0 / xm["ms_per_step"],
+                           "unit": UNIT, "ms_per_step": xm["ms_per_step"], "steps": Kx, "warmup": Wx,
+                           "step_kv_gbs": xm["step_kv_bytes"] / (xm["ms_per_step"] * 1e-3) / 1e9,
+                           "l2": ("flushed between steps" if xsb.flush else "inputs larger than L2"),
+                           "split": {k: xsb.g[k] for k in ("tiles_per_split", "n_splits", "cluster",
+                                                           "groups", "step_split")},
+                           "roofline": xroof, "_ring": xring, "_plan": xsb.P.plan,
+                           "_last": xm["last_step"], "_w": xw})
+            del xsb
+            torch.cuda.empty_cache()
+
     cpu = None
+    state = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, kind, budget_s=args.cpu_seconds, kv_format=args.kv_format)
+        # the oracle leg: the oracle timed on the host cores, and its bookkeeping (slot map,
+        # masks, tile flags) carried through the same commits the timed steps made and
+        # compared bit for bit with the GPU ring's final state
+        cpu = cpu_baseline(w, kind, n_steps=args.cpu_steps, kv_format=args.kv_format)
+        state = state_check(w, kind, P.plan, head["last_step"], head_ring)
+        for x in extras:
+            n_x = 1 if x["_w"].cap > 8192 else 2
+            x["cpu_baseline"] = cpu_baseline(x["_w"], x["mask"], n_steps=n_x, kv_format=args.kv_format)
+            x["state_check"] = state_check(x["_w"], x["mask"], x["_plan"], x["_last"], x["_ring"],
+                                           seqs=[0, x["_w"].n_seq // 2, x["_w"].n_seq - 1])
+    head_ring.close()
+    for x in extras:
+        x.pop("_ring").close()
+        for k in ("_plan", "_last", "_w"):
+            x.pop(k)
 
     if rank == 0:
-        vis_step = visible_rows(w, P.plan[1][0], kind) * row_bytes * 2 * w.n_layer
         line = {
             "metric": METRIC,
             "value": 1000.0 / ms_per_step * world,
@@ -584,27 +693,23 @@ def run_gb300(args):
                 "n_head": w.n_head, "mask": kind, "kv_format": args.kv_format,
                 "kv_total": g["kv_total"],
                 "tiles_per_split": g["tiles_per_split"], "n_splits": g["n_splits"],
-                "cluster": g["cluster"], "groups": g["groups"],
-                "l2": ("flushed between steps (512 MiB write, untimed)" if flush
+                "cluster": g["cluster"], "groups": g["groups"], "step_split": g["step_split"],
+                "l2": ("flushed between steps (512 MiB write, untimed)" if sb_flush(g, w)
                        else "inputs larger than L2"),
                 "api": "ring_step (one CUDA graph per step)",
                 "parallelism": f"independent rings x{world}",
             },
-            "gpu_launches": int(launches),
+            "gpu_launches": int(head["launches"]),
             "separate_calls": {"value": 1000.0 / ms_calls * world, "ms_per_step": ms_calls,
                                "api": "ring_begin_step + ring_attend per layer"},
             "with_producer": prod_obj,
-            "step_kv_gbs": vis_step / (ms_per_step * 1e-3) / 1e9,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "k_attend", "peak_source": f"{peak_kind} hbm_gbs",
-                         "alg_bytes_per_launch": alg_bytes, "launch_ms": attn_ms,
-                         "timing": "CUDA events around each launch on its stream, "
-                                   "instrumented repeat of the timed steps as separate calls",
-                         "kernel_time_share": shares},
-            "clocks": clocks,
+            "step_kv_gbs": head["step_kv_bytes"] / (ms_per_step * 1e-3) / 1e9,
+            "roofline": roof,
+            "configs": extras,
+            "clocks": head["clocks"],
             "e2e": e2e_obj,
             "cpu_baseline": cpu,
+            "state_check": state,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -612,77 +717,125 @@ def run_gb300(args):
         dist.destroy_process_group()
 
 
+def sb_flush(g, w):
+    return g["cache_bytes"] * w.n_seq < 2 * L2_BYTES
+
+
 # ----------------------------------------------------------------------------------------
 # CPU oracle legs
 # ----------------------------------------------------------------------------------------
 
-def _oracle_setup(w, kv_format="f16"):
+def _cpu_worker(task):
+    """Oracle work of one host process: a static share of the workload's (sequence, layer)
+    units, each a one-layer float64 ring of the step-by-step oracle.  Everything the timed
+    steps read (prefill, context rows, queries, noise rows) is made first, untimed; then the
+    process times begin_step + attention of its units for the sampled steps."""
+    w, kind, units, n_steps, kv_format = task
+    import time as _t
+
     import numpy as np
     import torch
+    torch.set_num_threads(1)
 
     import synth
     from oracle import ring_oracle as orc
 
-    sched = synth.commit_schedule(w, 10000)
-    S = w.n_seq
-    rings = [orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, w.n_layer,
-                            w.rope_theta, swa_window=w.swa_window, kv_format=kv_format)
-             for _ in range(S)]
+    # row 0 is the untimed first call (the prefill where the workload has one)
+    sched = synth.commit_schedule(w, n_steps + (0 if w.kind in ("decode", "batched", "large") else 1))
+    work = []
+    for s, layer in units:
+        ring = orc.RingOracle(w.cap, w.q_len, w.head_dim, w.n_head_kv, w.n_head, 1, w.rope_theta,
+                              swa_window=w.swa_window, kv_format=kv_format)
 
-    def rows(s, a, b):
-        ks, vs = [], []
-        for layer in range(w.n_layer):
+        def rows(a, b):
             k, v = synth.context_rows(w.seed, s, layer, torch.arange(a, b), w.kv_row, w.sigma)
-            ks.append(k.numpy())
-            vs.append(v.numpy())
-        return np.stack(ks), np.stack(vs)
+            return k.numpy()[None], v.numpy()[None]
 
-    def inputs(t, s):
-        out = []
-        for layer in range(w.n_layer):
+        c0 = int(sched[0, s])
+        st, _ = ring.rows_needed(c0)
+        ring.begin_step(c0, *rows(st, c0), st)            # prefill, untimed
+        steps = []
+        nxt = c0
+        for t in range(1, sched.shape[0]):
+            c = int(sched[t, s])
+            st = max(nxt, c - min(c, w.cap))
             q = synth.query_block(w.seed, t, s, layer, w.q_len, w.n_head, w.head_dim, w.sigma).numpy()
             kn, vn = synth.noise_rows(w.seed, t, s, layer, w.q_len, w.kv_row, w.sigma)
-            out.append((q, kn.numpy(), vn.numpy()))
-        return out
+            steps.append((c, rows(st, c), st, q, kn.numpy(), vn.numpy()))
+            nxt = c
+        work.append((ring, steps))
+    t0 = _t.perf_counter()
+    for j in range(n_steps):
+        for ring, steps in work:
+            c, (k, v), st, q, kn, vn = steps[j]
+            ring.begin_step(c, k, v, st)
+            ring.attend(0, q, kn, vn, kind)
+    return _t.perf_counter() - t0
 
-    return sched, rings, rows, inputs
+
+def cpu_baseline(w, kind, n_steps, kv_format="f16"):
+    """Time the float64 oracle (ring-state route) on the host's cores: the workload's
+    (sequence, layer) units are split statically over one process per core (at most one
+    per unit); every process runs the same sampled steps of its units, and a step of the
+    whole workload takes the slowest process's time."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+
+    units = [(s, layer) for s in range(w.n_seq) for layer in range(w.n_layer)]
+    cores = max(1, min(os.cpu_count() or 1, len(units)))
+    parts = [units[i::cores] for i in range(cores)]
+    with ProcessPoolExecutor(cores, mp_context=mp.get_context("spawn")) as ex:
+        secs = list(ex.map(_cpu_worker, [(w, kind, part, n_steps, kv_format) for part in parts]))
+    sec_per_step = max(secs) / n_steps
+    return {"value": 1.0 / sec_per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_steps} steps x {w.n_seq} sequences x {w.n_layer} layers ({w.name}, "
+                      f"mask {kind}): {len(units)} (sequence, layer) units over {cores} processes, "
+                      f"slowest process {max(secs):.1f} s; float64 numpy, one thread each; "
+                      f"prefill and input generation untimed"}
 
 
-def cpu_baseline(w, kind, budget_s=15.0, max_steps=None, kv_format="f16"):
-    """Time the float64 oracle (ring-state route) on the host: untimed prefill, then as many
-    full steps (begin_step for every sequence + every layer's attention, inputs drawn
-    beforehand) as fit in ``budget_s``."""
-    import time as _t
+def _tile_flags(mask, tile):
+    """0: no slot of a tile visible to any row; 1: every slot of a full tile visible to
+    every row; 2: anything else."""
+    import numpy as np
+    n_tiles = (mask.shape[1] + tile - 1) // tile
+    out = np.zeros(n_tiles, np.uint8)
+    for t in range(n_tiles):
+        seg = mask[:, t * tile:(t + 1) * tile] == 0
+        out[t] = 0 if not seg.any() else (1 if seg.shape[1] == tile and seg.all() else 2)
+    return out
 
-    sched, rings, rows, inputs = _oracle_setup(w, kv_format)
-    S = w.n_seq
-    sample_seqs = min(S, 1)
-    for s in range(sample_seqs):
-        st, _ = rings[s].rows_needed(int(sched[0, s]))
-        k, v = rows(s, st, int(sched[0, s]))
-        rings[s].begin_step(int(sched[0, s]), k, v, st)
-    done, elapsed = 0, 0.0
-    t = 1
-    while elapsed < budget_s and (max_steps is None or done < max_steps):
-        pre = []
-        for s in range(sample_seqs):
-            c = int(sched[t, s])
-            st, _ = rings[s].rows_needed(c)
-            pre.append((c, rows(s, st, c), st, inputs(t, s)))
-        t0 = _t.perf_counter()
-        for s in range(sample_seqs):
-            c, (k, v), st, inp = pre[s]
-            rings[s].begin_step(c, k, v, st)
-            for layer, (q, kn, vn) in enumerate(inp):
-                rings[s].attend(layer, q, kn, vn, kind)
-        elapsed += _t.perf_counter() - t0
-        done += 1
-        t += 1
-    # a step of the workload covers all S sequences; the sample covered sample_seqs
-    sec_per_step = elapsed / done * (S / sample_seqs)
-    return {"value": 1.0 / sec_per_step, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} steps x {sample_seqs} of {S} sequences x {w.n_layer} layers "
-                      f"({elapsed:.1f} s), scaled to all sequences; float64 numpy, one thread"}
+
+def state_check(w, kind, plan, last, ring, seqs=None):
+    """The oracle's bookkeeping (slot map and masks of a head_dim-2 ring) carried through
+    the commits plan[0 .. last], against the GPU ring's slot_pos, masks and tile flags,
+    bit for bit."""
+    import numpy as np
+
+    from oracle import ring_oracle as orc
+
+    g = ring.geometry
+    kinds = ["full"] + (["swa"] if w.swa_window else [])
+    checked = []
+    for s in (range(w.n_seq) if seqs is None else seqs):
+        book = orc.RingOracle(w.cap, w.q_len, 2, 1, 1, 1, w.rope_theta, swa_window=w.swa_window)
+        for t in range(last + 1):
+            c = int(plan[t][0][s])
+            st, n = book.rows_needed(c)
+            z = np.zeros((1, n, 2), np.float16)
+            book.begin_step(c, z, z, st)
+        if not np.array_equal(ring.slot_pos(s), book.slot_pos.astype(np.int32)):
+            return {"ok": False, "failed": f"slot_pos of sequence {s}"}
+        for k in kinds:
+            want = book.mask(k)
+            got = ring.mask(s, k)
+            if got.view(np.uint32).tobytes() != want.view(np.uint32).tobytes():
+                return {"ok": False, "failed": f"mask {k} of sequence {s}"}
+            if not np.array_equal(ring.tile_flags(s, k), _tile_flags(want, g["tile_slots"])):
+                return {"ok": False, "failed": f"tile flags {k} of sequence {s}"}
+        checked.append(s)
+    return {"ok": True, "steps": last, "sequences": checked, "masks": kinds,
+            "what": "slot_pos, masks and tile flags after the timed steps, bit for bit"}
 
 
 def run_reference(args):
@@ -690,9 +843,8 @@ def run_reference(args):
     if rank != 0:
         return
     w = _workload(args)
-    budget = max(5.0, min(150.0, 0.6 * (args.steps + args.warmup)))
-    cpu = cpu_baseline(w, args.mask, budget_s=budget, max_steps=args.steps + args.warmup,
-                       kv_format=args.kv_format)
+    n = max(1, min(args.steps + args.warmup, args.ref_steps))
+    cpu = cpu_baseline(w, args.mask, n_steps=n, kv_format=args.kv_format)
     line = {
         "impl": "reference",
         "metric": METRIC, "value": cpu["value"], "unit": UNIT, "n_gpus": world,
@@ -708,8 +860,9 @@ def run_reference(args):
 
 
 def main():
-    # The oracle legs report one host thread: keep numpy's BLAS (and torch's CPU pool) at one
-    # thread.  Set before numpy or torch is first imported; the GPU path does not use them.
+    # Every oracle process runs one thread (the oracle legs spread over processes): keep
+    # numpy's BLAS at one thread.  Set before numpy or torch is first imported (inherited
+    # by the spawned oracle processes); the GPU path does not use them.
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ.setdefault(var, "1")
     ap = argparse.ArgumentParser()
@@ -725,7 +878,13 @@ def main():
     ap.add_argument("--step-split", type=int, default=0,
                     help="ring_step attention: 0 one launch per layer, -1 the persistent "
                          "whole-step kernel with the widest cluster, >0 its cluster size")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-steps", type=int, default=100,
+                    help="steps of the headline workload the oracle leg times")
+    ap.add_argument("--ref-steps", type=int, default=200,
+                    help="at most this many steps for the reference arm (the oracle)")
+    ap.add_argument("--extra-steps", type=int, default=40,
+                    help="timed steps of each of the method's other roofline workloads")
+    ap.add_argument("--no-extra-configs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-format", choices=["f16", "q8_0"], default="f16",

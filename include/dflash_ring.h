@@ -368,14 +368,17 @@ int64_t ring_launch_count(const ring_t *r);
  * inside CUDA graphs too: each launch of the attention kernel (one per layer, or the
  * persistent whole-step kernel) records, with the GPU's global nanosecond timer, the
  * earliest moment any of its CTAs passed its grid dependency and the latest moment any
- * CTA exited; the last CTA out adds the difference to a running sum.  (No counterpart on
- * the page: it is how the throughput of the kernel inside a replayed step is measured.)
+ * CTA was done, in a slot for that layer of that step (every begin-step call starts a
+ * step).  The stamps are reductions nobody waits for, so the clock does not slow the
+ * launches it times.  (No counterpart on the page: it is how the throughput of the
+ * kernel inside a replayed step is measured.)
  *
  * ring_clock_enable -- on != 0 starts recording with the next launch (ring_step re-captures
  *   its graph); 0 stops.  Errors: EINVAL.
- * ring_clock_read -- synchronise, return the summed milliseconds and the number of
- *   launches recorded since the last read, and reset both.  Either pointer may be NULL.
- *   Errors: EINVAL, ECUDA.
+ * ring_clock_read -- synchronise, return the summed milliseconds of the recorded launches
+ *   and their number, and clear them.  Slots cover the last 2048 steps: read at least that
+ *   often; two launches of one layer within one step share a slot (their joint span).
+ *   Either pointer may be NULL.  Errors: EINVAL, ECUDA.
  */
 int ring_clock_enable(ring_t *r, int32_t on);
 int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches);

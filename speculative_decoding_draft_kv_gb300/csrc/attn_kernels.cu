@@ -111,6 +111,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const uint64_t *sbits = reinterpret_cast<const uint64_t *>(smem + kOffBits);
     const uint32_t bar0 = smem_u32(smem + kOffBars);   // full[0..S-1], then empty[0..S-1]
     __shared__ volatile int s_abort;
+    int clk_slot = 0;     // kernel clock slot of this launch (thread 0)
 
     const uint32_t nct = CLUSTER ? cluster_size() : 1u, rank = CLUSTER ? cluster_rank() : 0u;
     // receive buffer (clusters only): dedicated, since other CTAs of the cluster push into
@@ -256,7 +257,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         // dependency
         pdl_wait();
         if (d.single_wave) pdl_trigger();
-        if (threadIdx.x == 0 && m.clock) clock_start(m.clock);
+        if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, layer);
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
@@ -813,7 +814,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if constexpr (!CLUSTER) {
         if (m.clock) {
             __syncthreads();
-            if (threadIdx.x == 0) clock_stop(m.clock, gridDim.x * gridDim.y * gridDim.z);
+            if (threadIdx.x == 0) clock_stop(m.clock, clk_slot);
         }
         return;
     }
@@ -857,7 +858,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
     if (m.clock) {
         __syncthreads();
-        if (threadIdx.x == 0) clock_stop(m.clock, gridDim.x * gridDim.y * gridDim.z);
+        if (threadIdx.x == 0) clock_stop(m.clock, clk_slot);
     }
 }
 

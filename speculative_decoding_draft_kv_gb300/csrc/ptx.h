@@ -225,29 +225,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     return false;
 }
 
-// Kernel clock, on while `clk` is not NULL: the earliest start (taken after the grid
-// dependency resolves) and the latest exit over the CTAs of a launch.  The last CTA out
-// adds their difference to a running sum (clk[2], ns) and counts the launch (clk[3]);
-// clk[0], clk[1] and the CTA count clk[4] return to their idle values for the next
-// launch, which can only begin after this one has ended.  One thread per CTA calls each.
-__device__ __forceinline__ void clock_start(unsigned long long *clk) {
-    atomicMin(&clk[0], (unsigned long long)global_ns());
+// Kernel clock, on while `clk` is not NULL (layout in ring_internal.h): every CTA of a
+// launch lowers the launch's earliest-start word once its grid dependency has resolved and
+// raises its latest-end word when it is done -- two reductions whose results nobody waits
+// for, so the clock adds no latency to the launch.  The slot is that of layer `layer` of
+// the current step (the begin-step kernel advances the step counter); the host adds up the
+// spans.  One thread per CTA calls each; clock_stop takes clock_start's slot.
+__device__ __forceinline__ int clock_start(unsigned long long *clk, int layer) {
+    const unsigned int step = *reinterpret_cast<volatile unsigned int *>(clk + 2 * kClockSlots);
+    const int slot = (int)(step % (unsigned int)kClockSteps) * kMaxStepLayers + layer;
+    atomicMin(&clk[slot], (unsigned long long)global_ns());
+    return slot;
 }
 
-__device__ __forceinline__ void clock_stop(unsigned long long *clk, unsigned int n_ctas) {
-    atomicMax(&clk[1], (unsigned long long)global_ns());
-    __threadfence();
-    if (atomicAdd(reinterpret_cast<unsigned int *>(&clk[4]), 1u) == n_ctas - 1u) {
-        __threadfence();
-        const unsigned long long t0 = atomicAdd(&clk[0], 0ull), t1 = atomicAdd(&clk[1], 0ull);
-        if (t1 > t0) {
-            atomicAdd(&clk[2], t1 - t0);
-            atomicAdd(&clk[3], 1ull);
-        }
-        atomicExch(&clk[0], ~0ull);
-        atomicExch(&clk[1], 0ull);
-        atomicExch(reinterpret_cast<unsigned int *>(&clk[4]), 0u);
-    }
+__device__ __forceinline__ void clock_stop(unsigned long long *clk, int slot) {
+    atomicMax(&clk[kClockSlots + slot], (unsigned long long)global_ns());
 }
 
 }  // namespace dflash

@@ -457,7 +457,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows);
     ALLOC(m.err, uint32_t, 1);
     ALLOC(m.inv_freq, double, d.head_dim / 2);
-    ALLOC(r->clock_buf, unsigned long long, 5);
+    ALLOC(r->clock_buf, unsigned long long, 2 * kClockSlots + 1);
     ALLOC(m.probe, uint32_t, 2);
     if (r->step_split > 0) ALLOC(m.step_sync, uint32_t, d.step_sync_words);
 #undef ALLOC
@@ -484,8 +484,8 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     zero(m.rope32, 0, (size_t)d.n_seq * d.q_len * d.head_dim / 2 * sizeof(float2));
     zero(m.err, 0, 4);
     zero(m.probe, 0, 8);
-    zero(r->clock_buf, 0, 5 * 8);
-    zero(r->clock_buf, 0xff, 8);                 // earliest start: none yet
+    zero(r->clock_buf, 0xff, (size_t)kClockSlots * 8);                  // earliest start: none yet
+    zero(r->clock_buf + kClockSlots, 0, ((size_t)kClockSlots + 1) * 8);   // latest end, step counter
     if (m.step_sync) zero(m.step_sync, 0, (size_t)d.step_sync_words * 4);
     std::vector<double> inv(d.head_dim / 2);
     for (int i = 0; i < d.head_dim / 2; ++i)
@@ -1201,13 +1201,24 @@ int ring_clock_enable(ring_t *r, int32_t on) {
 
 int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches) {
     if (!r) return RING_EINVAL;
-    unsigned long long w[5] = {};
+    std::vector<unsigned long long> w(2 * (size_t)kClockSlots);
     cudaError_t e = cudaDeviceSynchronize();
-    if (e == cudaSuccess) e = cudaMemcpy(w, r->clock_buf, sizeof w, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemset(r->clock_buf + 2, 0, 2 * sizeof(unsigned long long));
+    if (e == cudaSuccess)
+        e = cudaMemcpy(w.data(), r->clock_buf, w.size() * 8, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(r->clock_buf, 0xff, (size_t)kClockSlots * 8);
+    if (e == cudaSuccess) e = cudaMemset(r->clock_buf + kClockSlots, 0, (size_t)kClockSlots * 8);
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_clock_read");
-    if (total_ms) *total_ms = (double)w[2] * 1e-6;
-    if (launches) *launches = (int64_t)w[3];
+    double ns = 0.0;
+    int64_t n = 0;
+    for (int s = 0; s < kClockSlots; ++s) {
+        const unsigned long long t0 = w[s], t1 = w[kClockSlots + s];
+        if (t0 != ~0ull && t1 >= t0) {
+            ns += (double)(t1 - t0);
+            ++n;
+        }
+    }
+    if (total_ms) *total_ms = ns * 1e-6;
+    if (launches) *launches = n;
     return RING_OK;
 }
 

@@ -17,7 +17,8 @@
 //   err       U32  device error word (bounded waits that ran out)
 //   step_sync U32  [n_layer] + 1: the whole-step attention kernel's layer counters and
 //             abort word (few sequences, ring_step), zeroed by every begin_step
-//   clock     U64[5] kernel clock (earliest start, latest end, summed ns, launches, CTAs out)
+//   clock     U64  kernel clock while enabled: earliest start [kClockSlots], latest end
+//             [kClockSlots], then the step counter the begin-step kernel advances
 //
 // Attention work split: n_splits = cluster * groups CTAs per (sequence, kv head), each
 // streaming tiles_per_split consecutive 64-slot tiles.  The `cluster` CTAs of a group are
@@ -52,6 +53,11 @@ constexpr int kMaxStepTiles = 2048;  // slot tiles per (sequence, kv head): flag
 // one state per row from every CTA of the cluster: c * ceil(32 / c) receive slots.
 constexpr int kMaxRecvSlots = 40;
 constexpr int kMaxStepCluster = 16;
+
+// Kernel clock: one (earliest start, latest end) pair per attention launch -- per layer of
+// each of the last kClockSteps steps, slot (step % kClockSteps) * kMaxStepLayers + layer.
+constexpr int kClockSteps = 2048;
+constexpr int kClockSlots = kClockSteps * kMaxStepLayers;
 
 // Per-layer inputs and outputs of one step (layouts as for ring_attend).
 struct StepIO {

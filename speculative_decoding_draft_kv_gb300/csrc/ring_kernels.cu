@@ -242,6 +242,11 @@ k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
     // one small wave: the first attention kernel may settle its CTAs right away (it waits
     // for this grid to finish before reading anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // kernel clock: a new step (the attention launches read the counter after this grid)
+    if (m.clock && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        unsigned int *step = reinterpret_cast<unsigned int *>(m.clock + 2 * kClockSlots);
+        *step = *step + 1u;
+    }
     const int b = blockIdx.x, s = blockIdx.y;
     // the step's records: straight from the host's pinned staging slot when given (no
     // copy ahead of the launch), else from the device copy

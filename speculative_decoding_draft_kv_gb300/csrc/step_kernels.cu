@@ -151,7 +151,8 @@ k_attend_step(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     cluster_wait();
     // Everything below reads ring state written by begin_step.
     pdl_wait();
-    if (threadIdx.x == 0 && m.clock) clock_start(m.clock);
+    int clk_slot = 0;     // kernel clock slot of this launch (thread 0)
+    if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, 0);
 
     // This CTA's chunk of the visible tiles: [vb, ve) in visible order, raw range [tb, te).
     for (int t = threadIdx.x; t < d.n_tiles; t += kThreads) sflags[t] = m.flags[fbase + t];
@@ -601,7 +602,7 @@ k_attend_step(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         if (tid == 0) red_release_add(ys.layer_ctr + l, 1u);
     }
     if (!alive && tid == 0) atomicExch(ys.abort, 1u);
-    if (tid == 0 && m.clock) clock_stop(m.clock, gridDim.x);
+    if (tid == 0 && m.clock) clock_stop(m.clock, clk_slot);
     cluster_sync();          // no CTA leaves while a peer may still push into its shared memory
 }
 

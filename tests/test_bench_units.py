@@ -27,3 +27,29 @@ def test_visible_rows_sum_over_sequences():
     w = synth.workload(1, cap=64, swa_window=24)
     assert bench.visible_rows(w, [0, 10, 100], "full") == (0 + 8) + (10 + 8) + (64 + 8)
     assert bench.visible_rows(w, [0, 10, 100], "swa") == (0 + 8) + (10 + 8) + (24 + 8)
+
+
+def test_oracle_baseline_spreads_units_over_processes():
+    """The oracle leg splits the workload's (sequence, layer) units over host processes,
+    at most one per unit, and reports how many it used."""
+    import os
+
+    import synth
+
+    w = synth.workload(1, cap=64, n_layer=2, n_seq=2)
+    cpu = bench.cpu_baseline(w, "full", n_steps=3)
+    assert cpu["kind"] == "oracle" and cpu["value"] > 0
+    assert cpu["cores"] == min(os.cpu_count() or 1, 4)
+    assert "4 (sequence, layer) units" in cpu["sample"]
+
+
+def test_tile_flags_of_a_mask():
+    import numpy as np
+    inf = -np.inf
+    m = np.full((2, 130), inf, np.float32)
+    m[:, 0:64] = 0          # tile 0: every slot, every row
+    m[0, 70] = 0            # tile 1: one slot, one row
+    m[:, 128:130] = 0       # tile 2: a ragged two-slot tile, fully visible -> mixed
+    np.testing.assert_array_equal(bench._tile_flags(m, 64), [1, 2, 2])
+    m[0, 70] = inf
+    np.testing.assert_array_equal(bench._tile_flags(m, 64), [1, 0, 2])
