@@ -60,10 +60,10 @@ struct Shape {
     static constexpr int kOffBits = kOffQ + kQBytes;
     static constexpr int kOffBars = kOffBits + kStages * kBitsPerStage;
     static constexpr int kOffRecv = kOffBars + 2 * kStages * 8 + 16;
-    // cluster receive buffer: one partial per CTA of the cluster for each of this CTA's
-    // 32 / cluster rows -- 32 rows of numerators + (max, sum) per row in all
-    static constexpr int kRecvAcc = kRows * kHeadDim * 4;
-    static constexpr int kRecvBytes = kRecvAcc + kRows * 8;
+    // cluster receive buffer: one partial per CTA of the cluster for each of the at most
+    // ceil(32 / cluster) rows this CTA finishes -- numerators, then (max, sum) per slot
+    static constexpr int kRecvAcc = kMaxRecvSlots * kHeadDim * 4;
+    static constexpr int kRecvBytes = kRecvAcc + kMaxRecvSlots * 8;
     // key-slice pre-merge scratch (in the idle stage buffers): every warp's partial,
     // 64 numerators + 2 maxima + 2 sums per lane
     static constexpr int kXPer = 68 * 32;
@@ -118,7 +118,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     // it while this CTA may still be streaming
     float *recv_acc = reinterpret_cast<float *>(smem + kOffRecv);
     float2 *recv_ml = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(recv_acc) + SH::kRecvAcc);
-    const int rows_per = kRows / (int)nct;
+    const int rmax = (kRows + (int)nct - 1) / (int)nct;   // rows a cluster rank finishes, at most
 
     const int sp = blockIdx.x, gk = blockIdx.y, s = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -237,6 +237,31 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             ++it;
+        }
+        if constexpr (CLUSTER) {
+            // Every layer's context K/V is final once begin_step has run: with this layer's
+            // copies all issued, pull this CTA's tiles of the next layer into L2, so that the
+            // next layer's CTAs -- some launch only when this grid's CTAs leave -- find them
+            // there.  A hint: the next layer's noise rows, written later, update L2 as usual.
+            if (lane == 0 && layer + 1 < d.n_layer && !s_abort) {
+                const int zn = zrow + d.n_head_kv;
+                for (int u = t0; u < t1; ++u) {
+                    if (flags[u] == 0) continue;
+                    if constexpr (Q8) {
+                        const int rows = min(kTile, d.kv_total - u * kTile);
+                        const int64_t so = ((int64_t)zn * d.kv_total + (int64_t)u * kTile) * (kHeadDim / 32);
+                        tma_prefetch_3d(&tm_k, 0, u * kTile, zn);
+                        tma_prefetch_3d(&tm_v, 0, u * kTile, zn);
+                        bulk_prefetch_l2(m.ks + so, rows * 8);
+                        bulk_prefetch_l2(m.vs + so, rows * 8);
+                    } else {
+                        tma_prefetch_3d(&tm_k, 0, u * kTile, zn);
+                        tma_prefetch_3d(&tm_k, 64, u * kTile, zn);
+                        tma_prefetch_3d(&tm_v, 0, u * kTile, zn);
+                        tma_prefetch_3d(&tm_v, 64, u * kTile, zn);
+                    }
+                }
+            }
         }
         __syncwarp();
         if (!noise_ready) bar_sync(2, SH::kThreads);
@@ -689,8 +714,8 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     ll += wk[k] * x[(66 + j) * 32 + lane];
                 }
                 const int r = rr[j];
-                const int owner = r / rows_per, lr = r - owner * rows_per;
-                float *acc_row = recv_acc + ((int64_t)rank * rows_per + lr) * kHeadDim;
+                const int owner = r * (int)nct / kRows, lr = r - cluster_first_row(owner, (int)nct);
+                float *acc_row = recv_acc + ((int64_t)rank * rmax + lr) * kHeadDim;
                 const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
                 if constexpr (Q8) {
                     // n-tiles 2q / 2q+1 hold the even / odd dimensions of 16q .. 16q+15
@@ -722,7 +747,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     }
                 }
                 if (ksl == 0 && c == 0)
-                    st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rows_per + lr), (uint32_t)owner),
+                    st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rmax + lr), (uint32_t)owner),
                                   mm, ll);
             }
         } else {
@@ -819,28 +844,29 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         return;
     }
 
-    // ---------------- cluster merge: this CTA finishes rows [rank * rows_per, +rows_per) ----
+    // ---------------- cluster merge: this CTA finishes its rows (cluster_first_row) ----
     cluster_sync();     // every partial of this CTA's rows is in its receive buffer
     const int n_part = (int)nct;
-    const int items = rows_per * (kHeadDim / 4);
+    const int row0 = cluster_first_row((int)rank, n_part);
+    const int items = (min(kRows, cluster_first_row((int)rank + 1, n_part)) - row0) * (kHeadDim / 4);
     for (int u = threadIdx.x; u < items; u += SH::kThreads) {
         const int lr = u / (kHeadDim / 4), c4 = (u % (kHeadDim / 4)) * 4;
         float mm = -INFINITY;
-        for (int p = 0; p < n_part; ++p) mm = fmaxf(mm, recv_ml[p * rows_per + lr].x);
+        for (int p = 0; p < n_part; ++p) mm = fmaxf(mm, recv_ml[p * rmax + lr].x);
         const float muse = mm == -INFINITY ? 0.f : mm;
         float l = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p = 0; p < n_part; ++p) {
-            const float2 ml = recv_ml[p * rows_per + lr];
+            const float2 ml = recv_ml[p * rmax + lr];
             const float w = exp2f(ml.x - muse);
             l += w * ml.y;
-            const float4 v = *reinterpret_cast<const float4 *>(recv_acc + ((int64_t)p * rows_per + lr) * kHeadDim + c4);
+            const float4 v = *reinterpret_cast<const float4 *>(recv_acc + ((int64_t)p * rmax + lr) * kHeadDim + c4);
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
         }
-        const int r = (int)rank * rows_per + lr;
+        const int r = row0 + lr;
         if (d.groups == 1) {
             if (r < d.rows) {
                 const int hh = r / d.q_len, i = r - hh * d.q_len;

@@ -240,12 +240,6 @@ int pow2_floor(int x) {
     return p;
 }
 
-int pow2_ceil(int x) {
-    int p = 1;
-    while (p < x) p *= 2;
-    return p;
-}
-
 // Work split of the attention kernel.  A thread-block cluster holds every one of its SM
 // slots until its slowest CTA is done, so clusters (merging through distributed shared
 // memory, no second kernel) are used only when the whole grid fits in one wave of one
@@ -253,23 +247,28 @@ int pow2_ceil(int x) {
 // own group: about four waves of independent CTAs (two per SM) stream the tiles and a
 // small combine kernel merges the per-CTA partials.
 void choose_split(RingDims &d, int sms, int max_cluster, int tps_req) {
-    const int cmax = std::max(1, std::min(16, pow2_floor(std::max(1, max_cluster))));
+    const int cmax = std::max(1, std::min(kMaxStepCluster, max_cluster));
     const int pairs = d.n_seq * d.n_head_kv;
     if (tps_req > 0) {
         const int tps = std::min(tps_req, d.n_tiles);
         const int ns = (d.n_tiles + tps - 1) / tps;
-        d.cluster = std::min(cmax, pow2_floor(ns));
+        d.cluster = std::min(pow2_floor(cmax), pow2_floor(ns));
         while (d.cluster > 1 && attend_cluster_capacity(d.cluster, d.kv_q8 != 0) < 1) d.cluster /= 2;
         d.groups = (ns + d.cluster - 1) / d.cluster;
         d.tiles_per_split = tps;
         d.n_splits = d.cluster * d.groups;
         return;
     }
-    // widest cluster whose whole grid (pairs clusters) is resident at once
-    int c = std::min(cmax, pow2_ceil(d.n_tiles));
-    while (c > 1 && ((int64_t)attend_cluster_capacity(c, d.kv_q8 != 0) < pairs ||
-                     (int64_t)pairs * c > std::max(sms, 1)))
-        c /= 2;
+    // widest cluster (any size up to 16) whose whole grid -- a cluster per pair -- is
+    // resident at once and whose CTAs' row shares fit the receive buffers; then the
+    // narrowest cluster with as few tiles per CTA, so that no CTA is left without tiles
+    auto fits = [&](int c) {
+        return c * ((kRows + c - 1) / c) <= kMaxRecvSlots && (int64_t)pairs * c <= std::max(sms, 1) &&
+               (int64_t)attend_cluster_capacity(c, d.kv_q8 != 0) >= pairs;
+    };
+    int c = std::min(cmax, d.n_tiles);
+    while (c > 1 && !fits(c)) --c;
+    if (c >= 2) c = (d.n_tiles + (d.n_tiles + c - 1) / c - 1) / ((d.n_tiles + c - 1) / c);
     if (c >= 2 && (d.n_tiles + c - 1) / c <= 128) {
         d.cluster = c;
         d.groups = 1;

@@ -54,6 +54,11 @@ constexpr int kMaxStepTiles = 2048;  // slot tiles per (sequence, kv head): flag
 constexpr int kMaxRecvSlots = 40;
 constexpr int kMaxStepCluster = 16;
 
+// The 32 query rows of a (sequence, kv head) split over the c CTAs of a cluster: rank k
+// finishes rows [cluster_first_row(k, c), cluster_first_row(k + 1, c)), at most
+// ceil(32 / c) of them; row r belongs to rank r * c / 32.
+__host__ __device__ __forceinline__ int cluster_first_row(int k, int c) { return (k * kRows + c - 1) / c; }
+
 // Kernel clock: one (earliest start, latest end) pair per attention launch -- per layer of
 // each of the last kClockSteps steps, slot (step % kClockSteps) * kMaxStepLayers + layer.
 constexpr int kClockSteps = 2048;

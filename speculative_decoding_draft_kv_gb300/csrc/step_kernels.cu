@@ -98,8 +98,6 @@ __device__ __forceinline__ StepSync step_sync(const RingDev &m, int n_layer) {
     return y;
 }
 
-// Rows of the 32 query rows that cluster rank k finishes: [first_row(k), first_row(k + 1)).
-__device__ __forceinline__ int first_row(int k, int c) { return (k * kRows + c - 1) / c; }
 
 // ---------------------------------------------------------------------------------
 // Grid: pairs * c CTAs in clusters of c (cooperative, one CTA per SM), kThreads threads.
@@ -540,7 +538,7 @@ k_attend_step(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int r = jj ? r1 : r0;
-                const int owner = r * n_split / kRows, lr = r - first_row(owner, n_split);
+                const int owner = r * n_split / kRows, lr = r - cluster_first_row(owner, n_split);
                 const uint32_t dst = map_rank(smem_u32(recv + (j * rmax + lr) * kRecvStride), (uint32_t)owner);
 #pragma unroll
                 for (int n = 0; n < 16; ++n)
@@ -565,7 +563,8 @@ k_attend_step(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             break;
         }
         {
-            const int row0 = first_row(j, n_split), nrows = min(kRows, first_row(j + 1, n_split)) - row0;
+            const int row0 = cluster_first_row(j, n_split);
+            const int nrows = min(kRows, cluster_first_row(j + 1, n_split)) - row0;
             float *o = io.o[l];
             for (int u = tid; u < nrows * (kHeadDim / 4); u += kConsumers) {
                 const int lr = u / (kHeadDim / 4), c4 = (u % (kHeadDim / 4)) * 4;
