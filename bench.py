@@ -41,8 +41,13 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 17_120_300, "kernel": "a684f3ab371e7c90",
+    "steady_decode_cap4096_s1_l5": {"bytes": 33_012_480, "kernel": "765c8f8a2d59ca89",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
+    # captured on 4 of the 16 sequences (538,197,760 B read + 17,878,528 B written per
+    # launch) and scaled by the sequences a launch processes: every sequence's visible rows
+    # are read once, so the traffic grows in proportion
+    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_197_760 + 17_878_528), "kernel": "765c8f8a2d59ca89",
+                                   "source": "profiles/attend_plain_large_cap32768_s4_l5.md"},
 }
 
 
@@ -641,7 +646,9 @@ def run_gb300(args):
             xsb = StepBench(xw, xkind, args, dev, rank, Kx + Wx)
             xm = xsb.measure(Kx, Wx, None, keep_ring=True)
             xring = xm.pop("ring")
-            xroof = xsb.roofline(xm, peak, peak_kind)
+            xtr = NCU_TRAFFIC.get(xw.name + ("_q8_0" if q8 else "") if xkind == "full" else None)
+            xroof = xsb.roofline(xm, peak, peak_kind,
+                                 xtr["bytes"] if xtr and xtr.get("kernel") == _kernel_source_hash() else None)
             extras.append({"workload": xw.name, "mask": xkind, "value": 1000.0 / xm["ms_per_step"],
                            "unit": UNIT, "ms_per_step": xm["ms_per_step"], "steps": Kx, "warmup": Wx,
                            "step_kv_gbs": xm["step_kv_bytes"] / (xm["ms_per_step"] * 1e-3) / 1e9,
