@@ -239,8 +239,10 @@ def _workload(args):
 
 class StepBench:
     """One workload on the GPU: its prepared inputs, the ring factory and the timed loop.
-    The L2 is flushed between steps (an untimed 512 MiB write) when the ring would fit in
-    it; larger rings are read from HBM anyway."""
+    The L2 is flushed between steps when the ring would fit in it: an untimed 512 MiB
+    write, then an untimed read of another 512 MiB, so the timed kernels find neither
+    useful lines nor the flush's dirty lines (whose write-back they would otherwise pay
+    for); larger rings are read from HBM anyway."""
 
     def __init__(self, w, kind, args, dev, rank, n_steps):
         import torch
@@ -253,6 +255,8 @@ class StepBench:
         self.flush = self.g["cache_bytes"] * w.n_seq < 2 * L2_BYTES
         self.flush_buf = (torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
                           if self.flush else None)
+        self.flush_rd = (torch.zeros(128 * 1024 * 1024, dtype=torch.int32, device=dev)
+                         if self.flush else None)
 
     def new_ring(self, prefill=True):
         import torch
@@ -293,6 +297,7 @@ class StepBench:
             b.record(self.stream)
             if self.flush:
                 self.flush_buf.fill_(j & 0xFF)
+                self.flush_rd.amax()
         return evs
 
     @staticmethod
@@ -521,11 +526,14 @@ def run_gb300(args):
 
         n5 = min(K + W, 400)
         ring = prod_ring()
+        ring.clock_enable(True)
         sb.timed_loop(ring, step_prod, 1, min(W, n5))
         torch.cuda.synchronize()
+        ring.clock_read("produce")                      # forget the warm-up launches
         evs = sb.timed_loop(ring, step_prod, 1 + min(W, n5), n5 - min(W, n5))
         torch.cuda.synchronize()
         ms_prod = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n5 - min(W, n5))
+        clk_ms, clk_n = ring.clock_read("produce")
         assert ring.device_error() == 0
         ring.close()
         ring = prod_ring()
@@ -535,7 +543,8 @@ def run_gb300(args):
         pp = R.ring_profile_read(ring.h)
         ring.close()
         pr = pp["produce"]
-        prod_ms = pr["total_ms"] / max(pr["launches"], 1)
+        prod_ms_isolated = pr["total_ms"] / max(pr["launches"], 1)
+        prod_ms = clk_ms / max(clk_n, 1)
         rows = float(np.mean([int(P.plan[1 + j][3].sum()) for j in range(n5)
                               if int(P.plan[1 + j][3].sum()) > 0] or [0]))
         prod_bytes = (2 * w.n_layer * w.kv_row * H * 2 + rows * H * 2
@@ -552,7 +561,15 @@ def run_gb300(args):
                          "frac": prod_ach / peak, "traffic": prod_traffic, "kernel": "k_produce",
                          "alg_bytes_per_launch": prod_bytes, "launch_ms": prod_ms,
                          "rows_per_launch": rows,
-                         "unit_bytes": "W_k and W_v of every layer + feature rows + K/V rows written"},
+                         "unit_bytes": "W_k and W_v of every layer + feature rows + K/V rows written",
+                         "timing": "device clock of every producer launch inside the timed steps "
+                                   "(globaltimer: earliest CTA past its grid dependency to the last "
+                                   "CTA's exit; the first 4 weight tiles of each CTA are fetched "
+                                   "before the dependency, overlapping the previous kernel)",
+                         "launch_ms_isolated": prod_ms_isolated,
+                         "frac_isolated": prod_bytes / (prod_ms_isolated * 1e-3) / 1e9 / peak,
+                         "isolated": "CUDA events around each launch, launches serialised "
+                                     "(no programmatic overlap), launch latency included"},
         }
         # ---- pass 6: the page's legacy path for comparison -- the whole window produced
         # again every step (ring_recompute_window + ring_attend per layer); one sequence ----
@@ -610,11 +627,16 @@ def run_gb300(args):
 
         n7 = min(K + W, 400)
         ring = draft_ring()
+        ring.clock_enable(True)
         sb.timed_loop(ring, step_draft, 1, min(W, n7))
         torch.cuda.synchronize()
+        for kind_ in ("attend", "produce", "project"):
+            ring.clock_read(kind_)                      # forget the warm-up launches
         evs = sb.timed_loop(ring, step_draft, 1 + min(W, n7), n7 - min(W, n7))
         torch.cuda.synchronize()
-        ms_draft = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n7 - min(W, n7))
+        n7t = max(1, n7 - min(W, n7))
+        ms_draft = max_over_ranks(sb.ms_of(evs), dist, dev) / n7t
+        dclk = {kind_: ring.clock_read(kind_) for kind_ in ("attend", "produce", "project")}
         assert ring.device_error() == 0
         ring.close()
         ring = draft_ring()
@@ -624,11 +646,24 @@ def run_gb300(args):
         pd = R.ring_profile_read(ring.h)
         ring.close()
         n_prof = min(n7, 100)
+        nrow = w.n_seq * w.q_len
+        proj_bytes = (wq.shape[1] + 2 * w.kv_row) * H * 2 + nrow * H * 2 + nrow * (
+            w.n_head * w.head_dim * 4 + 2 * w.kv_row * 2)
+        proj_ms = dclk["project"][0] / max(dclk["project"][1], 1)
+        proj_ach = proj_bytes / (proj_ms * 1e-3) / 1e9
         prod_obj["draft_step"] = {
             "value": 1000.0 / ms_draft * world, "unit": UNIT, "ms_per_step": ms_draft,
             "steps": n7 - min(W, n7), "pattern": pattern,
-            "kernel_ms_per_step": {k: v["total_ms"] / n_prof for k, v in pd.items()
-                                   if k in ("produce", "begin", "attend", "combine")},
+            "device_clock_ms_per_step": {k: v[0] / n7t for k, v in dclk.items()},
+            "projection_roofline": {
+                "bound": "hbm", "achieved": proj_ach, "peak": peak, "unit": "GB/s",
+                "frac": proj_ach / peak, "kernel": "k_produce (noise rows)",
+                "alg_bytes_per_launch": proj_bytes, "launch_ms": proj_ms,
+                "unit_bytes": "W_q, W_k, W_v of one layer + its hidden-state rows + Q (F32), "
+                              "K, V (F16) rows written",
+                "timing": "device clock of every projection launch inside the timed steps"},
+            "kernel_ms_per_step_isolated": {k: v["total_ms"] / n_prof for k, v in pd.items()
+                                            if k in ("produce", "begin", "attend", "combine")},
             "api": "ring_draft_step (producer + begin + per layer: noise Q/K/V projection, attention)"}
         del wq, qn, noise_h
         del feat_all, wk, wv, kn
@@ -701,7 +736,7 @@ def run_gb300(args):
                 "kv_total": g["kv_total"],
                 "tiles_per_split": g["tiles_per_split"], "n_splits": g["n_splits"],
                 "cluster": g["cluster"], "groups": g["groups"], "step_split": g["step_split"],
-                "l2": ("flushed between steps (512 MiB write, untimed)" if sb_flush(g, w)
+                "l2": ("flushed between steps (untimed 512 MiB write, then 512 MiB read)" if sb_flush(g, w)
                        else "inputs larger than L2"),
                 "api": "ring_step (one CUDA graph per step)",
                 "parallelism": f"independent rings x{world}",

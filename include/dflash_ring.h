@@ -253,6 +253,10 @@ int ring_recompute_window(ring_t *r, const int64_t *committed, const void *feat,
  *   K = k_norm(W_k h), V = W_v h (the same W_k, W_v, k_norm as the context rows; pre-RoPE),
  *   and the layer's attention with mask kind mask_kinds[l] (a per-layer full / SWA
  *   pattern, as the Luce draft's sliding-window layers), output o[l].
+ * Layer 0's hidden states (the noise block's embeddings) are there from the start: its
+ * projection shares one launch with the context rows.  Layer l > 0's are read only after
+ * layer l - 1's attention has finished (in a draft model they are computed from its
+ * output).
  * Needs ring_set_producer with wq and q_norm.
  *
  *   feat, row_off, first_pos, n_rows   as in ring_begin_step_features.
@@ -364,24 +368,31 @@ int ring_profile_read(ring_t *r, ring_profile *out);
 int64_t ring_launch_count(const ring_t *r);
 
 /*
- * Kernel clock -- the duration of the ring's attention kernels measured on the device,
- * inside CUDA graphs too: each launch of the attention kernel (one per layer, or the
- * persistent whole-step kernel) records, with the GPU's global nanosecond timer, the
- * earliest moment any of its CTAs passed its grid dependency and the latest moment any
- * CTA was done, in a slot for that layer of that step (every begin-step call starts a
- * step).  The stamps are reductions nobody waits for, so the clock does not slow the
- * launches it times.  (No counterpart on the page: it is how the throughput of the
- * kernel inside a replayed step is measured.)
+ * Kernel clock -- the duration of the ring's kernels measured on the device, inside CUDA
+ * graphs too: each launch records, with the GPU's global nanosecond timer, the earliest
+ * moment any of its CTAs passed its grid dependency and the latest moment any CTA was
+ * done, in a slot for its kind and layer of that step (every begin-step call starts a
+ * step).  Kinds: RING_CLOCK_ATTEND, the attention kernel (one launch per layer, or the
+ * persistent whole-step kernel in slot 0); RING_CLOCK_PRODUCE, the context-row producer
+ * of ring_begin_step_features, ring_recompute_window and ring_draft_step (one launch per
+ * step, slot 0); RING_CLOCK_PROJECT, the noise-block projections of ring_draft_step (one
+ * per layer).  The stamps are reductions nobody waits for, so the clock does not slow the
+ * launches it times.  A launch that starts before its predecessor ends (programmatic
+ * serialization) counts from the moment its dependency resolved: the bytes it fetched
+ * before that -- the first weight or K/V stages -- overlap the previous kernel.  (No
+ * counterpart on the page: it is how the throughput of a kernel inside a pipelined or
+ * replayed step is measured.)
  *
  * ring_clock_enable -- on != 0 starts recording with the next launch (ring_step re-captures
  *   its graph); 0 stops.  Errors: EINVAL.
  * ring_clock_read -- synchronise, return the summed milliseconds of the recorded launches
- *   and their number, and clear them.  Slots cover the last 2048 steps: read at least that
- *   often; two launches of one layer within one step share a slot (their joint span).
- *   Either pointer may be NULL.  Errors: EINVAL, ECUDA.
+ *   of kind `kind` and their number, and clear them.  Slots cover the last 2048 steps:
+ *   read at least that often; two launches of one kind and layer within one step share a
+ *   slot (their joint span).  Either pointer may be NULL.  Errors: EINVAL (kind), ECUDA.
  */
+enum { RING_CLOCK_ATTEND = 0, RING_CLOCK_PRODUCE = 1, RING_CLOCK_PROJECT = 2 };
 int ring_clock_enable(ring_t *r, int32_t on);
-int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches);
+int ring_clock_read(ring_t *r, int32_t kind, double *total_ms, int64_t *launches);
 
 /*
  * ring_check_bounded_wait -- self-test of the kernels' bounded waits (no counterpart on the

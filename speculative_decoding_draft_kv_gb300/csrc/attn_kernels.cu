@@ -282,7 +282,7 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         // dependency
         pdl_wait();
         if (d.single_wave) pdl_trigger();
-        if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, layer);
+        if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, kClockAttend, layer);
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;

@@ -22,6 +22,7 @@
 // normalises, turns and stores its rows: one warp per row, lane l holding columns
 // l, l+32, l+64, l+96, so both members of every rotary pair sit in one lane.
 #include "ring_internal.h"
+#include "ptx.h"
 
 #include <cuda_fp16.h>
 
@@ -41,125 +42,18 @@ constexpr int kPABytes = kPM * kPAPitch;   // feature tile
 constexpr int kPStage = (kPBBytes + kPABytes + 1023) / 1024 * 1024;   // W tiles 1024-aligned
 constexpr int kPConsumers = 128;           // 4 warps, warp w -> columns [32 w, 32 w + 32)
 constexpr int kPThreads = kPConsumers + 32;
-constexpr int kPMaxSplit = 3;            // wider splits measured slower (merge cost)
 constexpr int kPRecvRows = 40;             // >= ks * ceil(32 / ks) for ks = 1 .. 8
 constexpr int kPOffRecv = kPStages * kPStage;                 // [ks][rows_per][128] f32
 constexpr int kPOffBars = kPOffRecv + kPRecvRows * kPN * 4;
 constexpr int kPOffMap = kPOffBars + 2 * kPStages * 8;
 constexpr int kPSmem = 1024 + kPOffMap + kPM * 16;
-constexpr uint64_t kPWaitNs = 2000000000ull;
 static_assert(kPSmem <= 113 * 1024, "two producer CTAs per SM");
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-// bounded: false after kPWaitNs (or 2^30 polls), never an endless spin
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kPWaitNs) return false;
-    }
-    return false;
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-// raise the phase's expected transaction bytes without arriving
-__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-// bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // byte offset of (row r, 16-byte chunk holding column dcol) in a 128-byte-swizzled tile of
 // 64 columns
 __device__ __forceinline__ uint32_t swz64(int r, int dcol) {
     return (uint32_t)(r * 128 + (((dcol >> 3) ^ (r & 7)) << 4));
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Remote shared-memory stores wait until every CTA of the cluster runs: all threads
-// arrive right after start-up and wait before the first remote store.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
-                 : "memory");
-}
-
 // One head's row of a q8_0 slot from a warp: lane holds the values at lane + 32 q4, so
 // 32-value block q4 is one value per lane.  Block maximum by a warp reduction, scale
 // d = max|x| / 127, codes roundf(x * (1 / d)) (half away from zero), all in float32; the
@@ -181,14 +75,16 @@ __device__ __forceinline__ void q8_store_head(int8_t *codes, uint16_t *scales, i
     }
 }
 
-// Grid (ks * m_tiles, heads, layers); clusters of ks CTAs along x when ks > 1.
-// blockIdx.y: K head y (y < n_head_kv), V head y - n_head_kv (y < 2 n_head_kv), else
-// query head y - 2 n_head_kv (noise rows only).  Layer = job.layer0 + blockIdx.z.
+// Grid (units * ks): CTA x works on unit x / ks (the units of job 0, then those of job 1)
+// as rank x % ks of a cluster of ks CTAs.  A unit is one 32-row tile of one output head of
+// one layer: K head y (y < n_head_kv), V head y - n_head_kv (y < 2 n_head_kv), else query
+// head y - 2 n_head_kv (noise rows only).
 __global__ void __launch_bounds__(kPThreads, 2)
-k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_feat,
-          RingDims d, RingDev m, const uint16_t *__restrict__ feat, int hidden, int ks,
-          int64_t m_total, const float *__restrict__ k_norm, float eps,
-          const __grid_constant__ ProduceSeqs seqs, int pdl, ProduceJob job, NoiseOut nout) {
+k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_feat0,
+          const __grid_constant__ CUtensorMap tm_feat1, RingDims d, RingDev m,
+          const uint16_t *__restrict__ feat0, const uint16_t *__restrict__ feat1, int hidden,
+          const float *__restrict__ k_norm, float eps, const __grid_constant__ ProduceSeqs seqs,
+          const __grid_constant__ ProduceLaunch L, NoiseOut nout) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,9 +96,26 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     __shared__ int s_fail, s_valid, s_contig;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ks = L.ks;
     const uint32_t rank = ks > 1 ? cluster_rank() : 0u;
-    const int64_t tile = (int64_t)blockIdx.x / ks;
-    const int yk = blockIdx.y, layer = job.layer0 + (int)blockIdx.z;
+    const int64_t unit = (int64_t)blockIdx.x / ks;
+    const int jb = L.n_jobs > 1 && unit >= L.job[0].units ? 1 : 0;
+    const ProduceJob job = L.job[jb];
+    const int64_t u = jb ? unit - L.job[0].units : unit;
+    const int64_t m_total = job.m_total;
+    const int64_t tiles = (m_total + kPM - 1) / kPM;
+    const int64_t tile = u % tiles;
+    int yk, layer;
+    if (job.mode == 1) {
+        yk = (int)(u / tiles);
+        layer = job.layer;
+    } else {
+        const int64_t hl = u / tiles;
+        yk = (int)(hl % (2 * d.n_head_kv));
+        layer = (int)(hl / (2 * d.n_head_kv));
+    }
+    const CUtensorMap *tm_feat = jb ? &tm_feat1 : &tm_feat0;
+    const uint16_t *__restrict__ feat = jb ? feat1 : feat0;
     const bool is_q = yk >= 2 * d.n_head_kv;
     const bool is_v = !is_q && yk >= d.n_head_kv;
     const int head = is_q ? yk - 2 * d.n_head_kv : (is_v ? yk - d.n_head_kv : yk);
@@ -213,7 +126,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
 
     // packed W tile (layer, K head y or V head y - n_head_kv, k-tile kt) is plane
     // wplane + kt of the packed weights
-    const int wplane = (layer * job.out_heads + yk) * nkt;
+    const int wplane = (layer * L.out_heads + yk) * nkt;
     const int n_pre = min(kPStages, kt1 - kt0);
     if (threadIdx.x == kPConsumers) {
         for (int k = 0; k < kPStages; ++k) {
@@ -230,7 +143,15 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
             tma_load_3d(smem_u32(smem + k * kPStage), &tm_w, 0, 0, wplane + kt0 + k, bar0 + 8 * k);
         }
     }
-    if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // features, ring slots and step records are touched only after the previous kernel
+    // is done
+    pdl_wait();
+    // kernel clock: the step counter is read before this grid releases its dependents (a
+    // begin-step kernel that follows advances it)
+    int clk_slot = 0;
+    if (threadIdx.x == 0 && m.clock)
+        clk_slot = job.mode == 1 ? clock_start(m.clock, kClockProject, job.layer)
+                                 : clock_start(m.clock, kClockProduce, 0);
     if (warp == 0) {
         // row map: packed row index -> (sequence, position, feature row).  Sequence s owns
         // rows [prod_base, prod_base + n_new) of the packed list.
@@ -277,6 +198,9 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
         }
     }
     __syncthreads();
+    // With every CTA of the grid resident, the next kernel's CTAs may settle onto idle SMs
+    // now and do what does not depend on this grid while it finishes.
+    if (L.single_wave) pdl_trigger();
     if (ks > 1) cluster_arrive_relaxed();
 
     if (warp == kPConsumers / 32) {
@@ -303,7 +227,7 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
                 const uint32_t a_bytes = contig ? (uint32_t)kPM * kPK * 2 : (uint32_t)s_valid * kPK * 2;
                 mbar_expect_tx(full, (it >= n_pre ? kPBBytes : 0) + a_bytes);
                 if (it >= n_pre) tma_load_3d(sb, &tm_w, 0, 0, wplane + kt, full);
-                if (contig) tma_load_2d(sa, &tm_feat, kt * kPK, (int)map_frow[0], full);
+                if (contig) tma_load_2d(sa, tm_feat, kt * kPK, (int)map_frow[0], full);
             }
             __syncwarp();
             const int64_t fr = map_frow[lane];      // row `lane` of the tile
@@ -478,6 +402,10 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
         // section 1.2: slot_pos[slot] = p (the begin-step kernel that follows reads it)
         if (layer == 0 && head == 0 && lane == 0) m.slot_pos[(int64_t)s * d.cap + slot] = (int32_t)p;
     }
+    if (m.clock) {
+        bar_sync(1, kPConsumers);         // every consumer warp is past its stores
+        if (threadIdx.x == 0) clock_stop(m.clock, clk_slot);
+    }
 }
 
 }  // namespace
@@ -525,33 +453,70 @@ cudaError_t produce_kernels_init() {
     return cudaFuncSetAttribute(k_produce, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem);
 }
 
-int produce_split(int64_t m_total, int64_t heads_layers, int hidden, int sms) {
+int produce_capacity(int ks, int sms) {
+    if (ks <= 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_produce, kPThreads, kPSmem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return per_sm * sms;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ks, 1, 1);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_produce, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n * ks;
+}
+
+int64_t produce_units(const RingDims &d, int mode, int64_t m_total, int out_heads) {
     const int64_t tiles = (m_total + kPM - 1) / kPM;
-    const int64_t base = tiles * heads_layers;
+    return mode == 1 ? tiles * out_heads : tiles * 2 * d.n_head_kv * d.n_layer;
+}
+
+int produce_split(int64_t units, int hidden, const int *cap) {
     const int nkt = hidden / kPK;
-    int ks = 1;
-    // as many CTAs as two per SM hold (any cluster size up to 8), at least 2 k-tiles each
-    while (ks < kPMaxSplit && base * (ks + 1) <= 2LL * sms && (ks + 1) * 2 <= nkt) ++ks;
-    return ks;
+    int best = 1;
+    for (int ks = 2; ks <= kProduceMaxSplit && 2 * ks <= nkt; ++ks)
+        if (units * ks * 20 <= (int64_t)cap[ks] * 17) best = ks;
+    return best;
 }
 
 cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
-                           const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
-                           int64_t m_total, int ks, const float *k_norm, float eps,
-                           const ProduceSeqs &seqs, bool pdl, const ProduceJob &job,
-                           const NoiseOut &nout, cudaStream_t st) {
-    const int64_t tiles = (m_total + kPM - 1) / kPM;
+                           const CUtensorMap *tm_feat0, const CUtensorMap *tm_feat1,
+                           const uint16_t *feat0, const uint16_t *feat1, int hidden,
+                           const ProduceLaunch &L, const float *k_norm, float eps,
+                           const ProduceSeqs &seqs, const NoiseOut &nout, bool pdl, int resident,
+                           cudaStream_t st) {
+    int64_t units = 0;
+    for (int j = 0; j < L.n_jobs; ++j) units += L.job[j].units;
+    const int64_t ctas = units * L.ks;
+    if (ctas <= 0 || ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    ProduceLaunch lc = L;
+    lc.single_wave = ctas <= resident ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = job.mode == 1 ? dim3((unsigned)(tiles * ks), job.out_heads, 1)
-                                : dim3((unsigned)(tiles * ks), 2 * d.n_head_kv, d.n_layer);
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = kPSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (ks > 1) {
+    if (L.ks > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = ks;
+        attr[na].val.clusterDim.x = L.ks;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -563,8 +528,8 @@ cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMa
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, k_produce, *tm_w, *tm_feat, d, m, feat, hidden, ks, m_total,
-                              k_norm, eps, seqs, pdl ? 1 : 0, job, nout);
+    return cudaLaunchKernelEx(&cfg, k_produce, *tm_w, *tm_feat0, *(tm_feat1 ? tm_feat1 : tm_feat0), d,
+                              m, feat0, feat1, hidden, k_norm, eps, seqs, lc, nout);
 }
 
 }  // namespace dflash

@@ -24,6 +24,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
+// raise the phase's expected transaction bytes without arriving
+__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -65,6 +71,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
 
@@ -241,18 +256,20 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 // Kernel clock, on while `clk` is not NULL (layout in ring_internal.h): every CTA of a
 // launch lowers the launch's earliest-start word once its grid dependency has resolved and
 // raises its latest-end word when it is done -- two reductions whose results nobody waits
-// for, so the clock adds no latency to the launch.  The slot is that of layer `layer` of
-// the current step (the begin-step kernel advances the step counter); the host adds up the
-// spans.  One thread per CTA calls each; clock_stop takes clock_start's slot.
-__device__ __forceinline__ int clock_start(unsigned long long *clk, int layer) {
-    const unsigned int step = *reinterpret_cast<volatile unsigned int *>(clk + 2 * kClockSlots);
-    const int slot = (int)(step % (unsigned int)kClockSteps) * kMaxStepLayers + layer;
+// for, so the clock adds no latency to the launch.  The slot is that of kernel kind `kind`
+// (kClockAttend, kClockProduce, kClockProject) and layer `layer` of the current step (the
+// begin-step kernel advances the step counter); the host adds up the spans.  One thread
+// per CTA calls each; clock_stop takes clock_start's slot.
+__device__ __forceinline__ int clock_start(unsigned long long *clk, int kind, int layer) {
+    const unsigned int step =
+        *reinterpret_cast<const volatile unsigned int *>(clk + 2 * kClockKinds * kClockSlots);
+    const int slot = kind * kClockSlots + (int)(step % (unsigned int)kClockSteps) * kMaxStepLayers + layer;
     atomicMin(&clk[slot], (unsigned long long)global_ns());
     return slot;
 }
 
 __device__ __forceinline__ void clock_stop(unsigned long long *clk, int slot) {
-    atomicMax(&clk[kClockSlots + slot], (unsigned long long)global_ns());
+    atomicMax(&clk[kClockKinds * kClockSlots + slot], (unsigned long long)global_ns());
 }
 
 }  // namespace dflash

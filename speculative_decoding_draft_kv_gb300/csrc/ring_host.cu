@@ -105,6 +105,7 @@ struct dflash_ring {
     uint16_t *noise_k = nullptr, *noise_v = nullptr;
     CUtensorMap tm_w{};
     int sms = 0;
+    int prod_slots[kProduceMaxSplit + 1] = {};   // resident producer CTAs per cluster size
 };
 
 namespace {
@@ -456,7 +457,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     ALLOC(m.part_ml, float2, (size_t)d.n_seq * d.n_head_kv * d.groups * kRows);
     ALLOC(m.err, uint32_t, 1);
     ALLOC(m.inv_freq, double, d.head_dim / 2);
-    ALLOC(r->clock_buf, unsigned long long, 2 * kClockSlots + 1);
+    ALLOC(r->clock_buf, unsigned long long, kClockWords);
     ALLOC(m.probe, uint32_t, 2);
     if (r->step_split > 0) ALLOC(m.step_sync, uint32_t, d.step_sync_words);
 #undef ALLOC
@@ -483,8 +484,9 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     zero(m.rope32, 0, (size_t)d.n_seq * d.q_len * d.head_dim / 2 * sizeof(float2));
     zero(m.err, 0, 4);
     zero(m.probe, 0, 8);
-    zero(r->clock_buf, 0xff, (size_t)kClockSlots * 8);                  // earliest start: none yet
-    zero(r->clock_buf + kClockSlots, 0, ((size_t)kClockSlots + 1) * 8);   // latest end, step counter
+    const size_t clock_bank = (size_t)kClockKinds * kClockSlots;
+    zero(r->clock_buf, 0xff, clock_bank * 8);                          // earliest start: none yet
+    zero(r->clock_buf + clock_bank, 0, (kClockWords - clock_bank) * 8);   // latest end, step counter
     if (m.step_sync) zero(m.step_sync, 0, (size_t)d.step_sync_words * 4);
     std::vector<double> inv(d.head_dim / 2);
     for (int i = 0; i < d.head_dim / 2; ++i)
@@ -796,6 +798,7 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
     r->hidden = p->hidden;
     r->eps = p->eps;
     r->out_heads = out_heads;
+    for (int ks = 1; ks <= kProduceMaxSplit; ++ks) r->prod_slots[ks] = produce_capacity(ks, r->sms);
     r->has_producer = true;
     return RING_OK;
 }
@@ -803,12 +806,19 @@ int ring_set_producer(ring_t *r, const ring_producer *p) {
 }  // extern "C"
 
 namespace {
+// A draft step's first-layer noise rows, projected in the same launch as its context rows.
+struct NoiseJob {
+    const void *h;            // every layer's hidden states [n_layer][n_seq][q_len][hidden]
+    const CUtensorMap *tm;    // 2-D TMA map over them
+};
+
 int begin_step_features(ring_t *r, const char *who, const int64_t *committed, const void *feat,
                         const int64_t *row_off, const int64_t *first_pos, int64_t n_rows,
-                        void *stream, bool full_window) {
+                        void *stream, bool full_window, const NoiseJob *noise = nullptr) {
     if (!r) return RING_EINVAL;
     if (!r->has_producer)
         return fail(r, RING_ESTATE, "%s: no producer set (ring_set_producer)", who);
+    const RingDims &d = r->d;
     std::vector<SeqStep> st;
     int64_t max_bulk = 0;
     int rc = validate_step(r, who, committed, feat, feat, row_off, first_pos, n_rows, st, max_bulk,
@@ -820,13 +830,12 @@ int begin_step_features(ring_t *r, const char *who, const int64_t *committed, co
         m_total += x.n_new;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // Few sequences: the row ranges travel as kernel parameters, so the producer goes first
-    // and may overlap the previous kernel (programmatic serialization); the step state is
-    // staged after it.  Otherwise the producer reads the staged step state.
+    // Few sequences: the row ranges travel as kernel parameters; otherwise the projection
+    // reads the staged step records from the device.
     ProduceSeqs ps{};
-    if (r->d.n_seq <= kProduceParamSeqs) {
-        ps.n = r->d.n_seq;
-        for (int s = 0; s < r->d.n_seq; ++s) {
+    if (d.n_seq <= kProduceParamSeqs) {
+        ps.n = d.n_seq;
+        for (int s = 0; s < d.n_seq; ++s) {
             ps.base[s] = st[s].prod_base;
             ps.n_new[s] = st[s].n_new;
             ps.start[s] = st[s].start;
@@ -836,34 +845,48 @@ int begin_step_features(ring_t *r, const char *who, const int64_t *committed, co
     CUtensorMap tm_feat{};
     if (m_total > 0 && !encode_weight_map(&tm_feat, feat, r->hidden, n_rows, 32))
         return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
-    auto produce = [&](bool pdl) -> cudaError_t {
-        if (m_total == 0) return cudaSuccess;
-        const int ks = produce_split(m_total, 2LL * r->d.n_head_kv * r->d.n_layer, r->hidden, r->sms);
-        const ProduceJob job{0, 0, r->out_heads};
-        return timed(r, 5, cs, [&] {
-            return launch_produce(r->d, r->m, &r->tm_w, &tm_feat,
-                                  static_cast<const uint16_t *>(feat), r->hidden, m_total, ks,
-                                  r->k_norm, r->eps, ps, pdl, job, NoiseOut{}, cs);
-        });
-    };
-    cudaError_t e = cudaSuccess;
-    if (ps.n > 0) {
-        e = produce(!r->profiling);
-        if (e != cudaSuccess) return cuda_fail(r, e, who);
-    }
-    // the producer reads the records from the device only when they are not its
-    // parameters (more sequences than fit there)
+    // Order: the step records, the projection, then the begin-step kernel.  The projection
+    // streams its first weight tiles while the previous kernel (the last reader of the ring)
+    // finishes and waits for it before it reads rows or writes slots; the begin-step kernel
+    // computes the slot_pos of the new rows itself, so it runs alongside the projection once
+    // that has passed its wait, and waits for it only before exiting.
     int slot = 0;
-    rc = stage_and_bulk(r, who, st, nullptr, nullptr, n_rows, 0, cs, &slot, ps.n == 0);
+    rc = stage_and_bulk(r, who, st, nullptr, nullptr, n_rows, 0, cs, &slot, ps.n == 0 && m_total > 0);
     if (rc != RING_OK) return rc;
-    if (ps.n == 0) {
-        e = produce(false);
-        if (e != cudaSuccess) return cuda_fail(r, e, who);
+    cudaError_t e = cudaSuccess;
+    const bool produce = m_total > 0 || noise;
+    if (produce) {
+        ProduceLaunch L{};
+        const uint16_t *in[2] = {nullptr, nullptr};
+        const CUtensorMap *tm[2] = {nullptr, nullptr};
+        int64_t units = 0;
+        if (m_total > 0) {
+            L.job[L.n_jobs] = ProduceJob{0, 0, m_total, produce_units(d, 0, m_total, r->out_heads)};
+            in[L.n_jobs] = static_cast<const uint16_t *>(feat);
+            tm[L.n_jobs] = &tm_feat;
+            units += L.job[L.n_jobs++].units;
+        }
+        if (noise) {
+            const int64_t nrow = (int64_t)d.n_seq * d.q_len;
+            L.job[L.n_jobs] = ProduceJob{1, 0, nrow, produce_units(d, 1, nrow, r->out_heads)};
+            in[L.n_jobs] = static_cast<const uint16_t *>(noise->h);
+            tm[L.n_jobs] = noise->tm;
+            units += L.job[L.n_jobs++].units;
+        }
+        L.ks = produce_split(units, r->hidden, r->prod_slots);
+        L.out_heads = r->out_heads;
+        const NoiseOut nout{r->noise_q, r->noise_k, r->noise_v, r->q_norm};
+        e = timed(r, 5, cs, [&] {
+            return launch_produce(d, r->m, &r->tm_w, tm[0], tm[1], in[0], in[1], r->hidden, L,
+                                  r->k_norm, r->eps, ps, nout, !r->profiling, r->prod_slots[L.ks],
+                                  cs);
+        });
     }
-    e = timed(r, 1, cs, [&] {
-        return launch_begin_step(r->d, r->m, nullptr, nullptr, n_rows, !r->profiling,
-                                 slot_steps(r, slot), cs);
-    });
+    if (e == cudaSuccess)
+        e = timed(r, 1, cs, [&] {
+            return launch_begin_step(d, r->m, nullptr, nullptr, n_rows, !r->profiling,
+                                     slot_steps(r, slot), cs, produce);
+        });
     mark_slot(r, slot, cs);
     if (e != cudaSuccess) return cuda_fail(r, e, who);
     r->last_was_begin = true;
@@ -907,25 +930,40 @@ int ring_draft_step(ring_t *r, const int64_t *committed, const void *feat,
     CUtensorMap tm_h{};
     if (!encode_weight_map(&tm_h, noise_h, r->hidden, nrow * d.n_layer, 32))
         return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
-    int rc = begin_step_features(r, who, committed, feat, row_off, first_pos, n_rows, stream, false);
+    // layer 0's hidden states are there from the start (the noise block's embeddings): its
+    // projection shares the context rows' launch
+    const NoiseJob first{noise_h, &tm_h};
+    int rc = begin_step_features(r, who, committed, feat, row_off, first_pos, n_rows, stream, false,
+                                 &first);
     if (rc != RING_OK) return rc;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const int ks = produce_split(nrow, r->out_heads, r->hidden, r->sms);
+    const int64_t units = produce_units(d, 1, nrow, r->out_heads);
+    const int ks = produce_split(units, r->hidden, r->prod_slots);
     const NoiseOut nout{r->noise_q, r->noise_k, r->noise_v, r->q_norm};
     ProduceSeqs ps{};
+    const bool pdl = !r->profiling;
     for (int l = 0; l < d.n_layer; ++l) {
-        // this layer's noise rows (Q, K, V from its hidden states), then its attention
-        const ProduceJob job{1, l, r->out_heads};
-        const bool pdl = !r->profiling;
-        cudaError_t e = timed(r, 5, cs, [&] {
-            return launch_produce(d, r->m, &r->tm_w, &tm_h, static_cast<const uint16_t *>(noise_h),
-                                  r->hidden, nrow, ks, r->k_norm, r->eps, ps, pdl, job, nout, cs);
-        });
-        if (e != cudaSuccess) return cuda_fail(r, e, who);
+        cudaError_t e = cudaSuccess;
+        if (l > 0) {
+            // this layer's noise rows (Q, K, V from its hidden states, which in a draft
+            // model come from the layer before: read after that kernel is done)
+            ProduceLaunch L{};
+            L.job[0] = ProduceJob{1, l, nrow, units};
+            L.n_jobs = 1;
+            L.ks = ks;
+            L.out_heads = r->out_heads;
+            e = timed(r, 5, cs, [&] {
+                return launch_produce(d, r->m, &r->tm_w, &tm_h, nullptr,
+                                      static_cast<const uint16_t *>(noise_h), nullptr, r->hidden, L,
+                                      r->k_norm, r->eps, ps, nout, pdl, r->prod_slots[ks], cs);
+            });
+            if (e != cudaSuccess) return cuda_fail(r, e, who);
+        }
         const int64_t qoff = (int64_t)l * nrow * d.n_head * d.head_dim;
         const int64_t koff = (int64_t)l * nrow * d.kv_row;
         // the projection writes no ring state, so the attention may fill its first stages
-        // early -- except after the begin-step kernel (layer 0), as in ring_step
+        // early -- except right after the begin-step kernel (layer 0), whose completion
+        // stands for this step's context rows
         r->last_was_begin = l == 0;
         e = launch_layer(r, l, mask_kinds[l], r->noise_q + qoff, r->noise_k + koff,
                          r->noise_v + koff, o[l], pdl, cs);
@@ -1198,14 +1236,21 @@ int ring_clock_enable(ring_t *r, int32_t on) {
     return RING_OK;
 }
 
-int ring_clock_read(ring_t *r, double *total_ms, int64_t *launches) {
+int ring_clock_read(ring_t *r, int32_t kind, double *total_ms, int64_t *launches) {
     if (!r) return RING_EINVAL;
+    if (kind < 0 || kind >= kClockKinds)
+        return fail(r, RING_EINVAL, "ring_clock_read: kind %d outside [0, %d)", kind, kClockKinds);
+    const size_t bank = (size_t)kClockKinds * kClockSlots;
+    unsigned long long *t0w = r->clock_buf + (size_t)kind * kClockSlots;
+    unsigned long long *t1w = r->clock_buf + bank + (size_t)kind * kClockSlots;
     std::vector<unsigned long long> w(2 * (size_t)kClockSlots);
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
-        e = cudaMemcpy(w.data(), r->clock_buf, w.size() * 8, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemset(r->clock_buf, 0xff, (size_t)kClockSlots * 8);
-    if (e == cudaSuccess) e = cudaMemset(r->clock_buf + kClockSlots, 0, (size_t)kClockSlots * 8);
+        e = cudaMemcpy(w.data(), t0w, (size_t)kClockSlots * 8, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(w.data() + kClockSlots, t1w, (size_t)kClockSlots * 8, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(t0w, 0xff, (size_t)kClockSlots * 8);
+    if (e == cudaSuccess) e = cudaMemset(t1w, 0, (size_t)kClockSlots * 8);
     if (e != cudaSuccess) return cuda_fail(r, e, "ring_clock_read");
     double ns = 0.0;
     int64_t n = 0;

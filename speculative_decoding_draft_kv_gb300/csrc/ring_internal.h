@@ -17,8 +17,9 @@
 //   err       U32  device error word (bounded waits that ran out)
 //   step_sync U32  [n_layer] + 1: the whole-step attention kernel's layer counters and
 //             abort word (few sequences, ring_step), zeroed by every begin_step
-//   clock     U64  kernel clock while enabled: earliest start [kClockSlots], latest end
-//             [kClockSlots], then the step counter the begin-step kernel advances
+//   clock     U64  kernel clock while enabled: earliest start [kClockKinds][kClockSlots],
+//             latest end [kClockKinds][kClockSlots], then the step counter the begin-step
+//             kernel advances
 //
 // Attention work split: n_splits = cluster * groups CTAs per (sequence, kv head), each
 // streaming tiles_per_split consecutive 64-slot tiles.  The `cluster` CTAs of a group are
@@ -59,10 +60,14 @@ constexpr int kMaxStepCluster = 16;
 // ceil(32 / c) of them; row r belongs to rank r * c / 32.
 __host__ __device__ __forceinline__ int cluster_first_row(int k, int c) { return (k * kRows + c - 1) / c; }
 
-// Kernel clock: one (earliest start, latest end) pair per attention launch -- per layer of
-// each of the last kClockSteps steps, slot (step % kClockSteps) * kMaxStepLayers + layer.
+// Kernel clock: one (earliest start, latest end) pair per launch of each kind -- per layer
+// of each of the last kClockSteps steps, slot (step % kClockSteps) * kMaxStepLayers + layer
+// within the kind's bank: attention (ring_attend, ring_step, ring_draft_step), the
+// context-row producer (layer 0: one launch per step), the noise-block projections.
 constexpr int kClockSteps = 2048;
 constexpr int kClockSlots = kClockSteps * kMaxStepLayers;
+constexpr int kClockAttend = 0, kClockProduce = 1, kClockProject = 2, kClockKinds = 3;
+constexpr size_t kClockWords = 2 * (size_t)kClockKinds * kClockSlots + 1;
 
 // Per-layer inputs and outputs of one step (layouts as for ring_attend).
 struct StepIO {
@@ -170,9 +175,12 @@ cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16
 // pdl: launch with programmatic stream serialization (the kernel waits on its
 // predecessor before touching ring state).  host_steps: the step records in pinned host
 // memory, read by the kernel directly (NULL: read m.steps, copied to the device before).
+// after_producer: the predecessor is the producer of this step's rows (k_rows NULL): the
+// kernel runs alongside it and waits for it only before exiting.
 cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
-                              const SeqStep *host_steps, cudaStream_t st);
+                              const SeqStep *host_steps, cudaStream_t st,
+                              bool after_producer = false);
 
 // Row ranges of the producer's packed row list, passed by value (no copy to the device
 // before the launch, so the launch can overlap the previous kernel) when n_seq is small.
@@ -194,15 +202,30 @@ struct NoiseOut {
     const float *q_norm;      // [n_layer][128]
 };
 
-// One launch of the projection kernel.
-//   mode 0: the step's new context rows (packed over sequences), every layer (grid z),
-//           K and V heads, written into the ring with RoPE at their positions;
-//   mode 1: the noise-block rows of layer `layer0` (n_seq * q_len rows of its hidden
-//           states), Q, K and V heads, written to NoiseOut.
+// One kind of rows in a projection launch.
+//   mode 0: the step's new context rows (m_total, packed over sequences), every layer, K and
+//           V heads, written into the ring with RoPE at their positions (feat: the fused
+//           target features);
+//   mode 1: the noise-block rows of layer `layer` (m_total = n_seq * q_len rows of its
+//           hidden states; feat: every layer's hidden states, layer-major), Q, K and V
+//           heads, written to NoiseOut.
 struct ProduceJob {
     int mode;
-    int layer0;
+    int layer;
+    int64_t m_total;
+    int64_t units;            // 32-row tiles x heads (x layers in mode 0)
+};
+
+// One launch of the projection kernel: one or two jobs (a draft step's context rows and
+// its first layer's noise rows share a launch), their work units numbered job after job,
+// each unit's hidden dimension split over a cluster of ks CTAs.
+struct ProduceLaunch {
+    ProduceJob job[2];
+    int n_jobs;
+    int ks;
     int out_heads;            // heads in the packed weights per layer: 2 n_head_kv (+ n_head)
+    int single_wave;          // set by launch_produce: every CTA of the grid is resident at
+                              // once, so the kernel may release its dependents early
 };
 
 // ---- launchers (produce_kernels.cu) ----
@@ -214,23 +237,34 @@ cudaError_t launch_pack_weights(const uint16_t *wk, const uint16_t *wv, const ui
                                 uint16_t *out, int n_layer, int n_head_kv, int n_q_heads,
                                 int hidden, cudaStream_t st);
 size_t produce_smem_bytes();
-// split of the hidden dimension over a cluster (1, 2, 4 or 8 CTAs) for m_total rows and
-// heads_layers (heads x layers) CTAs per row tile
-int produce_split(int64_t m_total, int64_t heads_layers, int hidden, int sms);
-// Context rows of the step's m_total new positions (packed over sequences by
-// SeqStep::prod_base) from F16 features [rows][hidden]: K = RoPE(k_norm(W_k x)), V = W_v x,
-// both rounded to F16 and stored in their ring slots, with slot_pos.  tm_w: 3-D TMA map
-// over the packed weights (launch_pack_weights): 64 x 128 x 1 boxes, 128-byte swizzle.
-// seqs.n == 0: the row ranges are read from m.steps (staged before the launch).
-// pdl: launch with programmatic stream serialization; the kernel streams its first weight
-// tiles before its grid dependency resolves (weights are constant while steps run) and
-// waits before it reads features or touches ring state.
-// tm_feat: 2-D TMA map over the features [n_rows][hidden], 64 x 32 boxes, 128-byte swizzle.
+// Split of the hidden dimension over a cluster of 1 .. kProduceMaxSplit CTAs for `units`
+// work units: the widest that keeps the grid within 85% of the CTAs resident at once
+// (cap[ks], produce_capacity) -- one wave even while the previous kernel still holds some
+// SMs -- with at least two 64-column k-tiles per CTA.
+constexpr int kProduceMaxSplit = 8;
+int produce_split(int64_t units, int hidden, const int *cap);
+// CTAs of a producer grid with clusters of ks that are resident at once on sms SMs (0 if
+// the occupancy query fails)
+int produce_capacity(int ks, int sms);
+// Units of a job: 32-row tiles x (2 n_head_kv x n_layer) in mode 0, x out_heads in mode 1.
+int64_t produce_units(const RingDims &d, int mode, int64_t m_total, int out_heads);
+// The projection launch.  tm_w: 3-D TMA map over the packed weights (launch_pack_weights):
+// 64 x 128 x 1 boxes, 128-byte swizzle.  tm_feat[j], feat[j]: job j's input rows, F16
+// [rows][hidden], 16-byte aligned, with a 2-D TMA map of 64 x 32 boxes, 128-byte swizzle.
+// Mode 0: K = RoPE(k_norm(W_k x)), V = W_v x, rounded to F16 (or quantised to q8_0) and
+// stored in their ring slots, with slot_pos; seqs.n == 0: the row ranges are read from
+// m.steps (staged before the launch).  Mode 1: Q = q_norm(W_q h), K = k_norm(W_k h),
+// V = W_v h into nout.  pdl: launch with programmatic stream serialization; the kernel
+// streams its first weight tiles at once (weights are constant while steps run) and waits
+// for its predecessor before it reads rows or step records or writes anything; it reads
+// the kernel clock's step counter before it releases its dependents.  resident:
+// produce_capacity(L.ks).
 cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
-                           const CUtensorMap *tm_feat, const uint16_t *feat, int hidden,
-                           int64_t m_total, int ks, const float *k_norm, float eps,
-                           const ProduceSeqs &seqs, bool pdl, const ProduceJob &job,
-                           const NoiseOut &nout, cudaStream_t st);
+                           const CUtensorMap *tm_feat0, const CUtensorMap *tm_feat1,
+                           const uint16_t *feat0, const uint16_t *feat1, int hidden,
+                           const ProduceLaunch &L, const float *k_norm, float eps,
+                           const ProduceSeqs &seqs, const NoiseOut &nout, bool pdl, int resident,
+                           cudaStream_t st);
 
 // ---- shared host helpers (ring_host.cu) ----
 // 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],

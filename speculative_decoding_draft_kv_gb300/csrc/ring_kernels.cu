@@ -179,9 +179,10 @@ __device__ void pad_row(const RingDims &d, const RingDev &m, int s) {
 }
 
 // Masks, visibility bits and flags of one 64-slot tile.  The slot_pos a slot holds after
-// this step is computed here rather than read back: a slot written by this step's
-// fold-in rows holds start + k with k = (slot - start) mod cap < fold_rows; any other
-// slot keeps its value (already updated by the bulk kernels, which run before this one).
+// this step is computed here rather than read back: a slot written by this step's rows
+// holds start + k with k = (slot - start) mod cap < n_new (whichever kernel writes it: the
+// fold-in blocks of this grid, the bulk kernels before it, or the producer, which may run
+// after it); any other slot keeps its value.
 // Threads 0-63 own one slot each (warps 0 and 1); warps 2 and 3 only join the barriers.
 __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, const SeqStep &st) {
     const int slot = tile * kTile + (int)threadIdx.x;
@@ -193,7 +194,7 @@ __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, 
     int noise_j = -1;
     if (active && slot < d.cap) {
         const int64_t k = ((int64_t)slot - st.start % d.cap + d.cap) % d.cap;
-        const int64_t p = k < st.fold_rows ? st.start + k
+        const int64_t p = k < st.n_new ? st.start + k
                                            : (int64_t)m.slot_pos[(int64_t)s * d.cap + slot];
         ctx_full = p >= st.lo && p < st.committed;
         ctx_swa = p >= st.swa_lo && p < st.committed;
@@ -234,26 +235,18 @@ __device__ void mask_tile(const RingDims &d, const RingDev &m, int s, int tile, 
 //   blocks [0, a_step)                 fold-in row i (real row, or pad row to trash)
 //   blocks [a_step, a_step + n_tiles)  mask rows and flags of one tile
 //   block  a_step + n_tiles            cos/sin of the noise positions committed + i
-__global__ void __launch_bounds__(kBeginThreads)
-k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
-             const uint16_t *__restrict__ v_rows, int64_t n_rows, const SeqStep *host_steps) {
-    __shared__ float2 cs[kHeadDim / 2];
-    pdl_wait();   // the previous step's attention must be done with the ring state
-    // one small wave: the first attention kernel may settle its CTAs right away (it waits
-    // for this grid to finish before reading anything)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // kernel clock: a new step (the attention launches read the counter after this grid)
-    if (m.clock && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-        unsigned int *step = reinterpret_cast<unsigned int *>(m.clock + 2 * kClockSlots);
-        *step = *step + 1u;
-    }
+// The work of one block of the begin-step kernel.
+__device__ __forceinline__ void begin_block(const RingDims &d, const RingDev &m,
+                                            const uint16_t *__restrict__ k_rows,
+                                            const uint16_t *__restrict__ v_rows, int64_t n_rows,
+                                            const SeqStep *host_steps, float2 *cs) {
     const int b = blockIdx.x, s = blockIdx.y;
     // the step's records: straight from the host's pinned staging slot when given (no
     // copy ahead of the launch), else from the device copy
     const SeqStep st = host_steps ? host_steps[s] : m.steps[s];
     if (b < d.a_step) {
         if (b < st.fold_rows) {
-            if (!k_rows) return;        // the producer kernel already wrote the row and slot_pos
+            if (!k_rows) return;        // the producer kernel writes the row and slot_pos
             const int64_t p = st.start + b;
             rope_table(cs, p, m.inv_freq, d.head_dim / 2);
             __syncthreads();
@@ -273,9 +266,33 @@ k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
         m.rope32[((int64_t)s * d.q_len + i) * half + j] = rope_angle_cs(st.committed + i, m.inv_freq[j]);
     }
     // the whole-step attention kernel's counters start every step at zero (the previous
-    // step's kernel has finished: this grid waited for it above)
+    // step's kernel has finished: this grid, or the producer before it, waited for it)
     if (s == 0)
         for (int idx = threadIdx.x; idx < d.step_sync_words; idx += blockDim.x) m.step_sync[idx] = 0u;
+}
+
+// wait_end = 0: the previous kernel may still read the ring state -- wait for it first.
+// wait_end = 1: the previous kernel is the producer of this step's rows, which waited for
+// everything before it and writes none of what this grid reads or writes (the new rows'
+// slot_pos is computed here, not read): run alongside it, and wait for it only before
+// exiting, so that the kernels after this grid see its rows too.
+__global__ void __launch_bounds__(kBeginThreads)
+k_begin_step(RingDims d, RingDev m, const uint16_t *__restrict__ k_rows,
+             const uint16_t *__restrict__ v_rows, int64_t n_rows, const SeqStep *host_steps,
+             int wait_end) {
+    __shared__ float2 cs[kHeadDim / 2];
+    if (!wait_end) pdl_wait();
+    // one small wave: the first attention kernel may settle its CTAs right away (it waits
+    // for this grid to finish before reading anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // kernel clock: a new step (the attention launches read the counter after this grid;
+    // a producer before it read it before it let this grid start)
+    if (m.clock && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        unsigned int *step = reinterpret_cast<unsigned int *>(m.clock + 2 * kClockKinds * kClockSlots);
+        *step = *step + 1u;
+    }
+    begin_block(d, m, k_rows, v_rows, n_rows, host_steps, cs);
+    if (wait_end) pdl_wait();
 }
 
 // Bulk append, one chunk of bulk_chunk rows: grid (bulk_chunk, n_seq).  Only sequences
@@ -307,7 +324,7 @@ cudaError_t launch_bulk_append(const RingDims &d, const RingDev &m, const uint16
 
 cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_t *k_rows,
                               const uint16_t *v_rows, int64_t n_rows, bool pdl,
-                              const SeqStep *host_steps, cudaStream_t st) {
+                              const SeqStep *host_steps, cudaStream_t st, bool after_producer) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.a_step + d.n_tiles + 1, d.n_seq);
     cfg.blockDim = dim3(kBeginThreads);
@@ -317,7 +334,8 @@ cudaError_t launch_begin_step(const RingDims &d, const RingDev &m, const uint16_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_begin_step, d, m, k_rows, v_rows, n_rows, host_steps);
+    return cudaLaunchKernelEx(&cfg, k_begin_step, d, m, k_rows, v_rows, n_rows, host_steps,
+                              after_producer ? 1 : 0);
 }
 
 }  // namespace dflash

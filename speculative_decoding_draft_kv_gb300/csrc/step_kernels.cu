@@ -150,7 +150,7 @@ k_attend_step(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Everything below reads ring state written by begin_step.
     pdl_wait();
     int clk_slot = 0;     // kernel clock slot of this launch (thread 0)
-    if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, 0);
+    if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, kClockAttend, 0);
 
     // This CTA's chunk of the visible tiles: [vb, ve) in visible order, raw range [tb, te).
     for (int t = threadIdx.x; t < d.n_tiles; t += kThreads) sflags[t] = m.flags[fbase + t];

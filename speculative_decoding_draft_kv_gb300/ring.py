@@ -135,7 +135,7 @@ def _load():
         "ring_draft_step": ([vp, p64, vp, p64, p64, i64, vp, ctypes.POINTER(i32),
                              ctypes.POINTER(vp), vp], ctypes.c_int),
         "ring_clock_enable": ([vp, i32], ctypes.c_int),
-        "ring_clock_read": ([vp, ctypes.POINTER(ctypes.c_double), p64], ctypes.c_int),
+        "ring_clock_read": ([vp, i32, ctypes.POINTER(ctypes.c_double), p64], ctypes.c_int),
         "ring_check_bounded_wait": ([vp, i32, i32, vp], ctypes.c_int),
         "ring_attend_static_device_error": ([ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     }
@@ -425,11 +425,16 @@ def ring_clock_enable(h, on=True):
     _check(_load().ring_clock_enable(h, 1 if on else 0), h, "ring_clock_enable")
 
 
-def ring_clock_read(h):
-    """(summed milliseconds, launches) of the attention kernel since the last read."""
+CLOCK_KINDS = {"attend": 0, "produce": 1, "project": 2}
+
+
+def ring_clock_read(h, kind="attend"):
+    """(summed milliseconds, launches) of one kernel kind since the last read: "attend"
+    (attention), "produce" (context-row producer) or "project" (noise projections)."""
     ms = ctypes.c_double()
     n = ctypes.c_int64()
-    _check(_load().ring_clock_read(h, ctypes.byref(ms), ctypes.byref(n)), h, "ring_clock_read")
+    _check(_load().ring_clock_read(h, CLOCK_KINDS[kind], ctypes.byref(ms), ctypes.byref(n)), h,
+           "ring_clock_read")
     return ms.value, n.value
 
 
@@ -535,8 +540,8 @@ class Ring:
     def clock_enable(self, on=True):
         ring_clock_enable(self.h, on)
 
-    def clock_read(self):
-        return ring_clock_read(self.h)
+    def clock_read(self, kind="attend"):
+        return ring_clock_read(self.h, kind)
 
     def check_bounded_wait(self, which, limit_us, stream=None):
         ring_check_bounded_wait(self.h, which, limit_us, stream)

@@ -488,6 +488,45 @@ def test_draft_step_small_rings_mixed_pattern():
         run.close()
 
 
+def test_draft_step_kernel_clock_counts_each_kind():
+    """The device clock keeps one span per launch and kind through ring_draft_step: the
+    context-row producer once per step with new rows, the noise projections and the
+    attention once per layer; each kind's time fits inside the steps' event time, and the
+    outputs stay those of the float64 route."""
+    w = synth.workload(1, n_layer=3, n_seq=2, swa_window=24)
+    run = DraftRun(w, 192, ["full", "swa", "full"])
+    try:
+        run.step(0, [5, 0])
+        run.ring.clock_enable(True)
+        for kind in ("attend", "produce", "project"):
+            assert run.ring.clock_read(kind) == (0.0, 0)
+        steps = [[14, 9], [60, 41], [63, 200], [63, 200], [150, 205]]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        outs = [run.step(1 + t, c) for t, c in enumerate(steps)]
+        b.record()
+        torch.cuda.synchronize()
+        ev_ms = a.elapsed_time(b)
+        got = {kind: run.ring.clock_read(kind) for kind in ("attend", "produce", "project")}
+        prev = [[5, 0]] + steps[:-1]
+        with_rows = sum(1 for c, p in zip(steps, prev) if c != p)   # no rows: no producer launch
+        assert got["produce"][1] == with_rows
+        assert got["project"][1] == w.n_layer * len(steps)
+        assert got["attend"][1] == w.n_layer * len(steps)
+        for kind, (ms, n) in got.items():
+            assert 0.0 < ms <= ev_ms, kind
+        t = len(steps)
+        for layer in range(w.n_layer):
+            for s in range(w.n_seq):
+                assert_close(outs[-1][layer][s], run.expected_draft(t, layer, s),
+                             f"step {t} layer {layer} seq {s}")
+        assert R.library().ring_clock_read(run.ring.h, 3, None, None) == R.RING_EINVAL
+        run.ring.clock_enable(False)
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
 def test_draft_step_full_size():
     """cap 4096, 5 layers, hidden 4096: prefill then decode steps, sampled heads."""
     w = synth.workload(2)
