@@ -131,6 +131,8 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const int qw = (d.q_len + 1) & ~1;
 
     if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
         for (int k = 0; k < kStages; ++k) {
             mbar_init(bar0 + 8 * k, 1);
             mbar_init(bar0 + 8 * (kStages + k), CW);

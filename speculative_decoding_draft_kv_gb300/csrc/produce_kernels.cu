@@ -129,6 +129,8 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
     const int wplane = (layer * L.out_heads + yk) * nkt;
     const int n_pre = min(kPStages, kt1 - kt0);
     if (threadIdx.x == kPConsumers) {
+        prefetch_tensormap(&tm_w);
+        prefetch_tensormap(tm_feat);
         for (int k = 0; k < kPStages; ++k) {
             mbar_init(bar0 + 8 * k, 1);          // the producer's expect_tx arrival
             mbar_init(bar0 + 8 * (kPStages + k), kPConsumers / 32);

@@ -207,6 +207,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *tm, int x, in
                  : "memory");
 }
 
+// fetch a kernel parameter's TMA descriptor ahead of its first copy
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
                  "r"(bytes) : "memory");
