@@ -37,6 +37,7 @@ METRIC = "ring attention steps/s and HBM GB/s (% of GB300 peak) at cap 4096, q_l
 UNIT = "steps/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
@@ -72,6 +73,16 @@ def _peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def _tensor_peak():
+    """(bf16 dense TFLOP/s, source): MEASURED_PEAKS.json's burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def _dist_env():
@@ -598,10 +609,22 @@ def run_gb300(args):
             torch.cuda.synchronize()
             pl = R.ring_profile_read(ring.h)["produce"]
             ring.close()
+            rows6 = min(int(P.plan[1][0][0]), w.cap)
+            leg_ms = pl["total_ms"] / max(pl["launches"], 1)
+            leg_flops = 2.0 * rows6 * (2 * w.kv_row * w.n_layer) * H
+            tpeak, tpeak_kind = _tensor_peak()
             prod_obj["legacy_recompute"] = {
                 "value": 1000.0 / ms_leg * world, "unit": UNIT, "ms_per_step": ms_leg,
-                "steps": n6 - min(W, n6), "rows_per_step": min(int(P.plan[1][0][0]), w.cap),
-                "produce_ms": pl["total_ms"] / max(pl["launches"], 1),
+                "steps": n6 - min(W, n6), "rows_per_step": rows6,
+                "produce_ms": leg_ms,
+                "roofline": {"bound": "tensor", "achieved": leg_flops / (leg_ms * 1e-3) / 1e12,
+                             "peak": tpeak, "unit": "TFLOP/s",
+                             "frac": leg_flops / (leg_ms * 1e-3) / 1e12 / tpeak,
+                             "kernel": "k_produce_tc (tcgen05, accumulators in tensor memory)",
+                             "flops_per_launch": leg_flops,
+                             "peak_source": f"{tpeak_kind} bf16_tflops (burst; F16 has the same "
+                                            "nominal dense rate)",
+                             "timing": "CUDA events around each launch, launches serialised"},
                 "api": "ring_recompute_window + ring_attend per layer (page section 1.6 fallback)"}
         # ---- pass 7: the whole draft step (ring_draft_step): the producer, the begin-step
         # kernel, then per layer the noise-block Q/K/V projections of its hidden states and

@@ -22,7 +22,7 @@ LIB_NAME = "libdflash_ring.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 
 SOURCES = ["ring_host.cu", "ring_kernels.cu", "attn_kernels.cu", "step_kernels.cu",
-           "static_attend.cu", "produce_kernels.cu"]
+           "static_attend.cu", "produce_kernels.cu", "produce_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -373,6 +373,7 @@ int ring_init_ex(ring_t **out, const ring_params *p) {
     r->sms = sms;
     e = attend_kernels_init();
     if (e == cudaSuccess) e = produce_kernels_init();
+    if (e == cudaSuccess) e = produce_tc_init();
     if (e != cudaSuccess) {
         int rc = cuda_fail(nullptr, e, "ring_init: kernel attributes");
         delete r;
@@ -855,12 +856,31 @@ int begin_step_features(ring_t *r, const char *who, const int64_t *committed, co
     if (rc != RING_OK) return rc;
     cudaError_t e = cudaSuccess;
     const bool produce = m_total > 0 || noise;
-    if (produce) {
+    // Many rows in one contiguous run of features: the context rows go to the tensor-core
+    // kernel (a dense contraction), the noise rows (if any) to the streaming kernel after it.
+    int64_t frow_base = -1;
+    bool tc = m_total >= kProduceTcMinRows;
+    for (int s = 0; s < d.n_seq && tc; ++s) {
+        if (st[s].n_new == 0) continue;
+        const int64_t b = st[s].src_row - st[s].prod_base;
+        if (frow_base < 0) frow_base = b;
+        tc = b == frow_base;
+    }
+    if (tc) {
+        CUtensorMap tm_feat128{};
+        if (!encode_weight_map(&tm_feat128, feat, r->hidden, n_rows, 128))
+            return fail(r, RING_ECUDA, "%s: cuTensorMapEncodeTiled failed", who);
+        e = timed(r, 5, cs, [&] {
+            return launch_produce_tc(d, r->m, &r->tm_w, &tm_feat128, r->hidden, m_total, frow_base,
+                                     r->out_heads, r->k_norm, r->eps, ps, r->sms, !r->profiling, cs);
+        });
+    }
+    if (e == cudaSuccess && ((m_total > 0 && !tc) || noise)) {
         ProduceLaunch L{};
         const uint16_t *in[2] = {nullptr, nullptr};
         const CUtensorMap *tm[2] = {nullptr, nullptr};
         int64_t units = 0;
-        if (m_total > 0) {
+        if (m_total > 0 && !tc) {
             L.job[L.n_jobs] = ProduceJob{0, 0, m_total, produce_units(d, 0, m_total, r->out_heads)};
             in[L.n_jobs] = static_cast<const uint16_t *>(feat);
             tm[L.n_jobs] = &tm_feat;

@@ -266,6 +266,17 @@ cudaError_t launch_produce(const RingDims &d, const RingDev &m, const CUtensorMa
                            const ProduceSeqs &seqs, const NoiseOut &nout, bool pdl, int resident,
                            cudaStream_t st);
 
+// ---- tensor-core producer (produce_tc.cu): context rows of steps with many new rows ----
+// Used from kProduceTcMinRows rows on, when packed row mr is feature row frow_base + mr
+// for every new row (one contiguous run).  tm_feat: 2-D TMA map over the features with
+// 64 x 128 boxes, 128-byte swizzle.  Same outputs as launch_produce in mode 0.
+constexpr int64_t kProduceTcMinRows = 256;
+cudaError_t produce_tc_init();        // per device, before the first launch
+cudaError_t launch_produce_tc(const RingDims &d, const RingDev &m, const CUtensorMap *tm_w,
+                              const CUtensorMap *tm_feat, int hidden, int64_t m_total,
+                              int64_t frow_base, int out_heads, const float *k_norm, float eps,
+                              const ProduceSeqs &seqs, int sms, bool pdl, cudaStream_t st);
+
 // ---- shared host helpers (ring_host.cu) ----
 // 3-D TMA map over F16 K or V laid out [n_seq * n_layer * n_head_kv][kv_total][head_dim],
 // 64 x 64 boxes, 128-byte swizzle.

@@ -297,6 +297,30 @@ def test_small_rings_full_state(hidden):
         run.close()
 
 
+@pytest.mark.parametrize("hidden,kv_format", [(256, "f16"), (320, "f16"), (256, "q8_0")])
+def test_many_rows_on_the_tensor_core_path(hidden, kv_format):
+    """Steps of 256 rows and more in one contiguous run of features go to the tcgen05
+    kernel (128-row tiles, accumulators in tensor memory): a partial last tile, two
+    sequences packed in one run, a whole-ring jump; every slot of every layer against the
+    float64 oracle within the float32-accumulation bound, state bit-exact, attention."""
+    w = synth.workload(1, cap=1024, n_layer=2, n_seq=2, swa_window=300)
+    run = ProducerRun(w, hidden, kv_format=kv_format)
+    try:
+        for t, c in enumerate([[300, 0], [301, 500], [1400, 700], [1401, 2900]]):
+            run.begin_step(c)
+            run.check_state()
+            for s in range(w.n_seq):
+                for layer in range(w.n_layer):
+                    run.check_kv(s, layer)
+            if kv_format == "f16":
+                o = run.attend(t, t % 2, "full")
+                for s in range(w.n_seq):
+                    assert_close(o[s], run.expected(t, t % 2, "full", s), f"step {t} seq {s}")
+        assert run.ring.device_error() == 0
+    finally:
+        run.close()
+
+
 def test_steady_decode_full_size():
     """cap 4096, 5 layers, hidden 4096: an 8192-row prefill (bulk) then decode steps of
     the acceptance histogram; sampled slots of every layer and sampled heads of the
