@@ -42,20 +42,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 33_012_480, "kernel": "765c8f8a2d59ca89",
+    "steady_decode_cap4096_s1_l5": {"bytes": 32_968_320, "kernel": "11ac1dd0d1d6f96d",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
-    # captured on 4 of the 16 sequences (538,197,760 B read + 17,878,528 B written per
+    # captured on 4 of the 16 sequences (538,208,000 B read + 15,361,024 B written per
     # launch) and scaled by the sequences a launch processes: every sequence's visible rows
     # are read once, so the traffic grows in proportion
-    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_197_760 + 17_878_528), "kernel": "765c8f8a2d59ca89",
+    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_208_000 + 15_361_024), "kernel": "11ac1dd0d1d6f96d",
                                    "source": "profiles/attend_plain_large_cap32768_s4_l5.md"},
 }
-
-
-# the same for the context-row producer kernel (workload: steady decode, hidden 4096)
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the producer kernels, keyed as
+# above (kernel = sha256[:16] of produce_kernels.cu or produce_tc.cu)
 PRODUCE_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 85_043_500, "kernel": "4be0a7000c1f4369",
+    "steady_decode_cap4096_s1_l5": {"bytes": 86_053_504, "kernel": "cfabead887c1fc63",
                                     "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
+    # the tensor-core kernel (produce_tc.cu) on the legacy recompute's 4096 rows
+    "steady_decode_cap4096_s1_l5_legacy": {"bytes": 181_065_984, "kernel": "bbb910017f056830",
+                                           "source": "profiles/produce_tc_legacy_recompute_cap4096_s1_l5.md"},
 }
 
 
@@ -596,11 +598,14 @@ def run_gb300(args):
 
             n6 = min(K + W, 100)
             ring = prod_ring()
+            ring.clock_enable(True)
             sb.timed_loop(ring, step_legacy, 1, min(W, n6))
             torch.cuda.synchronize()
+            ring.clock_read("produce")                  # forget the warm-up launches
             evs = sb.timed_loop(ring, step_legacy, 1 + min(W, n6), n6 - min(W, n6))
             torch.cuda.synchronize()
             ms_leg = max_over_ranks(sb.ms_of(evs), dist, dev) / max(1, n6 - min(W, n6))
+            lclk_ms, lclk_n = ring.clock_read("produce")
             assert ring.device_error() == 0
             ring.close()
             ring = prod_ring()                 # a fresh ring: committed never goes back
@@ -610,13 +615,15 @@ def run_gb300(args):
             pl = R.ring_profile_read(ring.h)["produce"]
             ring.close()
             rows6 = min(int(P.plan[1][0][0]), w.cap)
-            leg_ms = pl["total_ms"] / max(pl["launches"], 1)
+            leg_ms_isolated = pl["total_ms"] / max(pl["launches"], 1)
+            leg_ms = lclk_ms / max(lclk_n, 1)
             leg_flops = 2.0 * rows6 * (2 * w.kv_row * w.n_layer) * H
+            ltr = PRODUCE_TRAFFIC.get(w.name + "_legacy" + ("_q8_0" if q8 else ""))
             tpeak, tpeak_kind = _tensor_peak()
             prod_obj["legacy_recompute"] = {
                 "value": 1000.0 / ms_leg * world, "unit": UNIT, "ms_per_step": ms_leg,
                 "steps": n6 - min(W, n6), "rows_per_step": rows6,
-                "produce_ms": leg_ms,
+                "produce_ms": leg_ms, "produce_ms_isolated": leg_ms_isolated,
                 "roofline": {"bound": "tensor", "achieved": leg_flops / (leg_ms * 1e-3) / 1e12,
                              "peak": tpeak, "unit": "TFLOP/s",
                              "frac": leg_flops / (leg_ms * 1e-3) / 1e12 / tpeak,
@@ -624,7 +631,12 @@ def run_gb300(args):
                              "flops_per_launch": leg_flops,
                              "peak_source": f"{tpeak_kind} bf16_tflops (burst; F16 has the same "
                                             "nominal dense rate)",
-                             "timing": "CUDA events around each launch, launches serialised"},
+                             "traffic": (ltr["bytes"] if ltr and H == 4096 and ltr.get("kernel") ==
+                                         _kernel_source_hash("produce_tc.cu") else None),
+                             "timing": "device clock of every producer launch inside the timed "
+                                       "steps (earliest CTA past its grid dependency to the "
+                                       "last CTA's exit)",
+                             "frac_isolated": leg_flops / (leg_ms_isolated * 1e-3) / 1e12 / tpeak},
                 "api": "ring_recompute_window + ring_attend per layer (page section 1.6 fallback)"}
         # ---- pass 7: the whole draft step (ring_draft_step): the producer, the begin-step
         # kernel, then per layer the noise-block Q/K/V projections of its hidden states and
