@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the producer kernels, keyed as
 # above (kernel = sha256[:16] of produce_kernels.cu or produce_tc.cu)
 PRODUCE_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 86_053_504, "kernel": "cfabead887c1fc63",
+    "steady_decode_cap4096_s1_l5": {"bytes": 84_903_552, "kernel": "be211e23fd4180a7",
                                     "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
     # the tensor-core kernel (produce_tc.cu) on the legacy recompute's 4096 rows
     "steady_decode_cap4096_s1_l5_legacy": {"bytes": 181_065_984, "kernel": "bbb910017f056830",

@@ -298,14 +298,17 @@ k_produce(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUte
             if (lane == 0) mbar_arrive(bar0 + 8 * (kPStages + stg));
         }
         // partial tile -> the receive buffer of the CTA owning each row:
-        // recv[src rank][local row][128]
+        // recv[src rank][local row][128]; only the tile's rows that hold a new row (a
+        // prefix: rows are packed) -- a decode step fills a few of the 32
         if (ks > 1) cluster_wait();
         const int g = lane >> 2, c = lane & 3;
+        const int64_t n_rows_tile = m_total - tile * kPM;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int h8 = 0; h8 < 2; ++h8) {
                 const int r = mt * 16 + g + 8 * h8;
+                if (r >= n_rows_tile) continue;
                 const int owner = r / rows_per, lr = r - owner * rows_per;
                 float *row = recv + ((int64_t)rank * rows_per + lr) * kPN;
 #pragma unroll
