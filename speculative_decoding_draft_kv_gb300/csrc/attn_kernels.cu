@@ -30,6 +30,14 @@
 namespace dflash {
 namespace {
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error below 2^-22, results
+// under 2^-126 flushed to zero), for the probabilities, which are rounded to F16 next
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 constexpr int kTileBytes = kTile * kHeadDim * 2;   // one 64-slot tile of one head, K or V
 constexpr int kHalfBox = kTileBytes / 2;           // TMA box: 64 slots x 64 columns
 constexpr int kStageBytes = 2 * kTileBytes;        // K + V
@@ -51,6 +59,12 @@ struct Shape {
     static constexpr int kNT = kKeys / 8;           // n-tiles of S per warp
     static constexpr int kKK = kKeys / 16;          // k-steps of P V per warp
     static constexpr int kMinBlocks = CLUSTER ? 1 : 2;
+    // how far (log2) a row maximum may outgrow the softmax reference before O and l are
+    // rescaled (P stays within [0, 2^kLazyLog2]): the latency- and issue-bound instances
+    // skip most rescales; the HBM-bound plain F16 instance keeps the plain online softmax
+    // (exact running maximum), which it runs with fewer registers
+    static constexpr bool kLazy = CLUSTER || Q8;
+    static constexpr float kLazyLog2 = 8.f;
     // q8_0 slots: a stage holds a tile's K and V codes (two 128 x 64-byte TMA boxes) and
     // their scales (2 x 512 bytes); the consumers turn codes into F16 MMA operands in
     // registers, so a stage costs 17 KiB instead of 32 and five (plain) or ten (cluster)
@@ -177,7 +191,25 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         };
         bool noise_ready = false;
         int it = 0;
-        int t = t0;
+        // visible tiles of this split in order, 32 flags per load: `pt` is the next tile
+        // not yet issued (-1 past the end), `pflag` its flag
+        int cbase = t0, pt = -1, pflag = 0;
+        uint32_t vis = 0u, part = 0u;
+        auto advance = [&]() {
+            pt = -1;
+            while (vis == 0u) {
+                if (cbase >= t1) return;
+                const int u = cbase + lane;
+                const int f = u < t1 ? (int)flags[u] : 0;
+                vis = __ballot_sync(0xffffffffu, f != 0);
+                part = __ballot_sync(0xffffffffu, f == 2);
+                cbase += 32;
+            }
+            const int bit = __ffs(vis) - 1;
+            vis &= vis - 1u;
+            pt = cbase - 32 + bit;
+            pflag = ((part >> bit) & 1u) ? 2 : 1;
+        };
         {
             // L2 prefetch of this CTA's query rows, the step's RoPE table and the noise
             // rows: a hint only (L2 is coherent), so it is safe whatever runs before
@@ -202,22 +234,21 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             // tiles, flags or bits, so the first stages can be filled before the grid
             // dependency resolves.  The host never asks for this right after begin_step.
             // A tile holding noise slots is not touched before the noise rows are written.
-            for (; t < t1 && it < kStages; ++t) {
-                const int flag = flags[t];
-                if (flag == 0) continue;
-                if (t >= tn0 && t <= tn1) break;
-                if (lane == 0) issue(it, t, flag);
+            advance();
+            while (pt >= 0 && it < kStages && !(pt >= tn0 && pt <= tn1)) {
+                if (lane == 0) issue(it, pt, pflag);
                 __syncwarp();
                 ++it;
+                advance();
             }
         }
         pdl_wait();
         // A grid that fits in one wave lets the next kernel's CTAs settle onto idle SMs
         // now; a multi-wave grid must not, or they would take slots its own later CTAs need.
         if (d.single_wave) pdl_trigger();
-        for (; t < t1; ++t) {
-            const int flag = flags[t];
-            if (flag == 0) continue;
+        if (!(early & kAttendPreload)) advance();
+        for (; pt >= 0; advance()) {
+            const int t = pt, flag = pflag;
             if (!noise_ready && t >= tn0 && t <= tn1) {
                 __syncwarp();
                 bar_sync(2, SH::kThreads);
@@ -285,6 +316,9 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         pdl_wait();
         if (d.single_wave) pdl_trigger();
         if (threadIdx.x == 0 && m.clock) clk_slot = clock_start(m.clock, kClockAttend, layer);
+        // clusters: the split's first 32 tile flags, loaded now so that the load overlaps
+        // the query prologue's
+        const int f_first = CLUSTER && t0 + lane < t1 ? (int)flags[t0 + lane] : 0;
         const int tid = threadIdx.x;
         const int half = kHeadDim / 2;
         const float2 *csq = m.rope32 + (int64_t)s * d.q_len * half;
@@ -460,8 +494,9 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
         // Visible tiles of this split, 32 at a time: one flags load per chunk, then the
         // set bits of two warp ballots (any visible / partly visible) give the tiles.
-        int cbase = t0;
-        uint32_t vis = 0u, part = 0u;
+        int cbase = CLUSTER ? t0 + 32 : t0;
+        uint32_t vis = CLUSTER ? __ballot_sync(0xffffffffu, f_first != 0) : 0u;
+        uint32_t part = CLUSTER ? __ballot_sync(0xffffffffu, f_first == 2) : 0u;
         auto next_tile = [&](int &t, int &flag) -> bool {
             while (vis == 0u) {
                 if (cbase >= t1) return false;
@@ -487,8 +522,9 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             return false;
         };
         // S = Q K^T over this warp's keys of stage stg (F16 K tile at sk, or q8_0 codes and
-        // scales), scaled to the log2 domain and masked by the stage's per-row visibility
-        // bits when flag == 2.  nvalid: slots of the tile below kv_total.
+        // scales), masked by the stage's per-row visibility bits when flag == 2 and, in the
+        // plain online softmax, scaled to the log2 domain (the lazy one applies the scale in
+        // the exponent).  nvalid: slots of the tile below kv_total.
         auto qk = [&](uint32_t sk, int flag, int stg, int nvalid, float (&sc)[SH::kNT][4]) {
 #pragma unroll
             for (int n = 0; n < SH::kNT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
@@ -555,10 +591,12 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     }
                 }
             }
+            if constexpr (!SH::kLazy) {
 #pragma unroll
-            for (int n = 0; n < SH::kNT; ++n)
+                for (int n = 0; n < SH::kNT; ++n)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[n][e] *= scale_log2;
+                    for (int e = 0; e < 4; ++e) sc[n][e] *= scale_log2;
+            }
             if (flag == 2) {
                 const uint64_t w0 = sbits[stg * kMaxQWords + i0];
                 const uint64_t w1 = sbits[stg * kMaxQWords + i1];
@@ -574,9 +612,14 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         };
         // online softmax (log2 domain) of rows r0 (j = 0) and r1 (j = 1), then O += P V
         // over the same keys of stage stg (F16 V tile at sv, or q8_0 codes and scales);
-        // then the stage barrier `release` hands the stage back to the producer
+        // then the stage barrier `release` hands the stage back to the producer.
+        // The reference maximum mrow may move lazily: P = 2^(scale S - mrow) may reach
+        // 2^kLazyLog2 (exact in F16), and O and l are rescaled only when some row of the
+        // warp outgrows its reference by more than that -- rarely after a row's first
+        // visible tile.  O / l does not depend on the reference.
         auto softmax_pv = [&](uint32_t sv, uint32_t release, int stg, int nvalid,
                               float (&sc)[SH::kNT][4]) {
+          if constexpr (!SH::kLazy) {
             float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -610,6 +653,51 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     oacc[n][3] *= alpha[1];
                 }
             }
+          } else {
+            float mx[2];
+            bool move = false;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float x = -INFINITY;
+#pragma unroll
+                for (int n = 0; n < SH::kNT; ++n) x = fmaxf(x, fmaxf(sc[n][2 * j], sc[n][2 * j + 1]));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+                mx[j] = x * scale_log2;
+                move |= mx[j] > mrow[j] + SH::kLazyLog2;
+            }
+            if (__any_sync(0xffffffffu, move)) {
+                float alpha[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float mnew = fmaxf(mrow[j], mx[j]);
+                    alpha[j] = mnew == -INFINITY ? 1.f : exp2f(mrow[j] - mnew);
+                    mrow[j] = mnew;
+                    lrow[j] *= alpha[j];
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    oacc[n][0] *= alpha[0];
+                    oacc[n][1] *= alpha[0];
+                    oacc[n][2] *= alpha[1];
+                    oacc[n][3] *= alpha[1];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float muse = mrow[j] == -INFINITY ? 0.f : mrow[j];
+                float rs = 0.f;
+#pragma unroll
+                for (int n = 0; n < SH::kNT; ++n) {
+                    const float p0 = ex2_fast(fmaf(sc[n][2 * j], scale_log2, -muse));
+                    const float p1 = ex2_fast(fmaf(sc[n][2 * j + 1], scale_log2, -muse));
+                    sc[n][2 * j] = p0;
+                    sc[n][2 * j + 1] = p1;
+                    rs += p0 + p1;
+                }
+                lrow[j] += rs;
+            }
+          }
 #pragma unroll
             for (int kk = 0; kk < SH::kKK; ++kk) {
                 uint32_t pa[4];
