@@ -42,12 +42,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
 # from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 33_138_176, "kernel": "806fb402e0bd3e1f",
+    "steady_decode_cap4096_s1_l5": {"bytes": 33_856_128, "kernel": "28aefb00f82ddd23",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
-    # captured on 4 of the 16 sequences (538,212,608 B read + 15,369,216 B written per
+    # captured on 4 of the 16 sequences (538,202,368 B read + 14,991,872 B written per
     # launch) and scaled by the sequences a launch processes: every sequence's visible rows
     # are read once, so the traffic grows in proportion
-    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_212_608 + 15_369_216), "kernel": "806fb402e0bd3e1f",
+    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_202_368 + 14_991_872), "kernel": "28aefb00f82ddd23",
                                    "source": "profiles/attend_plain_large_cap32768_s4_l5.md"},
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the producer kernels, keyed as

@@ -770,75 +770,88 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             cluster_wait();     // every CTA of the cluster has started (see cluster_arrive_relaxed)
             // Merge the key slices of each row block inside this CTA, then push one partial
             // per row to the CTA of the cluster that finishes that row.  Every warp first
-            // publishes its partial (in the idle stage buffers); warp (mb, ksl) then merges
+            // publishes its partial (in the idle stage buffers: per lane one float4 per
+            // n-tile, then (max r0, max r1, sum r0, sum r1)); warp (mb, ksl) then merges
             // columns [32 ksl, 32 ksl + 32) of its row block and pushes them.
             bar_sync(1, SH::kConsumers);
-            float *xs = reinterpret_cast<float *>(smem);
+            constexpr int kX4 = 17 * 32;                  // float4 per warp partial
+            float4 *xs4 = reinterpret_cast<float4 *>(smem);
             {
-                float *x = xs + (mb * SH::kSlices + ksl) * SH::kXPer;
+                float4 *x = xs4 + (mb * SH::kSlices + ksl) * kX4;
 #pragma unroll
                 for (int n = 0; n < 16; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) x[(n * 4 + e) * 32 + lane] = oacc[n][e];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    x[(64 + j) * 32 + lane] = mrow[j];
-                    x[(66 + j) * 32 + lane] = lrow[j];
-                }
+                    x[n * 32 + lane] = make_float4(oacc[n][0], oacc[n][1], oacc[n][2], oacc[n][3]);
+                x[16 * 32 + lane] = make_float4(mrow[0], mrow[1], lrow[0], lrow[1]);
             }
             bar_sync(1, SH::kConsumers);
+            const float4 *xb = xs4 + mb * SH::kSlices * kX4;
+            float wk[2][SH::kSlices], mm[2], ll[2];
+            {
+                float4 ml[SH::kSlices];
+#pragma unroll
+                for (int k = 0; k < SH::kSlices; ++k) ml[k] = xb[k * kX4 + 16 * 32 + lane];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < SH::kSlices; ++k) m = fmaxf(m, j ? ml[k].y : ml[k].x);
+                    const float muse = m == -INFINITY ? 0.f : m;
+                    float l = 0.f;
+#pragma unroll
+                    for (int k = 0; k < SH::kSlices; ++k) {
+                        wk[j][k] = exp2f((j ? ml[k].y : ml[k].x) - muse);
+                        l += wk[j][k] * (j ? ml[k].w : ml[k].z);
+                    }
+                    mm[j] = m;
+                    ll[j] = l;
+                }
+            }
             const int rr[2] = {r0, r1};
+            uint32_t a_row[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                float wk[SH::kSlices];
-                float mm = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < SH::kSlices; ++k)
-                    mm = fmaxf(mm, xs[(mb * SH::kSlices + k) * SH::kXPer + (64 + j) * 32 + lane]);
-                const float muse = mm == -INFINITY ? 0.f : mm;
-                float ll = 0.f;
-#pragma unroll
-                for (int k = 0; k < SH::kSlices; ++k) {
-                    const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
-                    wk[k] = exp2f(x[(64 + j) * 32 + lane] - muse);
-                    ll += wk[k] * x[(66 + j) * 32 + lane];
-                }
                 const int r = rr[j];
                 const int owner = r * (int)nct / kRows, lr = r - cluster_first_row(owner, (int)nct);
-                float *acc_row = recv_acc + ((int64_t)rank * rmax + lr) * kHeadDim;
-                const uint32_t a_row = map_rank(smem_u32(acc_row), (uint32_t)owner);
-                if constexpr (Q8) {
-                    // n-tiles 2q / 2q+1 hold the even / odd dimensions of 16q .. 16q+15
-#pragma unroll
-                    for (int qq = 0; qq < 8 / SH::kSlices; ++qq) {
-                        const int q = ksl * (8 / SH::kSlices) + qq;
-                        float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int k = 0; k < SH::kSlices; ++k) {
-                            const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                v[e] += wk[k] * x[((2 * q + (e & 1)) * 4 + 2 * j + (e >> 1)) * 32 + lane];
-                        }
-                        st_cluster_v4(a_row + 4u * (16 * q + 4 * c), v[0], v[1], v[2], v[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int nn = 0; nn < 16 / SH::kSlices; ++nn) {
-                        const int n = ksl * (16 / SH::kSlices) + nn;
-                        float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-                        for (int k = 0; k < SH::kSlices; ++k) {
-                            const float *x = xs + (mb * SH::kSlices + k) * SH::kXPer;
-                            v0 += wk[k] * x[(n * 4 + 2 * j) * 32 + lane];
-                            v1 += wk[k] * x[(n * 4 + 2 * j + 1) * 32 + lane];
-                        }
-                        st_cluster_v2(a_row + 4u * (n * 8 + 2 * c), v0, v1);
-                    }
-                }
+                a_row[j] = map_rank(smem_u32(recv_acc + ((int64_t)rank * rmax + lr) * kHeadDim), (uint32_t)owner);
                 if (ksl == 0 && c == 0)
                     st_cluster_v2(map_rank(smem_u32(recv_ml + (int)rank * rmax + lr), (uint32_t)owner),
-                                  mm, ll);
+                                  mm[j], ll[j]);
+            }
+            if constexpr (Q8) {
+                // n-tiles 2q / 2q+1 hold the even / odd dimensions of 16q .. 16q+15
+#pragma unroll
+                for (int qq = 0; qq < 8 / SH::kSlices; ++qq) {
+                    const int q = ksl * (8 / SH::kSlices) + qq;
+                    float v[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int k = 0; k < SH::kSlices; ++k) {
+                        const float4 a = xb[k * kX4 + (2 * q) * 32 + lane];
+                        const float4 b = xb[k * kX4 + (2 * q + 1) * 32 + lane];
+                        v[0][0] += wk[0][k] * a.x; v[0][1] += wk[0][k] * b.x;
+                        v[0][2] += wk[0][k] * a.y; v[0][3] += wk[0][k] * b.y;
+                        v[1][0] += wk[1][k] * a.z; v[1][1] += wk[1][k] * b.z;
+                        v[1][2] += wk[1][k] * a.w; v[1][3] += wk[1][k] * b.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        st_cluster_v4(a_row[j] + 4u * (16 * q + 4 * c), v[j][0], v[j][1], v[j][2], v[j][3]);
+                }
+            } else {
+#pragma unroll
+                for (int nn = 0; nn < 16 / SH::kSlices; ++nn) {
+                    const int n = ksl * (16 / SH::kSlices) + nn;
+                    float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < SH::kSlices; ++k) {
+                        const float4 a = xb[k * kX4 + n * 32 + lane];
+                        v[0] += wk[0][k] * a.x;
+                        v[1] += wk[0][k] * a.y;
+                        v[2] += wk[1][k] * a.z;
+                        v[3] += wk[1][k] * a.w;
+                    }
+                    st_cluster_v2(a_row[0] + 4u * (n * 8 + 2 * c), v[0], v[1]);
+                    st_cluster_v2(a_row[1] + 4u * (n * 8 + 2 * c), v[2], v[3]);
+                }
             }
         } else {
             // merge the two key halves through stage buffer 0 (idle now), then write this
@@ -939,17 +952,23 @@ k_attend(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const int n_part = (int)nct;
     const int row0 = cluster_first_row((int)rank, n_part);
     const int items = (min(kRows, cluster_first_row((int)rank + 1, n_part)) - row0) * (kHeadDim / 4);
+    // one warp per row (items: 32 per row): lane p < n_part reads partial p's (max, sum)
+    // and its weight; the warp's lanes then add the weighted numerators of their 4 columns
     for (int u = threadIdx.x; u < items; u += SH::kThreads) {
         const int lr = u / (kHeadDim / 4), c4 = (u % (kHeadDim / 4)) * 4;
-        float mm = -INFINITY;
-        for (int p = 0; p < n_part; ++p) mm = fmaxf(mm, recv_ml[p * rmax + lr].x);
+        const float2 ml = lane < n_part ? recv_ml[lane * rmax + lr] : make_float2(-INFINITY, 0.f);
+        float mm = ml.x;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
         const float muse = mm == -INFINITY ? 0.f : mm;
-        float l = 0.f;
+        const float wp = lane < n_part ? exp2f(ml.x - muse) : 0.f;
+        float l = wp * ml.y;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int p = 0; p < n_part; ++p) {
-            const float2 ml = recv_ml[p * rmax + lr];
-            const float w = exp2f(ml.x - muse);
-            l += w * ml.y;
+            const float w = __shfl_sync(0xffffffffu, wp, p);
             const float4 v = *reinterpret_cast<const float4 *>(recv_acc + ((int64_t)p * rmax + lr) * kHeadDim + c4);
             acc.x += w * v.x;
             acc.y += w * v.y;
