@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -40,31 +41,40 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the split-KV attention kernel,
-# from one ncu capture, keyed by workload; valid only for the kernel source it was taken on.
+# from one ncu capture, keyed by workload; valid only for the kernel code it was taken on
+# (kernel = _code_hash of attn_kernels.cu: sha256[:16] without comments and whitespace).
 NCU_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 33_856_128, "kernel": "28aefb00f82ddd23",
+    "steady_decode_cap4096_s1_l5": {"bytes": 33_856_128, "kernel": "2ee0f6a3f6510f19",
                                     "source": "profiles/attend_cluster_steady_decode_cap4096_s1_l5.md"},
     # captured on 4 of the 16 sequences (538,202,368 B read + 14,991,872 B written per
     # launch) and scaled by the sequences a launch processes: every sequence's visible rows
     # are read once, so the traffic grows in proportion
-    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_202_368 + 14_991_872), "kernel": "28aefb00f82ddd23",
+    "large_ring_cap32768_s16_l5": {"bytes": 4 * (538_202_368 + 14_991_872), "kernel": "2ee0f6a3f6510f19",
                                    "source": "profiles/attend_plain_large_cap32768_s4_l5.md"},
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the producer kernels, keyed as
-# above (kernel = sha256[:16] of produce_kernels.cu or produce_tc.cu)
+# above (kernel = _code_hash of produce_kernels.cu or produce_tc.cu)
 PRODUCE_TRAFFIC = {
-    "steady_decode_cap4096_s1_l5": {"bytes": 84_903_552, "kernel": "be211e23fd4180a7",
+    "steady_decode_cap4096_s1_l5": {"bytes": 84_903_552, "kernel": "1117b6f1d0ffc179",
                                     "source": "profiles/produce_steady_decode_cap4096_s1_l5.md"},
     # the tensor-core kernel (produce_tc.cu) on the legacy recompute's 4096 rows
-    "steady_decode_cap4096_s1_l5_legacy": {"bytes": 181_065_984, "kernel": "bbb910017f056830",
+    "steady_decode_cap4096_s1_l5_legacy": {"bytes": 181_065_984, "kernel": "c446e1838298dba4",
                                            "source": "profiles/produce_tc_legacy_recompute_cap4096_s1_l5.md"},
 }
 
 
+def _code_hash(text: str) -> str:
+    """sha256[:16] of a CUDA source's code: comments and whitespace removed, so that a
+    change to the comments alone leaves a capture of the kernel valid."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
 def _kernel_source_hash(name: str = "attn_kernels.cu") -> str:
     p = os.path.join(ROOT, "speculative_decoding_draft_kv_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(p) as f:
+        return _code_hash(f.read())
 
 
 def _peaks():

@@ -7,7 +7,8 @@
 // warp issues the copies (plus a 16-byte-aligned bulk copy of the tile's per-row
 // visibility bits when the tile is only partly visible); the consumer warps compute
 // S = Q K^T and O += P V on the F16 tensor cores (m16n8k16, F32 accumulation) with an
-// online softmax in F32 registers.  All 32 query rows that share a kv head (4 heads x 8
+// online softmax in F32 registers (its reference maximum moved lazily where the kernel is
+// bound by instruction issue).  All 32 query rows that share a kv head (4 heads x 8
 // queries) ride in one CTA, so each K/V byte is read from HBM once per step and layer.
 // Tiles whose flag says "no visible slot" are never fetched.
 //
@@ -16,10 +17,11 @@
 //     warps, two CTAs per SM; each CTA writes a partial softmax state and a combine
 //     kernel merges them (unless a pair has a single CTA);
 //   * few pairs -- one wave of thread-block clusters, 8 consumer warps per CTA (one CTA
-//     per SM, so per-tile latency halves); every warp pushes its partial state into the
-//     shared memory of the CTA that owns its rows (distributed shared memory stores),
-//     and after one cluster barrier each CTA finishes 32 / cluster rows locally.
-// q8_0 slots (int8 codes + one F16 scale per 32 values) take the first shape with 17 KiB
+//     per SM, so per-tile latency halves); the warps' key slices are merged in shared
+//     memory, each row's CTA state is pushed into the shared memory of the CTA that owns
+//     the row (distributed shared memory stores), and after one cluster barrier each CTA
+//     finishes 32 / cluster rows locally.
+// q8_0 slots (int8 codes + one F16 scale per 32 values) take either shape with 17 KiB
 // stages of codes and scales; the consumers turn the codes straight into F16 MMA operands
 // in registers (no second pass through shared memory).
 #include "ring_internal.h"
@@ -101,10 +103,12 @@ struct Shape {
 //              producer already streams the context tiles.
 //   main loop  consumer warp w owns query rows 16*(w & 1) .. +16 and key slice (w >> 1)
 //              of every 64-slot tile: S = Q K^T, online softmax, O += P V.
-//   merge      each warp stores its rows' (max, sum, numerators) into the receive buffer
-//              of the CTA that finishes those rows (itself without a cluster); after one
-//              barrier that CTA merges the kSlices * cluster partial states of its rows
-//              and writes O (or a group partial for the combine kernel).
+//   merge      without a cluster the two key halves merge in shared memory and the CTA
+//              writes O (or its partial for the combine kernel); in a cluster the key
+//              slices merge in shared memory, each row's CTA state goes to the receive
+//              buffer of the CTA that finishes the row, and after one cluster barrier that
+//              CTA merges the cluster's states of its rows and writes O (or a group
+//              partial for the combine kernel).
 // ---------------------------------------------------------------------------------
 template <bool CLUSTER, bool Q8>
 __global__ void __launch_bounds__(Shape<CLUSTER, Q8>::kThreads, Shape<CLUSTER, Q8>::kMinBlocks)

@@ -53,3 +53,21 @@ def test_tile_flags_of_a_mask():
     np.testing.assert_array_equal(bench._tile_flags(m, 64), [1, 2, 2])
     m[0, 70] = inf
     np.testing.assert_array_equal(bench._tile_flags(m, 64), [1, 0, 2])
+
+
+def test_code_hash_ignores_comments_and_whitespace_only():
+    src = "__global__ void k(int *p) {\n    p[0] = 1;  // one\n}\n"
+    same = "/* a kernel */\n__global__  void k(int *p)\n{ p[0] = 1; }\n// end\n"
+    other = "__global__ void k(int *p) {\n    p[0] = 2;  // one\n}\n"
+    assert bench._code_hash(src) == bench._code_hash(same)
+    assert bench._code_hash(src) != bench._code_hash(other)
+
+
+def test_recorded_traffic_matches_the_current_kernel_code():
+    # the committed captures were taken on the kernels as they stand
+    for rec in bench.NCU_TRAFFIC.values():
+        assert rec["kernel"] == bench._kernel_source_hash("attn_kernels.cu")
+    assert bench.PRODUCE_TRAFFIC["steady_decode_cap4096_s1_l5"]["kernel"] == \
+        bench._kernel_source_hash("produce_kernels.cu")
+    assert bench.PRODUCE_TRAFFIC["steady_decode_cap4096_s1_l5_legacy"]["kernel"] == \
+        bench._kernel_source_hash("produce_tc.cu")
